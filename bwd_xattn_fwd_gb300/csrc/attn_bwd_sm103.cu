@@ -1,0 +1,523 @@
+// Backward of fused causal attention with grouped KV heads on sm_103a tensor cores.
+//
+// Method (xtrain "演进总览" / docs/evolution.md, phase table row T14): recompute the
+// scores from Q, K and the saved log-sum-exp, use D_i = dO_i . O_i in place of the
+// softmax Jacobian, and produce dQ, dK, dV. Row T15: the gradient of a kv head is the
+// sum over its query group, taken deterministically without atomics.
+//
+// Three kernels, in stream order:
+//   1. preprocess (HBM-bound): D_i = sum_d dO_id O_id in fp32, the log2-domain LSE
+//      rows laid out [B, nh, S_pad], and a zeroed fp32 dQ accumulator.
+//   2. main (tensor cores). One CTA per (batch, kv head, 128-row key tile n). The K_n
+//      and V_n tiles stay in shared memory; the dK_n / dV_n accumulators stay in TMEM
+//      while the CTA walks every query head r of the group and every query tile m >= n
+//      (causal tile skipping). That walk *is* the group sum of row T15: no atomics on
+//      dK/dV, and a fixed order, so they are reproducible. Per (r, m):
+//        S^T  = K_n Q_m^T               (TMEM, 128 x 128 fp32)
+//        dP^T = V_n dO_m^T              (TMEM, 128 x 128 fp32)
+//        P^T  = exp2(S^T scale log2e - LSE2_m)      -> bf16 into TMEM over S^T
+//        dS^T = scale * P^T (dP^T - D_m)            -> bf16 into TMEM over dP^T, and
+//                                                      into shared memory (MN-major)
+//        dV_n += P^T dO_m ,  dK_n += dS^T Q_m       (A operand from TMEM)
+//        dQ_m  = dS K_n                 (TMEM) -> fp32 atomic adds into the accumulator
+//      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 4-7 = P/dS (one thread per
+//      key row), 8-11 = dQ drain (one thread per query row).
+//   3. dq convert: dq = bf16(accumulator).
+#include "sm103_ptx.cuh"
+#include "xattn_internal.h"
+
+namespace xattn {
+
+size_t bwd_workspace_bytes(int B, int S, int nh, int hd) {
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t rows = static_cast<size_t>(B) * nh * padded_rows(S);
+  return up(rows * 4) * 2 + up(static_cast<size_t>(B) * S * nh * hd * 4);
+}
+
+BwdWorkspace bwd_workspace_carve(void *base, int B, int S, int nh, int hd) {
+  (void)hd;
+  auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+  const size_t rows = static_cast<size_t>(B) * nh * padded_rows(S);
+  uint8_t *p = static_cast<uint8_t *>(base);
+  BwdWorkspace ws;
+  ws.D = reinterpret_cast<float *>(p);
+  ws.lse2 = reinterpret_cast<float *>(p + up(rows * 4));
+  ws.dqacc = reinterpret_cast<float *>(p + 2 * up(rows * 4));
+  return ws;
+}
+
+namespace {
+
+// ------------------------------------------------------------------------------------
+// 1. preprocess
+// ------------------------------------------------------------------------------------
+// One group of (hd / 8) lanes per row (b, i, h): each lane reads 8 bf16 of O and dO
+// (16 B each), the group reduces with shuffles. Rows are enumerated in memory order of
+// O/dO, so the loads are fully coalesced. The same lanes zero the row of the dQ
+// accumulator. Pad rows (S <= i < S_pad) get D = 0 and LSE2 = +inf, so that the main
+// kernel's partial query tiles contribute exactly zero.
+template <int HD>
+__global__ void __launch_bounds__(256) bwd_preprocess_kernel(
+    const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dO,
+    const float *__restrict__ lse, float *__restrict__ D, float *__restrict__ lse2,
+    float *__restrict__ dqacc, int B, int S, int nh) {
+  constexpr int kLanesPerRow = HD / 8;
+  const int S_pad = padded_rows(S);
+  const long long n_rows = static_cast<long long>(B) * S * nh;
+  const long long n_pad = static_cast<long long>(B) * nh * (S_pad - S);
+  const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long row = tid / kLanesPerRow;
+  const int sub = static_cast<int>(tid % kLanesPerRow);
+  const bool is_row = row < n_rows;
+  float acc = 0.f;
+  if (is_row) {
+    const uint4 ov = *reinterpret_cast<const uint4 *>(o + row * HD + sub * 8);
+    const uint4 dv = *reinterpret_cast<const uint4 *>(dO + row * HD + sub * 8);
+    const uint32_t a[4] = {ov.x, ov.y, ov.z, ov.w};
+    const uint32_t c[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      acc = fmaf(bf16lo_to_f32(a[e]), bf16lo_to_f32(c[e]), acc);
+      acc = fmaf(bf16hi_to_f32(a[e]), bf16hi_to_f32(c[e]), acc);
+    }
+  }
+  // Every lane of the warp takes part in the reduction (a warp may straddle the end of
+  // the real rows); the lane groups are aligned, so no group mixes real and pad rows.
+#pragma unroll
+  for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (is_row) {
+    float4 *z = reinterpret_cast<float4 *>(dqacc + row * HD + sub * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sub == 0) {
+      const int h = static_cast<int>(row % nh);
+      const long long bi = row / nh;
+      const int i = static_cast<int>(bi % S);
+      const int b = static_cast<int>(bi / S);
+      const size_t dst = (static_cast<size_t>(b) * nh + h) * S_pad + i;
+      D[dst] = acc;
+      lse2[dst] = lse[row] * kLog2e;
+    }
+  } else if (row - n_rows < n_pad && sub == 0) {
+    const long long p = row - n_rows;
+    const int pad = S_pad - S;
+    const long long bh = p / pad;
+    const int i = S + static_cast<int>(p % pad);
+    D[bh * S_pad + i] = 0.f;
+    lse2[bh * S_pad + i] = INFINITY;
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// 3. dq convert: 8 elements per thread (two 16-byte loads, one 16-byte store).
+// ------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
+                                                         __nv_bfloat16 *__restrict__ dq,
+                                                         size_t n8) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n8) return;
+  const float4 a = reinterpret_cast<const float4 *>(acc)[2 * t];
+  const float4 c = reinterpret_cast<const float4 *>(acc)[2 * t + 1];
+  reinterpret_cast<uint4 *>(dq)[t] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
+                                                pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
+}
+
+// ------------------------------------------------------------------------------------
+// 2. main kernel
+// ------------------------------------------------------------------------------------
+constexpr int kBwdThreads = 384;
+
+template <int HD>
+struct BwdLayout {
+  static constexpr uint32_t kRowBytes = HD * 2;
+  static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
+  static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kTileBytes;
+  static constexpr uint32_t kQ = kV + kTileBytes;          // 2 stages
+  static constexpr uint32_t kdO = kQ + 2 * kTileBytes;     // 2 stages
+  static constexpr uint32_t kdS = kdO + 2 * kTileBytes;    // 128 x 128 bf16, MN-major, 32 KB
+  static constexpr uint32_t kVec = kdS + 32768;            // LSE2[2][128], D[2][128] fp32
+  // barriers: kv_full, full[2], empty[2], s_full, dp_full, p_full, ds_full, dq_full,
+  //           dq_empty, acc_done, dv_done, dk_done
+  static constexpr int kNumBars = 14;
+  static constexpr uint32_t kBars = kVec + 4 * 512;
+  static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
+  static constexpr uint32_t kUsed = kMisc + 32;
+  static constexpr uint32_t kDynBytes = (kUsed + 1024 > 120 * 1024) ? kUsed + 1024 : 120 * 1024;
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+  const bool ok = mbar_wait(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// Offset of element (key row j, query column i) of the 128 x 128 dS^T tile, stored as
+// the A operand of dQ = dS K: M = query (contiguous), K = key rows; two 64-column
+// atoms of 128-byte rows with the 128-byte swizzle (16-byte chunk ^= row % 8).
+__device__ __forceinline__ uint32_t ds_offset(int j, int i) {
+  return static_cast<uint32_t>((i >> 6) * 16384 + j * 128 + ((((i & 63) >> 3) ^ (j & 7)) << 4));
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                         const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                         const float *__restrict__ Dvec, const float *__restrict__ lse2,
+                         float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dk,
+                         __nv_bfloat16 *__restrict__ dv, int B, int S, int nh, int nkv,
+                         float scale, float scale_log2, int *status, unsigned long long timeout_ns) {
+  using L = BwdLayout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Unit of this CTA: key tile n (most work first), batch b, kv head kvh.
+  const int num_m = (S + kTileRows - 1) / kTileRows;
+  const int S_pad = num_m * kTileRows;
+  const int BK = B * nkv;
+  const int n = static_cast<int>(blockIdx.x) / BK;
+  const int bk = static_cast<int>(blockIdx.x) % BK;
+  const int b = bk / nkv, kvh = bk % nkv;
+  const int group = nh / nkv;
+  const int per_head = num_m - n;         // query tiles m = n .. num_m-1
+  const int T = group * per_head;         // iterations (r, m)
+
+  const uint32_t sK = smem_u32(smem + L::kK);
+  const uint32_t sV = smem_u32(smem + L::kV);
+  const uint32_t sQ = smem_u32(smem + L::kQ);
+  const uint32_t sdO = smem_u32(smem + L::kdO);
+  uint8_t *sdS_ptr = smem + L::kdS;
+  const uint32_t sdS = smem_u32(sdS_ptr);
+  float *sLSE = reinterpret_cast<float *>(smem + L::kVec);         // [2][128]
+  float *sD = reinterpret_cast<float *>(smem + L::kVec + 1024);    // [2][128]
+  const uint32_t bar0 = smem_u32(smem + L::kBars);
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const uint32_t kv_full = bar(0);
+  auto full = [&](int s) { return bar(1 + s); };
+  auto empty = [&](int s) { return bar(3 + s); };
+  const uint32_t s_full = bar(5), dp_full = bar(6), p_full = bar(7), ds_full = bar(8);
+  const uint32_t dq_full = bar(9), dq_empty = bar(10), acc_done = bar(11);
+  const uint32_t dv_done = bar(12), dk_done = bar(13);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
+  const WaitCtl ctl{abort_flag, status, timeout_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
+    mbar_init(p_full, 128);
+    mbar_init(ds_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(acc_done, 1);
+    mbar_init(dv_done, 1);
+    mbar_init(dk_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mk);
+    tma_prefetch_desc(&mv);
+    tma_prefetch_desc(&mdo);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 320, tdQ = tmem + 384;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      mbar_expect_tx(kv_full, 2 * L::kTileBytes);
+      tma_load_4d(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
+      tma_load_4d(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
+      int issued = 0;
+      for (int t = 0; t < T; ++t) {
+        const int r = t / per_head, m = n + t % per_head;
+        const int h = kvh * group + r;
+        const int s = t & 1;
+        if (!mbar_wait(empty(s), ((t >> 1) & 1) ^ 1, ctl)) break;
+        mbar_expect_tx(full(s), 2 * L::kTileBytes + 2 * 512);
+        tma_load_4d(sQ + s * L::kTileBytes, &mq, full(s), 0, h, m * kTileRows, b);
+        tma_load_4d(sdO + s * L::kTileBytes, &mdo, full(s), 0, h, m * kTileRows, b);
+        const size_t vec = (static_cast<size_t>(b) * nh + h) * S_pad + static_cast<size_t>(m) * kTileRows;
+        bulk_load(smem_u32(sLSE + s * 128), lse2 + vec, 512, full(s));
+        bulk_load(smem_u32(sD + s * 128), Dvec + vec, 512, full(s));
+        issued = t + 1;
+      }
+      mbar_drain(kv_full, 0, ctl);
+      for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
+        mbar_drain(full(t & 1), (t >> 1) & 1, ctl);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A in TMEM)
+      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);    // dQ (A = dS, MN-major)
+      auto issue_kmajor = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t a = smem_desc(a_base + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
+          const uint64_t bd = smem_desc(b_base + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
+          mma_ss(d, a, bd, idesc_t, kk > 0);
+        }
+      };
+      auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint32_t b_base, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk) {
+          const uint64_t bd = smem_desc(b_base + kk * 16 * L::kRowBytes, 8192, 8 * L::kRowBytes,
+                                        L::kSwizzle);
+          mma_ts(d, a_tmem + kk * 8, bd, idesc_acc, (!first || kk > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, ctl) && mbar_wait(full(0), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_kmajor(tS, sK, sQ);
+        mma_commit(s_full);
+        issue_kmajor(tdP, sV, sdO);
+        mma_commit(dp_full);
+      }
+      for (int t = 0; ok && t < T; ++t) {
+        const int s = t & 1;
+        if (!mbar_wait(p_full, t & 1, ctl)) break;
+        tc_fence_after();
+        issue_acc(tdV, tS, sdO + s * L::kTileBytes, t == 0);             // dV += P^T dO
+        mma_commit(dv_done);
+        const bool more = t + 1 < T;
+        if (more) {
+          if (!mbar_wait(full(s ^ 1), ((t + 1) >> 1) & 1, ctl)) break;
+          // S^T(t+1) overwrites the P^T that dV(t) reads; MMAs into different
+          // accumulators are not ordered by issue, so wait for dV(t).
+          if (!mbar_wait(dv_done, t & 1, ctl)) break;
+          tc_fence_after();
+          issue_kmajor(tS, sK, sQ + (s ^ 1) * L::kTileBytes);             // S^T(t+1)
+          mma_commit(s_full);
+        }
+        if (!mbar_wait(ds_full, t & 1, ctl)) break;
+        tc_fence_after();
+        issue_acc(tdK, tdP, sQ + s * L::kTileBytes, t == 0);               // dK += dS^T Q
+        mma_commit(empty(s));
+        mma_commit(dk_done);
+        if (!mbar_wait(dq_empty, (t & 1) ^ 1, ctl)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk) {                      // dQ = dS K
+          const uint64_t a = smem_desc(sdS + kk * 2048, 16384, 1024, kSwizzle128);
+          const uint64_t bd = smem_desc(sK + kk * 16 * L::kRowBytes, 8192, 8 * L::kRowBytes,
+                                        L::kSwizzle);
+          mma_ss(tdQ, a, bd, idesc_dq, kk > 0);
+        }
+        mma_commit(dq_full);
+        if (more) {
+          // dP^T(t+1) overwrites the dS^T that dK(t) reads.
+          if (!mbar_wait(dk_done, t & 1, ctl)) break;
+          tc_fence_after();
+          issue_kmajor(tdP, sV, sdO + (s ^ 1) * L::kTileBytes);           // dP^T(t+1)
+          mma_commit(dp_full);
+        }
+      }
+      mma_commit(acc_done);
+      mbar_drain(acc_done, 0, ctl);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- P^T and dS^T: one thread per key row ----------------
+    const int quarter = warp & 3;
+    const int j = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      const int m = n + t % per_head;
+      const int s = t & 1;
+      const bool diag = (m == n);
+      const float *lse_s = sLSE + s * 128;
+      const float *D_s = sD + s * 128;
+      // Phase 1: P^T
+      if (!warp_wait(s_full, t & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(tS + lane_off + c, r);
+        tmem_wait_ld();
+        reg_fence<32>(r);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int i0 = c + 2 * e, i1 = i0 + 1;
+          float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * e]), scale_log2, -lse_s[i0]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -lse_s[i1]));
+          if (diag && i0 < j) p0 = 0.f;
+          if (diag && i1 < j) p1 = 0.f;
+          pk[c / 2 + e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16(tS + lane_off + c / 2, pk + c / 2);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+      // Phase 2: dS^T
+      if (!warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
+      if (t > 0 && !warp_wait(dq_full, (t - 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t r[32];
+        tmem_ld_x32(tdP + lane_off + c, r);
+        tmem_wait_ld();
+        reg_fence<32>(r);
+        uint32_t dsk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int i0 = c + 2 * e;
+          const uint32_t p = pk[c / 2 + e];
+          const float ds0 = bf16lo_to_f32(p) * (__uint_as_float(r[2 * e]) - D_s[i0]) * scale;
+          const float ds1 = bf16hi_to_f32(p) * (__uint_as_float(r[2 * e + 1]) - D_s[i0 + 1]) * scale;
+          dsk[e] = pack_bf16x2(ds0, ds1);
+        }
+        tmem_st_x16(tdP + lane_off + c / 2, dsk);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, c + 8 * e)) =
+              make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(ds_full);
+    }
+    // Epilogue: dV and dK rows of this key tile (dK already carries the scale).
+    if (ok && warp_wait(acc_done, 0, ctl)) {
+      tc_fence_after();
+      const int jg = n * kTileRows + j;
+      const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t tsrc = which == 0 ? tdV : tdK;
+        __nv_bfloat16 *dst_row = (which == 0 ? dv : dk) + row_off;
+#pragma unroll
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t r[32];
+          tmem_ld_x32(tsrc + lane_off + c, r);
+          tmem_wait_ld();
+          reg_fence<32>(r);
+          if (jg < S) {
+            uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * e]), __uint_as_float(r[8 * e + 1])),
+                                  pack_bf16x2(__uint_as_float(r[8 * e + 2]), __uint_as_float(r[8 * e + 3])),
+                                  pack_bf16x2(__uint_as_float(r[8 * e + 4]), __uint_as_float(r[8 * e + 5])),
+                                  pack_bf16x2(__uint_as_float(r[8 * e + 6]), __uint_as_float(r[8 * e + 7])));
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------- dQ drain: one thread per query row ----------------
+    const int quarter = warp & 3;
+    const int i = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    for (int t = 0; t < T; ++t) {
+      const int r = t / per_head, m = n + t % per_head;
+      const int h = kvh * group + r;
+      if (!warp_wait(dq_full, t & 1, ctl)) break;
+      tc_fence_after();
+      uint32_t v[HD];
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) tmem_ld_x32(tdQ + lane_off + c, v + c);
+      tmem_wait_ld();
+      reg_fence<HD>(v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      const int ig = m * kTileRows + i;
+      if (ig < S) {
+        float4 *dst = reinterpret_cast<float4 *>(dqacc + ((static_cast<size_t>(b) * S + ig) * nh + h) * HD);
+#pragma unroll
+        for (int e = 0; e < HD / 4; ++e)
+          atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD>
+cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                           const CUtensorMap &mdo, const BwdWorkspace &ws, __nv_bfloat16 *dk,
+                           __nv_bfloat16 *dv, int B, int S, int nh, int nkv, float scale,
+                           int *status, uint64_t timeout_ns, cudaStream_t stream) {
+  using L = BwdLayout<HD>;
+  cudaError_t err = cudaFuncSetAttribute(attn_bwd_main_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
+  if (err != cudaSuccess) return err;
+  const int num_n = (S + kTileRows - 1) / kTileRows;
+  const unsigned grid = static_cast<unsigned>(B) * nkv * num_n;
+  attn_bwd_main_kernel<HD><<<grid, kBwdThreads, L::kDynBytes, stream>>>(
+      mq, mk, mv, mdo, ws.D, ws.lse2, ws.dqacc, dk, dv, B, S, nh, nkv, scale, scale * kLog2e,
+      status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dO,
+                                  const float *lse, int B, int S, int nh, int hd,
+                                  const BwdWorkspace &ws, cudaStream_t stream) {
+  const long long n_rows = static_cast<long long>(B) * S * nh;
+  const long long n_pad = static_cast<long long>(B) * nh * (padded_rows(S) - S);
+  const int lanes = hd / 8;
+  const long long threads = (n_rows + n_pad) * lanes;
+  const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
+  if (hd == 64)
+    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dO, lse, ws.D, ws.lse2, ws.dqacc, B, S, nh);
+  else if (hd == 32)
+    bwd_preprocess_kernel<32><<<grid, 256, 0, stream>>>(o, dO, lse, ws.D, ws.lse2, ws.dqacc, B, S, nh);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
+                                 const CUtensorMap &mv, const CUtensorMap &mdo,
+                                 const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
+                                 int B, int S, int nh, int nkv, int hd, float scale, int *status,
+                                 uint64_t timeout_ns, cudaStream_t stream) {
+  if (hd == 64)
+    return launch_main_hd<64>(mq, mk, mv, mdo, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  if (hd == 32)
+    return launch_main_hd<32>(mq, mk, mv, mdo, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, size_t n_elems,
+                              cudaStream_t stream) {
+  const size_t n8 = n_elems / 8;
+  const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
+  if (grid == 0) return cudaSuccess;
+  dq_convert_kernel<<<grid, 256, 0, stream>>>(dqacc, dq, n8);
+  return cudaGetLastError();
+}
+
+}  // namespace xattn

@@ -1,0 +1,319 @@
+// Forward of fused causal attention with grouped KV heads on sm_103a tensor cores.
+//
+// Method (xtrain "演进总览" / docs/evolution.md, phase table row T14): one kernel, an
+// online softmax tiled over KV, the S x S scores never leave the chip, and each row's
+// log-sum-exp is kept for the backward. Grouped KV heads (row T15): query head h reads
+// kv head h / group.
+//
+// GB300 mapping (one CTA per 128-row query tile, 8 warps):
+//   warp 0    : TMA producer. Q tile once; K/V tiles into a 3-stage shared-memory ring.
+//   warp 1    : allocates TMEM; one lane issues tcgen05.mma:
+//                 S_n  = Q K_n^T  (A, B from shared memory)      -> TMEM, double-buffered
+//                 O   += P_n V_n  (A = P from TMEM, B from smem) -> TMEM accumulator
+//   warps 4-7 : softmax, one thread per query row (TMEM lane). Loads S_n, applies the
+//               causal mask on the diagonal tile, keeps the running max and sum in fp32
+//               (log2 domain), writes P_n (bf16) over S_n in TMEM, and rescales O only
+//               when the running max grows by more than 2^8 (the stale max is exact
+//               because the final normalisation uses the same max). Epilogue: O / l in
+//               bf16 and LSE = (m + log2 l) ln 2.
+// Causal tile skipping: query tile m visits key tiles 0..m only. Tiles are issued
+// longest first (m descending) so the last wave holds short tiles.
+#include "sm103_ptx.cuh"
+#include "xattn_internal.h"
+
+namespace xattn {
+namespace {
+
+constexpr int kFwdThreads = 256;
+constexpr int kFwdStages = 3;
+
+template <int HD>
+struct FwdLayout {
+  static constexpr uint32_t kRowBytes = HD * 2;
+  static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
+  static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kK = kQ + kTileBytes;
+  static constexpr uint32_t kV = kK + kFwdStages * kTileBytes;
+  static constexpr uint32_t kBars = kV + kFwdStages * kTileBytes;
+  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done, mma_final
+  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2;
+  static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
+  static constexpr uint32_t kUsed = kMisc + 32;
+  // Ask for enough shared memory that one CTA occupies an SM: each CTA holds all 512
+  // TMEM columns, so a second resident CTA would only spin in tcgen05.alloc.
+  static constexpr uint32_t kDynBytes = (kUsed + 1024 > 120 * 1024) ? kUsed + 1024 : 120 * 1024;
+};
+
+// Warp-uniform bounded wait: every lane waits, then all agree.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+  const bool ok = mbar_wait(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                    const __grid_constant__ CUtensorMap mv, __nv_bfloat16 *__restrict__ o,
+                    float *__restrict__ lse, int B, int S, int nh, int nkv, float scale_log2,
+                    int *status, unsigned long long timeout_ns) {
+  using L = FwdLayout<HD>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // Tile of this CTA, longest first.
+  const int num_m = (S + kTileRows - 1) / kTileRows;
+  const int BH = B * nh;
+  const int m = num_m - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int b = bh / nh, h = bh % nh;
+  const int kvh = h / (nh / nkv);
+  const int n_kv = m + 1;
+
+  const uint32_t sQ = smem_u32(smem + L::kQ);
+  const uint32_t sK = smem_u32(smem + L::kK);
+  const uint32_t sV = smem_u32(smem + L::kV);
+  const uint32_t bar0 = smem_u32(smem + L::kBars);
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  const uint32_t q_full = bar(0);
+  auto full = [&](int s) { return bar(1 + s); };
+  auto empty = [&](int s) { return bar(1 + kFwdStages + s); };
+  auto s_full = [&](int x) { return bar(1 + 2 * kFwdStages + x); };
+  auto p_full = [&](int x) { return bar(3 + 2 * kFwdStages + x); };
+  const uint32_t o_done = bar(5 + 2 * kFwdStages);
+  const uint32_t mma_final = bar(6 + 2 * kFwdStages);
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
+  const WaitCtl ctl{abort_flag, status, timeout_ns};
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kFwdStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(s_full(0), 1);
+    mbar_init(s_full(1), 1);
+    mbar_init(p_full(0), 128);
+    mbar_init(p_full(1), 128);
+    mbar_init(o_done, 1);
+    mbar_init(mma_final, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mq);
+    tma_prefetch_desc(&mk);
+    tma_prefetch_desc(&mv);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t tS[2] = {tmem, tmem + 128};
+  const uint32_t tO = tmem + 256;
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      mbar_expect_tx(q_full, L::kTileBytes);
+      tma_load_4d(sQ, &mq, q_full, 0, h, m * kTileRows, b);
+      int issued = 0;
+      for (int n = 0; n < n_kv; ++n) {
+        const int s = n % kFwdStages;
+        if (!mbar_wait(empty(s), ((n / kFwdStages) & 1) ^ 1, ctl)) break;
+        mbar_expect_tx(full(s), 2 * L::kTileBytes);
+        tma_load_4d(sK + s * L::kTileBytes, &mk, full(s), 0, kvh, n * kTileRows, b);
+        tma_load_4d(sV + s * L::kTileBytes, &mv, full(s), 0, kvh, n * kTileRows, b);
+        issued = n + 1;
+      }
+      // Let every copy in flight land before the CTA can exit.
+      mbar_drain(q_full, 0, ctl);
+      for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
+        mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+      auto issue_qk = [&](uint32_t d, int s) {
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t a = smem_desc(sQ + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
+          const uint64_t bdesc =
+              smem_desc(sK + s * L::kTileBytes + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
+          mma_ss(d, a, bdesc, idesc_qk, kk > 0);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, ctl) && mbar_wait(full(0), 0, ctl);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(tS[0], 0);
+        mma_commit(s_full(0));
+      }
+      for (int n = 0; ok && n < n_kv; ++n) {
+        if (n + 1 < n_kv) {
+          const int s1 = (n + 1) % kFwdStages;
+          if (!mbar_wait(full(s1), ((n + 1) / kFwdStages) & 1, ctl)) break;
+          // S(n+1) overwrites the TMEM buffer that holds P(n-1). MMAs into different
+          // accumulators are not ordered by issue, so P(n-1)'s reader, PV(n-1), must
+          // have completed first.
+          if (n > 0 && !mbar_wait(o_done, (n - 1) & 1, ctl)) break;
+          tc_fence_after();
+          issue_qk(tS[(n + 1) & 1], s1);
+          mma_commit(s_full((n + 1) & 1));
+        }
+        if (!mbar_wait(p_full(n & 1), (n >> 1) & 1, ctl)) break;
+        tc_fence_after();
+        const int s = n % kFwdStages;
+        const uint32_t tP = tS[n & 1];
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk) {
+          const uint64_t bdesc = smem_desc(sV + s * L::kTileBytes + kk * 16 * L::kRowBytes,
+                                           8192, 8 * L::kRowBytes, L::kSwizzle);
+          mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (n > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(empty(s));
+        mma_commit(o_done);
+      }
+      mma_commit(mma_final);
+      mbar_drain(mma_final, 0, ctl);
+    }
+  } else if (warp >= 4) {
+    // ---------------- softmax + epilogue (one thread per query row) ----------------
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    float mrow = -INFINITY, lrow = 0.f;
+    bool ok = true;
+    for (int n = 0; n < n_kv; ++n) {
+      if (!warp_wait(s_full(n & 1), (n >> 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r[128];
+      tmem_ld_x32(tS[n & 1] + lane_off + 0, r);
+      tmem_ld_x32(tS[n & 1] + lane_off + 32, r + 32);
+      tmem_ld_x32(tS[n & 1] + lane_off + 64, r + 64);
+      tmem_ld_x32(tS[n & 1] + lane_off + 96, r + 96);
+      tmem_wait_ld();
+      reg_fence<128>(r);
+      const bool diag = (n == m);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        float x = __uint_as_float(r[c]) * scale_log2;
+        if (diag && c > row) x = -INFINITY;
+        r[c] = __float_as_uint(x);
+        mx = fmaxf(mx, x);
+      }
+      // Conditional rescaling: keep the stale max unless some row of the warp grew by
+      // more than 2^8; the decision is per warp because TMEM loads/stores are collective.
+      const float mnew = fmaxf(mrow, mx);
+      const bool rescale = __any_sync(0xffffffffu, mnew > mrow + 8.0f);
+      const float m_use = rescale ? mnew : mrow;
+      const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2_approx(__uint_as_float(r[c + 2 * e]) - m_use);
+          const float p1 = ex2_approx(__uint_as_float(r[c + 2 * e + 1]) - m_use);
+          psum += p0 + p1;
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16(tS[n & 1] + lane_off + c / 2, pk);
+      }
+      // PV(n-1) is waited for on every tile, not only when rescaling: a parity wait is
+      // only unambiguous if the waiter has seen every earlier phase of the barrier.
+      if (n > 0) {
+        if (!warp_wait(o_done, (n - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        if (rescale) {
+#pragma unroll
+          for (int c = 0; c < HD; c += 32) {
+            uint32_t ov[32];
+            tmem_ld_x32(tO + lane_off + c, ov);
+            tmem_wait_ld();
+            reg_fence<32>(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st_x32(tO + lane_off + c, ov);
+          }
+        }
+      }
+      lrow = lrow * alpha + psum;
+      mrow = m_use;
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full(n & 1));
+    }
+    if (ok && warp_wait(o_done, (n_kv - 1) & 1, ctl)) {
+      tc_fence_after();
+      const int i = m * kTileRows + row;
+      const float inv = 1.f / lrow;
+      __nv_bfloat16 *orow = o + (static_cast<size_t>(b) * S + i) * nh * HD + static_cast<size_t>(h) * HD;
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t ov[32];
+        tmem_ld_x32(tO + lane_off + c, ov);
+        tmem_wait_ld();
+        reg_fence<32>(ov);
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+        if (i < S) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+        }
+      }
+      if (i < S) lse[(static_cast<size_t>(b) * S + i) * nh + h] = (mrow + __log2f(lrow)) * kLn2;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int HD>
+cudaError_t launch_fwd_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          __nv_bfloat16 *o, float *lse, int B, int S, int nh, int nkv, float scale,
+                          int *status, uint64_t timeout_ns, cudaStream_t stream) {
+  using L = FwdLayout<HD>;
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_kernel<HD>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
+  if (err != cudaSuccess) return err;
+  const int num_m = (S + kTileRows - 1) / kTileRows;
+  const unsigned grid = static_cast<unsigned>(B) * nh * num_m;
+  attn_fwd_kernel<HD><<<grid, kFwdThreads, L::kDynBytes, stream>>>(
+      mq, mk, mv, o, lse, B, S, nh, nkv, scale * kLog2e, status, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_bf16(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                            __nv_bfloat16 *o, float *lse, int B, int S, int nh, int nkv, int hd,
+                            float scale, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+  if (hd == 64)
+    return launch_fwd_hd<64>(mq, mk, mv, o, lse, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  if (hd == 32)
+    return launch_fwd_hd<32>(mq, mk, mv, o, lse, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace xattn

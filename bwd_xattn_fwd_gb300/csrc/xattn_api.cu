@@ -1,0 +1,284 @@
+// C ABI of libxattn (declared in include/xattn.h): argument checks, TMA tensor maps,
+// scratch handling and kernel launches. No call synchronises the device except
+// xattn_check_device_status.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/xattn.h"
+#include "xattn_internal.h"
+
+namespace xattn {
+namespace {
+
+// Device status word, written by kernels whose bounded waits expire.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  bool sm103 = false;
+  int *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+uint64_t wait_limit_ns() {
+  static const uint64_t v = [] {
+    const char *s = std::getenv("XATTN_WAIT_LIMIT_NS");
+    const unsigned long long x = s ? std::strtoull(s, nullptr, 10) : 0ull;
+    return x > 0 ? static_cast<uint64_t>(x) : static_cast<uint64_t>(2000000000ull);
+  }();
+  return v;
+}
+
+xattn_status device_info(DeviceInfo **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return XATTN_ERR_CUDA;
+  DeviceInfo &d = g_dev[dev];
+  std::call_once(d.once, [&d, dev] {
+    int major = 0, minor = 0;
+    d.err = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (d.err == cudaSuccess) d.err = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    d.sm103 = (major == 10 && minor == 3);
+    if (d.err == cudaSuccess) d.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_device_status);
+  });
+  if (d.err != cudaSuccess) return XATTN_ERR_CUDA;
+  *out = &d;
+  return XATTN_OK;
+}
+
+xattn_status get_encode() {
+  std::call_once(g_encode_once, [] {
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
+// 4-D map over a contiguous [B, S, H, hd] bf16 tensor; box = one head's 128-row tile.
+// The 128-byte (hd = 64) or 64-byte (hd = 32) swizzle matches the UMMA operand layout.
+// Rows past S read as zeros.
+xattn_status make_map(CUtensorMap *map, const void *ptr, int B, int S, int H, int hd) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t row = static_cast<cuuint64_t>(hd) * 2;
+  const cuuint64_t strides[3] = {row, row * H, row * H * S};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(hd), 1, static_cast<cuuint32_t>(kTileRows), 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims,
+                              strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              hd == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+xattn_status check_shape(int B, int S, int nh, int nkv, int hd, float scale) {
+  if (B <= 0 || S <= 0 || nh <= 0 || nkv <= 0 || hd <= 0) return XATTN_ERR_BAD_SHAPE;
+  // Keep every element index and grid size well inside their integer types.
+  const long long elems = static_cast<long long>(B) * S * nh * hd;
+  if (elems > (1ll << 40) || static_cast<long long>(B) * nh * ((S + 127) / 128) > (1ll << 31) - 1)
+    return XATTN_ERR_BAD_SHAPE;
+  if (nh % nkv != 0) return XATTN_ERR_GROUP;
+  if (!std::isfinite(scale)) return XATTN_ERR_BAD_SCALE;
+  return XATTN_OK;
+}
+
+xattn_status check_bf16(int hd) { return (hd == 32 || hd == 64) ? XATTN_OK : XATTN_ERR_UNSUPPORTED_HD; }
+
+xattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA; }
+
+#define XATTN_TRY(expr)                          \
+  do {                                           \
+    const xattn_status st_ = (expr);             \
+    if (st_ != XATTN_OK) return st_;             \
+  } while (0)
+
+xattn_status bf16_device(DeviceInfo **dev) {
+  XATTN_TRY(device_info(dev));
+  if (!(*dev)->sm103) return XATTN_ERR_NO_DEVICE_SUPPORT;
+  return get_encode();
+}
+
+xattn_status check_workspace(void *ws, size_t bytes, int B, int S, int nh, int hd) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return XATTN_ERR_WORKSPACE;
+  if (bytes < bwd_workspace_bytes(B, S, nh, hd)) return XATTN_ERR_WORKSPACE;
+  return XATTN_OK;
+}
+
+}  // namespace
+}  // namespace xattn
+
+using namespace xattn;
+
+extern "C" {
+
+xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S, int nh, int nkv,
+                       int hd, float scale, void *o, float *lse, void *stream) {
+  if (!q || !k || !v || !o || !lse) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  XATTN_TRY(check_bf16(hd));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return XATTN_ERR_MISALIGNED;
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(bf16_device(&dev));
+  CUtensorMap mq, mk, mv;
+  XATTN_TRY(make_map(&mq, q, B, S, nh, hd));
+  XATTN_TRY(make_map(&mk, k, B, S, nkv, hd));
+  XATTN_TRY(make_map(&mv, v, B, S, nkv, hd));
+  return cuda_status(launch_fwd_bf16(mq, mk, mv, static_cast<__nv_bfloat16 *>(o), lse, B, S, nh, nkv,
+                                     hd, scale, dev->status, wait_limit_ns(),
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+size_t xattn_bwd_workspace_bytes(int B, int S, int nh, int hd) {
+  if (B <= 0 || S <= 0 || nh <= 0 || hd <= 0) return 0;
+  return bwd_workspace_bytes(B, S, nh, hd);
+}
+
+xattn_status xattn_bwd_preprocess(const void *o, const void *dO, const float *lse, int B, int S,
+                                  int nh, int hd, void *workspace, size_t workspace_bytes,
+                                  void *stream) {
+  if (!o || !dO || !lse) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nh, hd, 1.0f));
+  XATTN_TRY(check_bf16(hd));
+  if (!aligned16(o) || !aligned16(dO)) return XATTN_ERR_MISALIGNED;
+  XATTN_TRY(check_workspace(workspace, workspace_bytes, B, S, nh, hd));
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(bf16_device(&dev));
+  const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
+  return cuda_status(launch_bwd_preprocess(static_cast<const __nv_bfloat16 *>(o),
+                                           static_cast<const __nv_bfloat16 *>(dO), lse, B, S, nh, hd,
+                                           ws, static_cast<cudaStream_t>(stream)));
+}
+
+xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const void *dO, int B,
+                            int S, int nh, int nkv, int hd, float scale, void *dk, void *dv,
+                            void *workspace, size_t workspace_bytes, void *stream) {
+  if (!q || !k || !v || !dO || !dk || !dv) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  XATTN_TRY(check_bf16(hd));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) ||
+      !aligned16(dv))
+    return XATTN_ERR_MISALIGNED;
+  XATTN_TRY(check_workspace(workspace, workspace_bytes, B, S, nh, hd));
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(bf16_device(&dev));
+  CUtensorMap mq, mk, mv, mdo;
+  XATTN_TRY(make_map(&mq, q, B, S, nh, hd));
+  XATTN_TRY(make_map(&mk, k, B, S, nkv, hd));
+  XATTN_TRY(make_map(&mv, v, B, S, nkv, hd));
+  XATTN_TRY(make_map(&mdo, dO, B, S, nh, hd));
+  const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
+  return cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, ws, static_cast<__nv_bfloat16 *>(dk),
+                                          static_cast<__nv_bfloat16 *>(dv), B, S, nh, nkv, hd, scale,
+                                          dev->status, wait_limit_ns(),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, void *dq, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
+  if (!dq) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nh, hd, 1.0f));
+  XATTN_TRY(check_bf16(hd));
+  if (!aligned16(dq)) return XATTN_ERR_MISALIGNED;
+  XATTN_TRY(check_workspace(workspace, workspace_bytes, B, S, nh, hd));
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(bf16_device(&dev));
+  const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
+  return cuda_status(launch_dq_convert(ws.dqacc, static_cast<__nv_bfloat16 *>(dq),
+                                       static_cast<size_t>(B) * S * nh * hd,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *o, const void *dO,
+                       const float *lse, int B, int S, int nh, int nkv, int hd, float scale, void *dq,
+                       void *dk, void *dv, void *stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  XATTN_TRY(check_bf16(hd));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return XATTN_ERR_MISALIGNED;
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(bf16_device(&dev));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = bwd_workspace_bytes(B, S, nh, hd);
+  void *ws = nullptr;
+  if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return XATTN_ERR_CUDA;
+  xattn_status r = xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, ws, bytes, stream);
+  if (r == XATTN_OK) r = xattn_bwd_main(q, k, v, dO, B, S, nh, nkv, hd, scale, dk, dv, ws, bytes, stream);
+  if (r == XATTN_OK) r = xattn_bwd_dq_convert(B, S, nh, hd, dq, ws, bytes, stream);
+  const cudaError_t fe = cudaFreeAsync(ws, st);
+  if (r == XATTN_OK && fe != cudaSuccess) r = XATTN_ERR_CUDA;
+  return r;
+}
+
+xattn_status xattn_fwd_f32(const float *q, const float *k, const float *v, int B, int S, int nh,
+                           int nkv, int hd, float scale, float *o, float *lse, void *stream) {
+  if (!q || !k || !v || !o || !lse) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  if (hd > 128) return XATTN_ERR_UNSUPPORTED_HD;
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(device_info(&dev));
+  return cuda_status(launch_fwd_f32(q, k, v, o, lse, B, S, nh, nkv, hd, scale,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+xattn_status xattn_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+                           const float *dO, const float *lse, int B, int S, int nh, int nkv, int hd,
+                           float scale, float *dq, float *dk, float *dv, void *stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  if (hd > 128) return XATTN_ERR_UNSUPPORTED_HD;
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(device_info(&dev));
+  return cuda_status(launch_bwd_f32(q, k, v, o, dO, lse, dq, dk, dv, B, S, nh, nkv, hd, scale,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+const char *xattn_status_string(xattn_status s) {
+  switch (s) {
+    case XATTN_OK: return "ok";
+    case XATTN_ERR_NULL_PTR: return "a required pointer is NULL";
+    case XATTN_ERR_BAD_SHAPE: return "B, S, nh, nkv and hd must be positive and within size limits";
+    case XATTN_ERR_GROUP: return "nh must be a multiple of nkv";
+    case XATTN_ERR_UNSUPPORTED_HD: return "unsupported head dimension (bf16: 32 or 64; fp32: <= 128)";
+    case XATTN_ERR_MISALIGNED: return "a bf16 tensor pointer is not 16-byte aligned";
+    case XATTN_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case XATTN_ERR_NO_DEVICE_SUPPORT: return "the current device is not compute capability 10.3 (sm_103)";
+    case XATTN_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait expired";
+    case XATTN_ERR_BAD_SCALE: return "scale must be finite";
+    case XATTN_ERR_WORKSPACE: return "workspace is NULL, not 256-byte aligned, or too small";
+  }
+  return "unknown xattn status";
+}
+
+xattn_status xattn_check_device_status(void *stream) {
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(device_info(&dev));
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return XATTN_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return XATTN_ERR_CUDA;
+  if (word != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return XATTN_ERR_CUDA;
+    return static_cast<xattn_status>(word);
+  }
+  return XATTN_OK;
+}
+
+}  // extern "C"

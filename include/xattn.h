@@ -1,0 +1,136 @@
+/*
+ * libxattn: fused causal scaled-dot-product attention with grouped KV heads (GQA),
+ * forward and backward, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (xtrain "演进总览" / docs/evolution.md, phase table):
+ *   - row T14: one fused attention op. The forward runs an online softmax tiled over
+ *     KV and never materialises the S x S scores; it keeps each row's log-sum-exp.
+ *     The backward recomputes the scores and replaces the softmax Jacobian by
+ *     D_i = sum_d dO_id O_id, giving dQ, dK and dV.
+ *   - row T15: grouped KV heads. Query head h reads kv head h / (nh / nkv); the
+ *     gradient of a kv head is the deterministic sum over its query group.
+ *   - causal masking as in the composed path of xtrain "Known Issues & Perf Backlog"
+ *     (docs/known-issues.md), KI-1 fix: query i sees keys j <= i (diagonal included);
+ *     queries and keys have the same length S.
+ *
+ * Definition (natural log; scale multiplies the scores before the softmax):
+ *   s_ij = scale * q_i . k_j (j <= i),  LSE_i = log sum_{j<=i} exp(s_ij),
+ *   P_ij = exp(s_ij - LSE_i),  O_i = sum_j P_ij v_j,
+ *   dS_ij = P_ij (dO_i . v_j - dO_i . O_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_{group} sum_i dS_ij q_i,
+ *   dV_j = sum_{group} sum_i P_ij dO_i.
+ *
+ * Layout: every tensor is contiguous and row-major.
+ *   q, o, dO, dq : [B, S, nh,  hd]
+ *   k, v, dk, dv : [B, S, nkv, hd]
+ *   lse          : [B, S, nh] float (natural log of the scaled scores' sum of exps)
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller, unless a comment says
+ *     otherwise. Inputs are read only. Outputs are overwritten, never accumulated into.
+ *   - stream is a cudaStream_t (NULL = the legacy default stream). Calls enqueue work
+ *     and return; none synchronises the device (xtrain docs/06-performance.md,
+ *     "Phase T7", design decision 3: no per-op synchronisation).
+ *   - Argument checks run before any launch. On a check failure nothing is enqueued
+ *     and the outputs are untouched. Launch failures return XATTN_ERR_CUDA.
+ *   - A kernel that waits on an on-chip barrier longer than a bounded time (about
+ *     two seconds) gives up, records XATTN_ERR_DEVICE_TIMEOUT in a device status word
+ *     and finishes; xattn_check_device_status reports it.
+ */
+#ifndef XATTN_H
+#define XATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    XATTN_OK = 0,
+    XATTN_ERR_NULL_PTR = 1,           /* a required pointer is NULL */
+    XATTN_ERR_BAD_SHAPE = 2,          /* B, S, nh, nkv or hd <= 0, or a size overflows int32 */
+    XATTN_ERR_GROUP = 3,              /* nh is not a multiple of nkv */
+    XATTN_ERR_UNSUPPORTED_HD = 4,     /* bf16: hd not in {32, 64}; fp32: hd > 128 */
+    XATTN_ERR_MISALIGNED = 5,         /* a bf16 tensor pointer is not 16-byte aligned */
+    XATTN_ERR_CUDA = 6,               /* a CUDA runtime or driver call failed */
+    XATTN_ERR_NO_DEVICE_SUPPORT = 7,  /* the current device is not compute capability 10.3 */
+    XATTN_ERR_DEVICE_TIMEOUT = 8,     /* a bounded on-device wait expired (reported later) */
+    XATTN_ERR_BAD_SCALE = 9,          /* scale is not finite */
+    XATTN_ERR_WORKSPACE = 10          /* workspace pointer NULL/misaligned or too small */
+} xattn_status;
+
+/*
+ * Forward, bf16 (xtrain docs/evolution.md, row T14: online softmax tiled over KV,
+ * per-row log-sum-exp kept). q, k, v, o are bf16; lse is float.
+ * hd in {32, 64}; any S >= 1. Arithmetic: bf16 products, fp32 accumulation and
+ * softmax statistics (row T12: softmax kept in fp32 under bf16); P is rounded to bf16
+ * before the P.V product; o is rounded to nearest even.
+ */
+xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S, int nh,
+                       int nkv, int hd, float scale, void *o, float *lse, void *stream);
+
+/*
+ * Backward, bf16 (row T14: recompute the scores, D = rowsum(dO * O); row T15: dK/dV
+ * summed over each kv head's query group without atomics). Takes the forward's o and
+ * lse. Writes dq [B,S,nh,hd], dk and dv [B,S,nkv,hd] in bf16.
+ * Scratch (xattn_bwd_workspace_bytes) is taken with cudaMallocAsync on `stream` and
+ * released with cudaFreeAsync on the same stream; nothing else is allocated.
+ * dQ is accumulated across key tiles with fp32 atomic adds, so its last bits may
+ * vary from run to run; dK, dV, o and lse are bit-for-bit reproducible.
+ */
+xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const void *dO, const float *lse, int B, int S, int nh, int nkv,
+                       int hd, float scale, void *dq, void *dk, void *dv, void *stream);
+
+/*
+ * The backward's three steps with a caller-owned workspace, for callers that manage
+ * memory themselves (or capture the call in a CUDA graph). xattn_bwd is exactly
+ * workspace allocation + these three calls + release.
+ *
+ * workspace: device pointer, 256-byte aligned, at least xattn_bwd_workspace_bytes()
+ * bytes. Its contents on entry do not matter; the three steps must run in this order
+ * on one stream with the same arguments.
+ *   xattn_bwd_preprocess : D_i = dO_i . O_i (fp32), the log2-domain LSE rows, and a
+ *                          zeroed fp32 dQ accumulator (all inside the workspace).
+ *   xattn_bwd_main       : the recompute loop; writes dk, dv and adds into the dQ
+ *                          accumulator.
+ *   xattn_bwd_dq_convert : dq = bf16(dQ accumulator).
+ */
+size_t xattn_bwd_workspace_bytes(int B, int S, int nh, int hd);
+xattn_status xattn_bwd_preprocess(const void *o, const void *dO, const float *lse, int B,
+                                  int S, int nh, int hd, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const void *dO,
+                            int B, int S, int nh, int nkv, int hd, float scale, void *dk,
+                            void *dv, void *workspace, size_t workspace_bytes, void *stream);
+xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, void *dq, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
+ * fp32 mode: same parameters and layouts, float tensors, IEEE fp32 arithmetic on the
+ * CUDA cores (no TF32). hd in [1, 128]; any S >= 1. No scratch memory.
+ */
+xattn_status xattn_fwd_f32(const float *q, const float *k, const float *v, int B, int S,
+                           int nh, int nkv, int hd, float scale, float *o, float *lse,
+                           void *stream);
+xattn_status xattn_bwd_f32(const float *q, const float *k, const float *v, const float *o,
+                           const float *dO, const float *lse, int B, int S, int nh, int nkv,
+                           int hd, float scale, float *dq, float *dk, float *dv,
+                           void *stream);
+
+/* Static text for a status code (never NULL). */
+const char *xattn_status_string(xattn_status status);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns XATTN_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the
+ * last check, XATTN_ERR_CUDA if the synchronisation failed, else XATTN_OK.
+ */
+xattn_status xattn_check_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XATTN_H */

@@ -1,0 +1,100 @@
+"""Helpers shared by the GPU tests: run the libxattn path on seeded inputs and compare
+its outputs with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from bwd_xattn_fwd_gb300 import workloads as W
+
+# Parity bar: per output tensor, max|gpu - ref| / max|ref| (LSE: absolute, natural log).
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-4
+TOL_LSE = 1e-3
+
+
+def tol_for(dtype: str) -> float:
+    return TOL_BF16 if dtype == "bf16" else TOL_F32
+
+
+def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
+    # The floor only matters where the exact result is (near) zero everywhere, e.g. dQ
+    # and dK at S = 1; there the bar becomes an absolute 1e-4 * tol.
+    return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-4))
+
+
+def run_gpu(w: W.Workload, x: dict, device="cuda"):
+    """Forward then backward through the C ABI. Returns float64 numpy outputs."""
+    from bwd_xattn_fwd_gb300 import xattn
+    q, k, v, dO = (x[n].to(device) for n in ("q", "k", "v", "dO"))
+    o, lse = xattn.attention_fwd(q, k, v, w.scale)
+    dq, dk, dv = xattn.attention_bwd(q, k, v, o, dO, lse, w.scale)
+    torch.cuda.synchronize()
+    assert xattn.xattn_check_device_status() == 0
+    return {n: W.as_f64(t) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+
+
+def oracle_full(w: W.Workload, x: dict):
+    q, k, v, dO = (W.as_f64(x[n]) for n in ("q", "k", "v", "dO"))
+    orc = oracle.default()
+    o, lse = orc.fwd(q, k, v, w.scale)
+    dq, dk, dv = orc.bwd(q, k, v, dO, w.scale)
+    return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+
+def oracle_unit(w: W.Workload, x: dict, b: int, kvh: int):
+    """Oracle outputs of one (batch, kv head) unit: a complete attention problem with
+    B=1, nkv=1 and nh=group."""
+    q, k, v, dO = (W.as_f64(x[n][b:b + 1]) for n in ("q", "k", "v", "dO"))
+    uq, uk, uv, udo = oracle.unit_slices(q, k, v, dO, 0, kvh)
+    orc = oracle.default()
+    o, lse = orc.fwd(uq, uk, uv, w.scale)
+    dq, dk, dv = orc.bwd(uq, uk, uv, udo, w.scale)
+    return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+
+
+def gpu_unit(w: W.Workload, out: dict, b: int, kvh: int):
+    g = w.group
+    hs = slice(kvh * g, (kvh + 1) * g)
+    return {"o": out["o"][b:b + 1, :, hs], "lse": out["lse"][b:b + 1, :, hs],
+            "dq": out["dq"][b:b + 1, :, hs], "dk": out["dk"][b:b + 1, :, kvh:kvh + 1],
+            "dv": out["dv"][b:b + 1, :, kvh:kvh + 1]}
+
+
+def compare(got: dict, ref: dict, dtype: str, where: str = ""):
+    tol = tol_for(dtype)
+    report = {}
+    for name in ("o", "dq", "dk", "dv"):
+        assert np.all(np.isfinite(got[name])), f"{where} {name}: non-finite values"
+        e = rel_err(got[name], ref[name])
+        report[name] = e
+        assert e <= tol, f"{where} {name}: max|err|/max|ref| = {e:.3e} > {tol}"
+    e = float(np.abs(got["lse"] - ref["lse"]).max())
+    report["lse"] = e
+    assert e <= TOL_LSE, f"{where} lse: max|err| = {e:.3e} > {TOL_LSE}"
+    return report
+
+
+def check_invariants(w: W.Workload, x: dict, out: dict, tol: float):
+    """Identities of the exact gradient, per (batch, kv head), checked on the full GPU
+    outputs:
+      sum_j dV_j = sum of dO over the group's query rows,
+      sum_j dK_j = 0,
+      sum q.dq over the group = sum k.dk.
+    If every element is within tol * max|ref| of the exact gradient (the parity bar),
+    each identity holds up to the sum of those element bounds; that sum is the bound
+    checked here (with max|gpu| standing in for max|ref|)."""
+    q, k, dO = (W.as_f64(x[n]) for n in ("q", "k", "dO"))
+    B, S, nkv, g, hd = w.B, w.S, w.nkv, w.group, w.hd
+    dq, dk, dv = out["dq"], out["dk"], out["dv"]
+    sum_do = dO.reshape(B, S, nkv, g, hd).sum(axis=(1, 3))                  # [B, nkv, hd]
+    bound_v = tol * S * np.abs(dv).max(axis=(1, 3))[:, :, None]
+    assert np.all(np.abs(dv.sum(axis=1) - sum_do) <= bound_v), "sum dV"
+    bound_k = tol * S * np.abs(dk).max(axis=(1, 3))[:, :, None]
+    assert np.all(np.abs(dk.sum(axis=1)) <= bound_k), "sum dK"
+    lhs = (q * dq).reshape(B, S, nkv, g, hd).sum(axis=(1, 3, 4))            # [B, nkv]
+    rhs = (k * dk).sum(axis=(1, 3))
+    bound = tol * (np.abs(q).reshape(B, S, nkv, g, hd).sum(axis=(1, 3, 4)) * np.abs(dq).max()
+                   + np.abs(k).sum(axis=(1, 3)) * np.abs(dk).max())
+    assert np.all(np.abs(lhs - rhs) <= bound), "q.dq vs k.dk"

@@ -1,0 +1,103 @@
+"""libxattn's C ABI without a GPU: the library loads, exports every entry point that
+include/xattn.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xattn.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(xattn_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bwd_xattn_fwd_gb300 import build
+    return ctypes.CDLL(build.build())
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for s in ("xattn_fwd", "xattn_bwd", "xattn_fwd_f32", "xattn_bwd_f32", "xattn_status_string",
+              "xattn_check_device_status"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [s for s in declared_symbols() if not hasattr(lib, s)]
+    assert not missing, missing
+
+
+def test_binding_exposes_the_same_names():
+    from bwd_xattn_fwd_gb300 import xattn
+    missing = [s for s in declared_symbols() if not callable(getattr(xattn, s, None))]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    lib.xattn_status_string.restype = ctypes.c_char_p
+    seen = set()
+    for code in range(0, 11):
+        s = lib.xattn_status_string(code).decode()
+        assert s and s != "unknown xattn status"
+        seen.add(s)
+    assert len(seen) == 11
+    assert lib.xattn_status_string(99).decode() == "unknown xattn status"
+
+
+def _fwd(lib, q=16, k=32, v=48, B=1, S=4, nh=2, nkv=1, hd=64, scale=0.125, o=64, lse=80):
+    f = lib.xattn_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 3
+    return f(q, k, v, B, S, nh, nkv, hd, scale, o, lse, None)
+
+
+def test_fwd_argument_checks(lib):
+    # None of these reach the device: each is rejected by the host checks first.
+    assert _fwd(lib, q=None) == 1                      # NULL pointer
+    assert _fwd(lib, lse=None) == 1
+    assert _fwd(lib, B=0) == 2                         # bad shape
+    assert _fwd(lib, S=-1) == 2
+    assert _fwd(lib, nh=3, nkv=2) == 3                 # nh % nkv != 0
+    assert _fwd(lib, hd=48) == 4                       # unsupported head dim for bf16
+    assert _fwd(lib, hd=128) == 4
+    assert _fwd(lib, q=18) == 5                        # not 16-byte aligned
+    assert _fwd(lib, scale=float("nan")) == 9
+    assert _fwd(lib, scale=float("inf")) == 9
+
+
+def test_f32_head_dim_limit(lib):
+    f = lib.xattn_fwd_f32
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 3
+    assert f(16, 32, 48, 1, 4, 2, 1, 129, 0.1, 64, 80, None) == 4
+
+
+def test_workspace_checks(lib):
+    lib.xattn_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.xattn_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 4
+    n = lib.xattn_bwd_workspace_bytes(2, 200, 4, 64)
+    # D and LSE2 rows padded to 256 (=2 tiles): 2*4*256*4 B each; accumulator 2*200*4*64*4 B.
+    assert n == 2 * (2 * 4 * 256 * 4) + 2 * 200 * 4 * 64 * 4
+    assert lib.xattn_bwd_workspace_bytes(0, 200, 4, 64) == 0
+    f = lib.xattn_bwd_dq_convert
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert f(2, 200, 4, 64, 256, None, n, None) == 10          # NULL workspace
+    assert f(2, 200, 4, 64, 256, 4096 + 16, n, None) == 10     # not 256-byte aligned
+    assert f(2, 200, 4, 64, 256, 4096, n - 1, None) == 10      # too small
+
+
+def test_no_device_is_a_cuda_error(lib):
+    """With valid arguments and no usable GPU, the call fails with XATTN_ERR_CUDA
+    (it never silently does nothing or falls back to the CPU)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _fwd(lib) == 6

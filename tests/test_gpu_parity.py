@@ -1,0 +1,131 @@
+"""Parity of the CUDA path (through the C ABI) with the oracle, on the seeded workloads
+and on edge shapes. Tolerances: bf16 max|err|/max|ref| <= 2e-2, fp32 <= 1e-4 (O, dQ,
+dK, dV), LSE absolute <= 1e-3."""
+import numpy as np
+import pytest
+import torch
+
+from bwd_xattn_fwd_gb300 import workloads as W
+from gpu_path import (TOL_BF16, check_invariants, compare, gpu_unit, oracle_full, oracle_unit,
+                      run_gpu, tol_for)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA device required for -m gpu tests")
+    from bwd_xattn_fwd_gb300 import xattn  # noqa: F401  (fails loudly if not built)
+
+
+# Units compared element by element at full size: first and last batch, first and last kv head.
+def _units(w):
+    return sorted({(0, 0), (w.B - 1, w.nkv - 1), (w.B // 2, w.nkv // 2)})
+
+
+@pytest.mark.parametrize("name", ["tiny", "dim384"])
+def test_workload_full(name):
+    w = W.WORKLOADS[name]
+    x = W.make_inputs(w)
+    out = run_gpu(w, x)
+    ref = oracle_full(w, x)
+    print(name, compare(out, ref, w.dtype, name))
+
+
+@pytest.mark.parametrize("name", ["dim768", "gqa", "long"])
+def test_workload_sampled_units(name):
+    w = W.WORKLOADS[name]
+    x = W.make_inputs(w)
+    out = run_gpu(w, x)
+    for b, kvh in _units(w):
+        rep = compare(gpu_unit(w, out, b, kvh), oracle_unit(w, x, b, kvh), w.dtype,
+                      f"{name} unit (b={b}, kvh={kvh})")
+        print(name, (b, kvh), rep)
+    check_invariants(w, x, out, tol=TOL_BF16)
+
+
+EDGE = [
+    # (B, S, nh, nkv, hd) -- partial tiles, S = 1, one tile, group > 1, hd 32 and 64
+    (1, 1, 2, 1, 64),
+    (2, 77, 4, 2, 64),
+    (1, 128, 2, 2, 32),
+    (1, 129, 3, 1, 64),
+    (2, 200, 6, 3, 32),
+    (1, 300, 4, 1, 64),
+    (1, 513, 2, 2, 64),
+]
+
+
+@pytest.mark.parametrize("shape", EDGE, ids=lambda s: "B%d_S%d_nh%d_nkv%d_hd%d" % s)
+def test_edge_shapes_bf16(shape):
+    B, S, nh, nkv, hd = shape
+    w = W.Workload("edge", B, S, nh, nkv, hd, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=3)
+    compare(run_gpu(w, x), oracle_full(w, x), "bf16", str(shape))
+
+
+EDGE_F32 = [(1, 1, 1, 1, 8), (2, 37, 6, 3, 24), (1, 150, 4, 2, 128), (1, 64, 2, 1, 1)]
+
+
+@pytest.mark.parametrize("shape", EDGE_F32, ids=lambda s: "B%d_S%d_nh%d_nkv%d_hd%d" % s)
+def test_edge_shapes_f32(shape):
+    B, S, nh, nkv, hd = shape
+    w = W.Workload("edge32", B, S, nh, nkv, hd, "f32")
+    x = W.make_inputs(w, seed=4)
+    compare(run_gpu(w, x), oracle_full(w, x), "f32", str(shape))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_gqa_equals_repeated_mha(dtype):
+    """GQA on (K, V) equals MHA on K/V repeated per group, with dK/dV summed per group
+    (the broadcast and its backward of xtrain docs/evolution.md, row T15). The forward
+    is bit-identical: each query head reads the same K/V values either way."""
+    w = W.Workload("g", 2, 256, 8, 2, 64 if dtype == "bf16" else 32, dtype, qkv_scale=0.5)
+    x = W.make_inputs(w, seed=5)
+    g = w.group
+    xr = dict(x)
+    xr["k"] = x["k"].repeat_interleave(g, dim=2).contiguous()
+    xr["v"] = x["v"].repeat_interleave(g, dim=2).contiguous()
+    wr = w.with_(nkv=w.nh)
+    a = run_gpu(w, x)
+    r = run_gpu(wr, xr)
+    assert np.array_equal(a["o"], r["o"]) and np.array_equal(a["lse"], r["lse"])
+    tol = tol_for(dtype)
+    for name in ("dk", "dv"):
+        summed = r[name].reshape(w.B, w.S, w.nkv, g, w.hd).sum(axis=3)
+        e = np.abs(a[name] - summed).max() / np.abs(summed).max()
+        assert e <= tol, (name, e)
+    e = np.abs(a["dq"] - r["dq"]).max() / np.abs(r["dq"]).max()
+    assert e <= tol, ("dq", e)
+
+
+def test_reproducible():
+    """O, LSE, dK and dV are bit-identical run to run; dQ (fp32 atomic accumulation
+    across key tiles) agrees within the bf16 tolerance."""
+    w = W.WORKLOADS["gqa"].with_(B=2)
+    x = W.make_inputs(w, seed=6)
+    a, b = run_gpu(w, x), run_gpu(w, x)
+    for name in ("o", "lse", "dk", "dv"):
+        assert np.array_equal(a[name], b[name]), name
+    assert np.abs(a["dq"] - b["dq"]).max() <= TOL_BF16 * np.abs(a["dq"]).max()
+
+
+def test_stage_calls_match_bwd():
+    """xattn_bwd equals its three steps run with a caller-owned workspace."""
+    from bwd_xattn_fwd_gb300 import xattn
+    w = W.Workload("s", 2, 384, 4, 2, 64, "bf16", qkv_scale=0.5)
+    x = {n: t.cuda() for n, t in W.make_inputs(w, seed=7).items()}
+    o, lse = xattn.attention_fwd(x["q"], x["k"], x["v"], w.scale)
+    dq, dk, dv = xattn.attention_bwd(x["q"], x["k"], x["v"], o, x["dO"], lse, w.scale)
+    nbytes = xattn.xattn_bwd_workspace_bytes(w.B, w.S, w.nh, w.hd)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dq2, dk2, dv2 = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+    xattn.xattn_bwd_preprocess(o, x["dO"], lse, w.B, w.S, w.nh, w.hd, ws, nbytes)
+    xattn.xattn_bwd_main(x["q"], x["k"], x["v"], x["dO"], w.B, w.S, w.nh, w.nkv, w.hd, w.scale,
+                         dk2, dv2, ws, nbytes)
+    xattn.xattn_bwd_dq_convert(w.B, w.S, w.nh, w.hd, dq2, ws, nbytes)
+    torch.cuda.synchronize()
+    assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
+    assert (dq.float() - dq2.float()).abs().max() <= TOL_BF16 * dq.float().abs().max()
+    assert xattn.xattn_check_device_status() == 0
