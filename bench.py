@@ -1,0 +1,416 @@
+"""Benchmark of fused causal GQA attention, forward + backward, on GB300.
+
+One step = the whole hot path over one batch of seeded synthetic input already resident
+in HBM: forward (xattn_fwd), then the backward's three kernels (D/LSE preprocess, main
+recompute loop, dQ convert). The L2 cache (larger than the step's working set) is
+flushed by a 256 MiB device write before every step, outside the timed events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gqa] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0). `value` is fwd+bwd TFLOP/s of algorithmic work
+(4 hd flops per causal pair forward, 10 hd backward) summed over all ranks and divided
+by the slowest rank's time. `--impl reference` times the CPU oracle on the host cores
+instead (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from bwd_xattn_fwd_gb300 import workloads as W  # noqa: E402
+
+METRIC = "causal GQA attention fwd+bwd TFLOP/s & tok/s (bf16), % of GB300 tensor peak"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+KERNEL_SOURCES = {
+    "attn_fwd_kernel": ["attn_fwd_sm103.cu", "sm103_ptx.cuh"],
+    "attn_bwd_main_kernel": ["attn_bwd_sm103.cu", "sm103_ptx.cuh"],
+    "bwd_preprocess_kernel": ["attn_bwd_sm103.cu"],
+    "dq_convert_kernel": ["attn_bwd_sm103.cu"],
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="gqa", choices=[n for n in W.ORDER if n != "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"tflops": p["bf16_tflops"], "tflops_sustained": p.get("bf16_tflops_sustained"),
+                "gbs": p["hbm_gbs"], "source": "measured"}
+    return {"tflops": 1900.0, "tflops_sustained": 1700.0, "gbs": 6800.0, "source": "fallback"}
+
+
+def source_sha(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "bwd_xattn_fwd_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu capture, or None if there is none
+    for this kernel and workload or the kernel's source changed since."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f).get(kernel, {}).get(workload)
+    if not rec or rec.get("source_sha") != source_sha(kernel):
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ---------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]),
+                             "power": float(parts[3]) if parts[3] not in ("[N/A]", "") else None,
+                             "hw": parts[5], "hw_th": parts[6], "sw_th": parts[7], "pcap": parts[8]})
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] is None or r["power"] > 200.0] or rows
+        reasons = []
+        for key, name in (("hw", "hw_slowdown"), ("hw_th", "hw_thermal_slowdown"),
+                          ("sw_th", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+            if any(r[key].lower() == "active" for r in loaded):
+                reasons.append(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": reasons,
+                "samples": len(loaded)}
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; no collective on the data path)
+# ---------------------------------------------------------------------------------------
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != n_gpus:
+        raise SystemExit(f"--gpus {n_gpus} but WORLD_SIZE={world}")
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl")
+        pg = dist
+    return rank, local, world, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x: float, device) -> float:
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (reported baseline)
+# ---------------------------------------------------------------------------------------
+def oracle_sample(w: W.Workload, x_cpu: dict, budget_s: float, max_units: int | None = None):
+    """Times the oracle (fwd + bwd, all host cores) on whole (batch, kv head) units of the
+    workload, in order, until `budget_s` seconds have passed or max_units are done."""
+    cores = os.cpu_count() or 1
+    os.environ["OMP_NUM_THREADS"] = str(cores)
+    import oracle
+    orc = oracle.default()
+    units = [(b, kvh) for b in range(w.B) for kvh in range(w.nkv)]
+    if max_units is not None:
+        units = units[:max_units]
+    done, elapsed = 0, 0.0
+    for b, kvh in units:
+        q, k, v, dO = (W.as_f64(x_cpu[n][b:b + 1]) for n in ("q", "k", "v", "dO"))
+        uq, uk, uv, udo = oracle.unit_slices(q, k, v, dO, 0, kvh)
+        t0 = time.perf_counter()
+        orc.fwd(uq, uk, uv, w.scale)
+        orc.bwd(uq, uk, uv, udo, w.scale)
+        elapsed += time.perf_counter() - t0
+        done += 1
+        if elapsed >= budget_s:
+            break
+    frac = done / len([(b, k) for b in range(w.B) for k in range(w.nkv)])
+    flops = (w.fwd_flops + w.bwd_flops) * frac
+    return {"flops": flops, "tokens": w.tokens * frac, "seconds": elapsed, "units": done,
+            "cores": cores,
+            "sample": f"{done} of {w.B * w.nkv} (batch, kv-head) units of '{w.name}' at full S={w.S} "
+                      f"({w.group} query heads each), fwd+bwd, fp64, OpenMP over rows"}
+
+
+def run_reference(args, w: W.Workload):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    x = W.make_inputs(w, seed=0)
+    for _ in range(args.warmup):
+        oracle_sample(w, x, budget_s=0.0, max_units=1)
+    per = [oracle_sample(w, x, budget_s=0.0, max_units=1) for _ in range(args.steps)]
+    flops = sum(p["flops"] for p in per)
+    secs = sum(p["seconds"] for p in per)
+    toks = sum(p["tokens"] for p in per)
+    value = flops / secs / 1e12
+    cores = per[0]["cores"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "tok_per_s": toks / secs,
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "nh": w.nh, "nkv": w.nkv, "hd": w.hd,
+                   "step": "one (batch, kv-head) unit, fwd+bwd"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": per[0]["sample"] + " per step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+def run_ours(args, w: W.Workload):
+    import torch
+    rank, local, world, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from bwd_xattn_fwd_gb300 import xattn
+
+    x_cpu = W.make_inputs(w, seed=rank)
+    x = {n: t.to(dev) for n, t in x_cpu.items()}
+    B, S, nh, nkv, hd, scale = w.B, w.S, w.nh, w.nkv, w.hd, w.scale
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((B, S, nh), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    ws_bytes = xattn.xattn_bwd_workspace_bytes(B, S, nh, hd)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    names = ["attn_fwd_kernel", "bwd_preprocess_kernel", "attn_bwd_main_kernel", "dq_convert_kernel"]
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        xattn.xattn_fwd(x["q"], x["k"], x["v"], B, S, nh, nkv, hd, scale, o, lse, stream)
+        if evs:
+            evs[1].record(stream)
+        xattn.xattn_bwd_preprocess(o, x["dO"], lse, B, S, nh, hd, ws, ws_bytes, stream)
+        if evs:
+            evs[2].record(stream)
+        xattn.xattn_bwd_main(x["q"], x["k"], x["v"], x["dO"], B, S, nh, nkv, hd, scale, dk, dv,
+                             ws, ws_bytes, stream)
+        if evs:
+            evs[3].record(stream)
+        xattn.xattn_bwd_dq_convert(B, S, nh, hd, dq, ws, ws_bytes, stream)
+        if evs:
+            evs[4].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    status = xattn.xattn_check_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            step(events[i])
+        torch.cuda.synchronize(dev)
+    barrier(pg)
+    status = xattn.xattn_check_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region")
+
+    per_kernel = {n: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, n in enumerate(names)}
+    step_ms = [ev[0].elapsed_time(ev[4]) for ev in events]
+    total_ms = max_over_ranks(pg, sum(step_ms), dev)
+    ms_per_step = total_ms / args.steps
+    flops_step = w.fwd_flops + w.bwd_flops
+    value = flops_step * world * args.steps / (total_ms * 1e-3) / 1e12
+    tok_s = w.tokens * world * args.steps / (total_ms * 1e-3)
+
+    pk = peaks()
+    kavg = {n: statistics.mean(v) for n, v in per_kernel.items()}
+    S_pad = (S + 127) // 128 * 128
+    elems = B * S * nh * hd
+    kernel_work = {
+        "attn_fwd_kernel": ("tensor", w.fwd_flops),
+        "attn_bwd_main_kernel": ("tensor", w.bwd_flops),
+        "bwd_preprocess_kernel": ("hbm", 2 * elems * 2 + B * S * nh * 4 + 2 * B * nh * S_pad * 4 + elems * 4),
+        "dq_convert_kernel": ("hbm", elems * 4 + elems * 2),
+    }
+    kernels = {}
+    for n in names:
+        bound, work = kernel_work[n]
+        ms = kavg[n]
+        if bound == "tensor":
+            ach = work / (ms * 1e-3) / 1e12
+            kernels[n] = {"ms": ms, "bound": "tensor", "achieved": ach, "unit": "TFLOP/s",
+                          "frac": ach / pk["tflops"], "share": ms / sum(kavg.values())}
+        else:
+            ach = work / (ms * 1e-3) / 1e9
+            kernels[n] = {"ms": ms, "bound": "hbm", "achieved": ach, "unit": "GB/s",
+                          "frac": ach / pk["gbs"], "share": ms / sum(kavg.values())}
+    dominant = max(names, key=lambda n: kavg[n])
+    d = kernels[dominant]
+    bound, work = kernel_work[dominant]
+    roofline = {"kernel": dominant, "bound": d["bound"], "achieved": d["achieved"],
+                "peak": pk["tflops"] if bound == "tensor" else pk["gbs"], "unit": d["unit"],
+                "frac": d["frac"], "traffic": ncu_traffic(dominant, w.name),
+                "algorithmic_per_launch": work, "peak_source": pk["source"] + " (burst)"}
+
+    # End to end through the public API with host buffers: H2D of the step's inputs,
+    # xattn_fwd + xattn_bwd (which takes its own scratch), D2H of every output.
+    e2e = None
+    if not args.no_e2e:
+        h_in = {n: t.pin_memory() for n, t in x_cpu.items()}
+        d_in = {n: torch.empty_like(t, device=dev) for n, t in x_cpu.items()}
+        h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                 for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        d_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+
+        def e2e_step():
+            for n in h_in:
+                d_in[n].copy_(h_in[n], non_blocking=True)
+            xattn.xattn_fwd(d_in["q"], d_in["k"], d_in["v"], B, S, nh, nkv, hd, scale, o, lse, stream)
+            xattn.xattn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["dO"], lse, B, S, nh, nkv, hd,
+                            scale, dq, dk, dv, stream)
+            for n in h_out:
+                h_out[n].copy_(d_out[n], non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(pg)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t_e2e = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+        if xattn.xattn_check_device_status(stream) != 0:
+            raise RuntimeError("device status in the e2e run")
+        e2e = {"value": flops_step * world * args.steps / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "tok_per_s": w.tokens * world * args.steps / (t_e2e * 1e-3),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = oracle_sample(w, x_cpu, budget_s=12.0)
+        cpu = {"value": r["flops"] / r["seconds"] / 1e12, "unit": "TFLOP/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"],
+               "tok_per_s": r["tokens"] / r["seconds"], "seconds": r["seconds"]}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "S": w.S, "nh": w.nh, "nkv": w.nkv,
+                       "hd": w.hd, "scale": scale,
+                       "parallelism": f"{world} rank(s), each its own batch of (batch, kv-head) units; no collective",
+                       "l2": "flushed before every step (256 MiB device write, outside the timed events)"},
+            "tok_per_s": tok_s,
+            "frac_of_peak": value / world / pk["tflops"],
+            "frac_of_sustained_peak": value / world / pk["tflops_sustained"] if pk["tflops_sustained"] else None,
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * args.steps, "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def main():
+    args = parse()
+    w = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()
