@@ -261,6 +261,8 @@ const char *xattn_status_string(xattn_status s) {
     case XATTN_ERR_DEVICE_TIMEOUT: return "a bounded on-device wait expired";
     case XATTN_ERR_BAD_SCALE: return "scale must be finite";
     case XATTN_ERR_WORKSPACE: return "workspace is NULL, not 256-byte aligned, or too small";
+    case XATTN_ERR_SCRATCH_LIMIT:
+      return "these sizes need more scratch than xattn_bwd_noalloc's fixed array holds";
   }
   return "unknown xattn status";
 }

@@ -41,6 +41,7 @@ class Status(enum.IntEnum):
     ERR_DEVICE_TIMEOUT = 8
     ERR_BAD_SCALE = 9
     ERR_WORKSPACE = 10
+    ERR_SCRATCH_LIMIT = 11
 
 
 class XattnError(RuntimeError):
@@ -57,6 +58,7 @@ _sz = ctypes.c_size_t
 _SIGS = {
     "xattn_fwd": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp],
     "xattn_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp],
+    "xattn_bwd_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp],
     "xattn_bwd_preprocess": [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp],
     "xattn_bwd_main": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _sz, _vp],
     "xattn_bwd_dq_convert": [_i, _i, _i, _i, _vp, _vp, _sz, _vp],
@@ -115,6 +117,17 @@ def xattn_fwd(q, k, v, B, S, nh, nkv, hd, scale, o, lse, stream=None):
 def xattn_bwd(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream=None):
     _call("xattn_bwd", _addr(q), _addr(k), _addr(v), _addr(o), _addr(dO), _addr(lse), B, S, nh,
           nkv, hd, scale, _addr(dq), _addr(dk), _addr(dv), _stream(stream))
+
+
+def xattn_bwd_noalloc(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream=None):
+    """xattn_bwd using the library's fixed device scratch array instead of allocating
+    (for callers that may not allocate device memory). Sizes whose scratch exceeds
+    NOALLOC_SCRATCH_BYTES raise ERR_SCRATCH_LIMIT; overlapping calls race on the array."""
+    _call("xattn_bwd_noalloc", _addr(q), _addr(k), _addr(v), _addr(o), _addr(dO), _addr(lse), B,
+          S, nh, nkv, hd, scale, _addr(dq), _addr(dk), _addr(dv), _stream(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # XATTN_NOALLOC_SCRATCH_BYTES in xattn.h
 
 
 def xattn_bwd_workspace_bytes(B, S, nh, hd) -> int:

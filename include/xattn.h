@@ -57,7 +57,8 @@ typedef enum {
     XATTN_ERR_NO_DEVICE_SUPPORT = 7,  /* the current device is not compute capability 10.3 */
     XATTN_ERR_DEVICE_TIMEOUT = 8,     /* a bounded on-device wait expired (reported later) */
     XATTN_ERR_BAD_SCALE = 9,          /* scale is not finite */
-    XATTN_ERR_WORKSPACE = 10          /* workspace pointer NULL/misaligned or too small */
+    XATTN_ERR_WORKSPACE = 10,         /* workspace pointer NULL/misaligned or too small */
+    XATTN_ERR_SCRATCH_LIMIT = 11      /* xattn_bwd_noalloc: sizes need more than its fixed scratch */
 } xattn_status;
 
 /*
@@ -106,6 +107,30 @@ xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const v
                             void *dv, void *workspace, size_t workspace_bytes, void *stream);
 xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, void *dq, void *workspace,
                                   size_t workspace_bytes, void *stream);
+
+/*
+ * xattn_bwd with no allocation at all. The pages have no counterpart: this entry point
+ * exists for callers that may not allocate device memory, such as a loop running under
+ * a no-allocation rule once started (cudaFree synchronises the whole device), or a host
+ * whose device memory is already fully reserved by its own allocator, so the
+ * cudaMallocAsync inside xattn_bwd would fail.
+ *
+ * Same arguments and results as xattn_bwd. The scratch (xattn_bwd_workspace_bytes(B, S,
+ * nh, hd) bytes) lives in one fixed device array of XATTN_NOALLOC_SCRATCH_BYTES inside
+ * the library; every GPU that loads the library holds that array until the process
+ * exits. Sizes that need more return XATTN_ERR_SCRATCH_LIMIT before anything is
+ * launched (64 MiB fits, e.g., B=8, S=2048, nh=8, hd=64).
+ * The first call on a device looks up the array's device address for that device
+ * (cudaGetSymbolAddress); make that first call before any stream capture on the device.
+ * All calls share the one array and each call overwrites all of the scratch it uses, so
+ * nothing carries over between calls, but calls whose work overlaps on the GPU (on
+ * different streams, or from different threads) race on it and must be serialised by
+ * the caller.
+ */
+#define XATTN_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+xattn_status xattn_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                               const void *dO, const float *lse, int B, int S, int nh, int nkv,
+                               int hd, float scale, void *dq, void *dk, void *dv, void *stream);
 
 /*
  * fp32 mode: same parameters and layouts, float tensors, IEEE fp32 arithmetic on the

@@ -43,11 +43,11 @@ def test_binding_exposes_the_same_names():
 def test_status_strings(lib):
     lib.xattn_status_string.restype = ctypes.c_char_p
     seen = set()
-    for code in range(0, 11):
+    for code in range(0, 12):
         s = lib.xattn_status_string(code).decode()
         assert s and s != "unknown xattn status"
         seen.add(s)
-    assert len(seen) == 11
+    assert len(seen) == 12
     assert lib.xattn_status_string(99).decode() == "unknown xattn status"
 
 

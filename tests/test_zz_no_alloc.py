@@ -1,0 +1,58 @@
+"""xattn_bwd_noalloc: the backward for callers that may not allocate device memory
+(a loop under a no-allocation rule, or a host whose device memory is all reserved by
+its own allocator). It runs on the library's fixed device scratch array instead of
+cudaMallocAsync; its results must match xattn_bwd's.
+
+This file is collected last on purpose, so a run that stops at the first failure has
+already run every other test."""
+import pytest
+import torch
+
+from bwd_xattn_fwd_gb300 import workloads as W
+from gpu_path import TOL_BF16
+
+pytestmark = pytest.mark.gpu
+
+
+def _max_rel(a, b):
+    a, b = a.float(), b.float()
+    return float((a - b).abs().max() / b.abs().max().clamp_min(1e-4))
+
+
+def test_noalloc_matches_bwd_on_two_calls_in_a_row():
+    from bwd_xattn_fwd_gb300 import xattn
+    # Two consecutive calls with different shapes and inputs: the second one uses less
+    # of the shared scratch array than the first (shorter S, smaller head dim, partial
+    # tiles), so stale contents from the first call would show up in its results.
+    cases = [W.Workload("na1", B=2, S=384, nh=8, nkv=2, hd=64, dtype="bf16", qkv_scale=0.5),
+             W.Workload("na2", B=1, S=300, nh=6, nkv=3, hd=32, dtype="bf16", qkv_scale=0.5)]
+    for seed, w in enumerate(cases, start=11):
+        assert xattn.xattn_bwd_workspace_bytes(w.B, w.S, w.nh, w.hd) <= xattn.NOALLOC_SCRATCH_BYTES
+        x = {n: t.cuda() for n, t in W.make_inputs(w, seed=seed).items()}
+        q, k, v, dO = x["q"], x["k"], x["v"], x["dO"]
+        o, lse = xattn.attention_fwd(q, k, v, w.scale)
+        dq, dk, dv = xattn.attention_bwd(q, k, v, o, dO, lse, w.scale)
+        dq2, dk2, dv2 = (torch.full_like(t, float("nan")) for t in (dq, dk, dv))
+        xattn.xattn_bwd_noalloc(q, k, v, o, dO, lse, w.B, w.S, w.nh, w.nkv, w.hd, w.scale,
+                                dq2, dk2, dv2)
+        torch.cuda.synchronize()
+        assert xattn.xattn_check_device_status() == 0
+        for name, got, ref in (("dq", dq2, dq), ("dk", dk2, dk), ("dv", dv2, dv)):
+            assert torch.isfinite(got).all(), (w.name, name)
+            e = _max_rel(got, ref)
+            assert e <= TOL_BF16, f"{w.name} {name}: max|err|/max|ref| = {e:.3e}"
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    from bwd_xattn_fwd_gb300 import xattn
+    B, S, nh, nkv, hd = 32, 1024, 12, 12, 64      # needs ~100 MB of scratch
+    assert xattn.xattn_bwd_workspace_bytes(B, S, nh, hd) > xattn.NOALLOC_SCRATCH_BYTES
+    # Small stand-in buffers: the call must refuse before it touches any of them.
+    t = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(64, dtype=torch.float32, device="cuda")
+    dq = torch.full((64,), 7.0, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(xattn.XattnError) as err:
+        xattn.xattn_bwd_noalloc(t, t, t, t, t, lse, B, S, nh, nkv, hd, 0.125, dq, dq, dq)
+    assert err.value.status == xattn.Status.ERR_SCRATCH_LIMIT
+    torch.cuda.synchronize()
+    assert bool((dq == 7.0).all())
