@@ -15,13 +15,14 @@
 //      dK/dV, and a fixed order, so they are reproducible. Per (r, m):
 //        S^T  = K_n Q_m^T               (TMEM, 128 x 128 fp32)
 //        dP^T = V_n dO_m^T              (TMEM, 128 x 128 fp32)
-//        P^T  = exp2(S^T scale log2e - LSE2_m)      -> bf16 into TMEM over S^T
-//        dS^T = scale * P^T (dP^T - D_m)            -> bf16 into TMEM over dP^T, and
+//        P^T  = exp2(S^T scale log2e - LSE2_m)      -> bf16 into a TMEM slot
+//        dS^T = scale * P^T (dP^T - D_m)            -> bf16 into the same slot, and
 //                                                      into shared memory (MN-major)
 //        dV_n += P^T dO_m ,  dK_n += dS^T Q_m       (A operand from TMEM)
 //        dQ_m  = dS K_n                 (TMEM) -> fp32 atomic adds into the accumulator
-//      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 4-7 = P/dS (one thread per
-//      key row), 8-11 = dQ drain (one thread per query row).
+//      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 4-11 = P/dS (one thread
+//      per key row, two warps per row splitting the 128 query columns), which also
+//      drain each dQ tile from TMEM.
 //   3. dq convert: dq = bf16(accumulator).
 #include "sm103_ptx.cuh"
 #include "xattn_internal.h"
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
 // ------------------------------------------------------------------------------------
 // 2. main kernel
 // ------------------------------------------------------------------------------------
-constexpr int kBwdThreads = 384;
+constexpr int kBwdThreads = 384;  // 12 warps, see the role map in the kernel
 
 template <int HD>
 struct BwdLayout {
@@ -159,8 +160,23 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
   return static_cast<uint32_t>((i >> 6) * 16384 + j * 128 + ((((i & 63) >> 3) ^ (j & 7)) << 4));
 }
 
+// Role map (12 warps; registers are split evenly over the 4 SM sub-partitions, so 12
+// warps leave 168 per thread):
+//   warp 0     : TMA producer
+//   warp 1     : TMEM owner and MMA issuer
+//   warps 2-3  : idle
+//   warps 4-11 : P^T / dS^T, one thread per key row; warps 4-7 take query columns 0-63
+//                and warps 8-11 columns 64-127 (two warps per lane quarter, so each SM
+//                sub-partition interleaves two of them). They also drain dQ(t-1) from
+//                TMEM into the fp32 accumulator (one query row per thread, each half
+//                taking half of the head dimension).
+// TMEM columns: S^T [0,128) fp32 | dP^T [128,256) fp32 | P^T, then dS^T, bf16 [256,320)
+//               | dV [320,384) | dK [384,448) | dQ [448,512)
+// P^T and dS^T share one slot that no other result overlaps, so the two column halves
+// never write over values the other half still has to read; the MMA readers of that
+// slot (dV reads P^T, dK reads dS^T) are waited for before it is overwritten.
 template <int HD>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __maxnreg__(168)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                          const float *__restrict__ Dvec, const float *__restrict__ lse2,
@@ -213,10 +229,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(ds_full, 128);
+    mbar_init(p_full, 256);
+    mbar_init(ds_full, 256);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
+    mbar_init(dq_empty, 256);
     mbar_init(acc_done, 1);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
@@ -236,7 +252,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 320, tdQ = tmem + 384;
+  const uint32_t tS = tmem, tdP = tmem + 128, tP = tmem + 256;
+  const uint32_t tdV = tmem + 320, tdK = tmem + 384, tdQ = tmem + 448;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -276,12 +293,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           mma_ss(d, a, bd, idesc_t, kk > 0);
         }
       };
-      auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint32_t b_base, bool first) {
+      auto issue_acc = [&](uint32_t d, uint32_t b_base, bool first) {
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk) {
           const uint64_t bd = smem_desc(b_base + kk * 16 * L::kRowBytes, 8192, 8 * L::kRowBytes,
                                         L::kSwizzle);
-          mma_ts(d, a_tmem + kk * 8, bd, idesc_acc, (!first || kk > 0) ? 1u : 0u);
+          mma_ts(d, tP + kk * 8, bd, idesc_acc, (!first || kk > 0) ? 1u : 0u);
         }
       };
       bool ok = mbar_wait(kv_full, 0, ctl) && mbar_wait(full(0), 0, ctl);
@@ -294,23 +311,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       for (int t = 0; ok && t < T; ++t) {
         const int s = t & 1;
+        const bool more = t + 1 < T;
         if (!mbar_wait(p_full, t & 1, ctl)) break;
         tc_fence_after();
-        issue_acc(tdV, tS, sdO + s * L::kTileBytes, t == 0);             // dV += P^T dO
+        issue_acc(tdV, sdO + s * L::kTileBytes, t == 0);                   // dV += P^T dO
         mma_commit(dv_done);
-        const bool more = t + 1 < T;
         if (more) {
           if (!mbar_wait(full(s ^ 1), ((t + 1) >> 1) & 1, ctl)) break;
-          // S^T(t+1) overwrites the P^T that dV(t) reads; MMAs into different
-          // accumulators are not ordered by issue, so wait for dV(t).
-          if (!mbar_wait(dv_done, t & 1, ctl)) break;
           tc_fence_after();
-          issue_kmajor(tS, sK, sQ + (s ^ 1) * L::kTileBytes);             // S^T(t+1)
+          issue_kmajor(tS, sK, sQ + (s ^ 1) * L::kTileBytes);               // S^T(t+1)
           mma_commit(s_full);
         }
         if (!mbar_wait(ds_full, t & 1, ctl)) break;
         tc_fence_after();
-        issue_acc(tdK, tdP, sQ + s * L::kTileBytes, t == 0);               // dK += dS^T Q
+        issue_acc(tdK, sQ + s * L::kTileBytes, t == 0);                    // dK += dS^T Q
         mma_commit(empty(s));
         mma_commit(dk_done);
         if (!mbar_wait(dq_empty, (t & 1) ^ 1, ctl)) break;
@@ -324,75 +338,119 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(dq_full);
         if (more) {
-          // dP^T(t+1) overwrites the dS^T that dK(t) reads.
-          if (!mbar_wait(dk_done, t & 1, ctl)) break;
-          tc_fence_after();
-          issue_kmajor(tdP, sV, sdO + (s ^ 1) * L::kTileBytes);           // dP^T(t+1)
+          issue_kmajor(tdP, sV, sdO + (s ^ 1) * L::kTileBytes);             // dP^T(t+1)
           mma_commit(dp_full);
         }
       }
       mma_commit(acc_done);
       mbar_drain(acc_done, 0, ctl);
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ---------------- P^T and dS^T: one thread per key row ----------------
+  } else if (warp >= 4) {
+    // ---------------- P^T and dS^T: one thread per key row, half the query columns -----
+    const int g = (warp - 4) >> 2;           // column half
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col_f32 = 64u * g, col_bf16 = 32u * g;
+    constexpr int kHalf = HD / 2;
+    // dQ(tt) from TMEM (query row j of its tile, head-dim half g) into the accumulator.
+    auto drain_dq = [&](int tt) {
+      const int r_h = tt / per_head, m_t = n + tt % per_head;
+      const int h = kvh * group + r_h;
+      uint32_t v[kHalf];
+      if constexpr (kHalf == 32) tmem_ld_x32(tdQ + lane_off + kHalf * g, v);
+      else tmem_ld_x16(tdQ + lane_off + kHalf * g, v);
+      tmem_wait_ld();
+      reg_fence<kHalf>(v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      const int ig = m_t * kTileRows + j;
+      if (ig < S) {
+        float4 *dst = reinterpret_cast<float4 *>(
+            dqacc + ((static_cast<size_t>(b) * S + ig) * nh + h) * HD + kHalf * g);
+#pragma unroll
+        for (int e = 0; e < kHalf / 4; ++e)
+          atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+      }
+    };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int m = n + t % per_head;
       const int s = t & 1;
       const bool diag = (m == n);
-      const float *lse_s = sLSE + s * 128;
-      const float *D_s = sD + s * 128;
-      // Phase 1: P^T
+      // Phase 1: P^T = exp2(S^T scale log2e - LSE2), masked above the diagonal.
       if (!warp_wait(s_full, t & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t pk[64];
+      uint32_t r[64];
+      tmem_ld_x32(tS + lane_off + col_f32, r);
+      tmem_ld_x32(tS + lane_off + col_f32 + 32, r + 32);
+      tmem_wait_ld();
+      reg_fence<64>(r);
+      const float4 *lse4 = reinterpret_cast<const float4 *>(sLSE + s * 128 + col_f32);
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(tS + lane_off + c, r);
-        tmem_wait_ld();
-        reg_fence<32>(r);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i0 = c + 2 * e, i1 = i0 + 1;
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * e]), scale_log2, -lse_s[i0]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * e + 1]), scale_log2, -lse_s[i1]));
-          if (diag && i0 < j) p0 = 0.f;
-          if (diag && i1 < j) p1 = 0.f;
-          pk[c / 2 + e] = pack_bf16x2(p0, p1);
+      for (int q4 = 0; q4 < 16; ++q4) {
+        const float4 l4 = lse4[q4];
+        const int i = static_cast<int>(col_f32) + 4 * q4;
+        float p0 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 0]), scale_log2, -l4.x));
+        float p1 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 1]), scale_log2, -l4.y));
+        float p2 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 2]), scale_log2, -l4.z));
+        float p3 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 3]), scale_log2, -l4.w));
+        if (diag) {
+          if (i + 0 < j) p0 = 0.f;
+          if (i + 1 < j) p1 = 0.f;
+          if (i + 2 < j) p2 = 0.f;
+          if (i + 3 < j) p3 = 0.f;
         }
-        tmem_st_x16(tS + lane_off + c / 2, pk + c / 2);
+        pk[2 * q4] = pack_bf16x2(p0, p1);
+        pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
       }
+      // The P^T slot still holds dS^T(t-1) until dK(t-1) has read it.
+      if (t > 0 && !warp_wait(dk_done, (t - 1) & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      tmem_st_x16(tP + lane_off + col_bf16, pk);
+      tmem_st_x16(tP + lane_off + col_bf16 + 16, pk + 16);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full);
-      // Phase 2: dS^T
+
+      // Phase 2: dS^T = scale P^T (dP^T - D).
       if (!warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
-      if (t > 0 && !warp_wait(dq_full, (t - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
+      tmem_ld_x32(tdP + lane_off + col_f32, r);
+      tmem_ld_x32(tdP + lane_off + col_f32 + 32, r + 32);
+      tmem_wait_ld();
+      reg_fence<64>(r);
+      // dQ(t-1) must be done reading the shared-memory copy of dS (its result is drained
+      // here), and dV(t) must be done reading P^T before dS^T replaces it in TMEM.
+      if (t > 0) {
+        if (!warp_wait(dq_full, (t - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        drain_dq(t - 1);
+      }
+      if (!warp_wait(dv_done, t & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      const float4 *d4 = reinterpret_cast<const float4 *>(sD + s * 128 + col_f32);
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(tdP + lane_off + c, r);
-        tmem_wait_ld();
-        reg_fence<32>(r);
+      for (int half = 0; half < 2; ++half) {
         uint32_t dsk[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i0 = c + 2 * e;
-          const uint32_t p = pk[c / 2 + e];
-          const float ds0 = bf16lo_to_f32(p) * (__uint_as_float(r[2 * e]) - D_s[i0]) * scale;
-          const float ds1 = bf16hi_to_f32(p) * (__uint_as_float(r[2 * e + 1]) - D_s[i0 + 1]) * scale;
-          dsk[e] = pack_bf16x2(ds0, ds1);
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const int c = half * 32 + 4 * q4;
+          const float4 dd = d4[c / 4];
+          const uint32_t pa = pk[c / 2], pb = pk[c / 2 + 1];
+          const float ds0 = bf16lo_to_f32(pa) * (__uint_as_float(r[c + 0]) - dd.x) * scale;
+          const float ds1 = bf16hi_to_f32(pa) * (__uint_as_float(r[c + 1]) - dd.y) * scale;
+          const float ds2 = bf16lo_to_f32(pb) * (__uint_as_float(r[c + 2]) - dd.z) * scale;
+          const float ds3 = bf16hi_to_f32(pb) * (__uint_as_float(r[c + 3]) - dd.w) * scale;
+          dsk[2 * q4] = pack_bf16x2(ds0, ds1);
+          dsk[2 * q4 + 1] = pack_bf16x2(ds2, ds3);
         }
-        tmem_st_x16(tdP + lane_off + c / 2, dsk);
+        tmem_st_x16(tP + lane_off + col_bf16 + 16 * half, dsk);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, c + 8 * e)) =
+          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, static_cast<int>(col_f32) + half * 32 + 8 * e)) =
               make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
       }
       tmem_wait_st();
@@ -400,57 +458,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tc_fence_before();
       mbar_arrive(ds_full);
     }
-    // Epilogue: dV and dK rows of this key tile (dK already carries the scale).
+    // Epilogue: drain the last dQ; then the first column half stores dV rows, the
+    // second dK rows (dK already carries the scale).
+    if (ok && warp_wait(dq_full, (T - 1) & 1, ctl)) {
+      tc_fence_after();
+      drain_dq(T - 1);
+    } else {
+      ok = false;
+    }
     if (ok && warp_wait(acc_done, 0, ctl)) {
       tc_fence_after();
       const int jg = n * kTileRows + j;
       const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
+      const uint32_t tsrc = g == 0 ? tdV : tdK;
+      __nv_bfloat16 *dst_row = (g == 0 ? dv : dk) + row_off;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t tsrc = which == 0 ? tdV : tdK;
-        __nv_bfloat16 *dst_row = (which == 0 ? dv : dk) + row_off;
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(tsrc + lane_off + c, v);
+        tmem_wait_ld();
+        reg_fence<32>(v);
+        if (jg < S) {
+          uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
 #pragma unroll
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t r[32];
-          tmem_ld_x32(tsrc + lane_off + c, r);
-          tmem_wait_ld();
-          reg_fence<32>(r);
-          if (jg < S) {
-            uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dst[e] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * e]), __uint_as_float(r[8 * e + 1])),
-                                  pack_bf16x2(__uint_as_float(r[8 * e + 2]), __uint_as_float(r[8 * e + 3])),
-                                  pack_bf16x2(__uint_as_float(r[8 * e + 4]), __uint_as_float(r[8 * e + 5])),
-                                  pack_bf16x2(__uint_as_float(r[8 * e + 6]), __uint_as_float(r[8 * e + 7])));
-          }
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]), __uint_as_float(v[8 * e + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7])));
         }
-      }
-    }
-  } else if (warp >= 8) {
-    // ---------------- dQ drain: one thread per query row ----------------
-    const int quarter = warp & 3;
-    const int i = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    for (int t = 0; t < T; ++t) {
-      const int r = t / per_head, m = n + t % per_head;
-      const int h = kvh * group + r;
-      if (!warp_wait(dq_full, t & 1, ctl)) break;
-      tc_fence_after();
-      uint32_t v[HD];
-#pragma unroll
-      for (int c = 0; c < HD; c += 32) tmem_ld_x32(tdQ + lane_off + c, v + c);
-      tmem_wait_ld();
-      reg_fence<HD>(v);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      const int ig = m * kTileRows + i;
-      if (ig < S) {
-        float4 *dst = reinterpret_cast<float4 *>(dqacc + ((static_cast<size_t>(b) * S + ig) * nh + h) * HD);
-#pragma unroll
-        for (int e = 0; e < HD / 4; ++e)
-          atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
       }
     }
   }

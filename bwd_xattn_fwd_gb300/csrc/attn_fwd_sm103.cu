@@ -5,17 +5,17 @@
 // log-sum-exp is kept for the backward. Grouped KV heads (row T15): query head h reads
 // kv head h / group.
 //
-// GB300 mapping (one CTA per 128-row query tile, 8 warps):
-//   warp 0    : TMA producer. Q tile once; K/V tiles into a 3-stage shared-memory ring.
-//   warp 1    : allocates TMEM; one lane issues tcgen05.mma:
-//                 S_n  = Q K_n^T  (A, B from shared memory)      -> TMEM, double-buffered
-//                 O   += P_n V_n  (A = P from TMEM, B from smem) -> TMEM accumulator
-//   warps 4-7 : softmax, one thread per query row (TMEM lane). Loads S_n, applies the
-//               causal mask on the diagonal tile, keeps the running max and sum in fp32
-//               (log2 domain), writes P_n (bf16) over S_n in TMEM, and rescales O only
-//               when the running max grows by more than 2^8 (the stale max is exact
-//               because the final normalisation uses the same max). Epilogue: O / l in
-//               bf16 and LSE = (m + log2 l) ln 2.
+// GB300 mapping (one CTA per 128-row query tile, 12 warps):
+//   warp 0     : TMA producer. Q tile once; K/V tiles into a 3-stage shared-memory ring.
+//   warp 1     : allocates TMEM; one lane issues tcgen05.mma:
+//                  S_n  = Q K_n^T  (A, B from shared memory)      -> TMEM, double-buffered
+//                  O   += P_n V_n  (A = P from TMEM, B from smem) -> TMEM accumulator
+//   warps 4-11 : softmax, one thread per query row (TMEM lane) and key-column half.
+//                Loads S_n, applies the causal mask on the diagonal tile, keeps the
+//                running max and sum in fp32 (log2 domain), writes P_n (bf16) to TMEM,
+//                and rescales O only when the running max grows by more than 2^8 (the
+//                stale max is exact because the final normalisation uses the same max).
+//                Epilogue: O / l in bf16 and LSE = (m + log2 l) ln 2.
 // Causal tile skipping: query tile m visits key tiles 0..m only. Tiles are issued
 // longest first (m descending) so the last wave holds short tiles.
 #include "sm103_ptx.cuh"
@@ -24,7 +24,7 @@
 namespace xattn {
 namespace {
 
-constexpr int kFwdThreads = 256;
+constexpr int kFwdThreads = 384;  // 12 warps, see the role map in the kernel
 constexpr int kFwdStages = 3;
 
 template <int HD>
@@ -35,9 +35,10 @@ struct FwdLayout {
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kK = kQ + kTileBytes;
   static constexpr uint32_t kV = kK + kFwdStages * kTileBytes;
-  static constexpr uint32_t kBars = kV + kFwdStages * kTileBytes;
-  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done, mma_final
-  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2;
+  static constexpr uint32_t kRed = kV + kFwdStages * kTileBytes;  // max [2][2][128], l [2][128]
+  static constexpr uint32_t kBars = kRed + 3 * 1024;
+  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done, mma_final, pair[4]
+  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 4;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   // Ask for enough shared memory that one CTA occupies an SM: each CTA holds all 512
@@ -51,13 +52,36 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(0xffffffffu, ok);
 }
 
+// TMEM <-> registers for half an O row (HD/2 columns).
+template <int N>
+__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, uint32_t *r) {
+  if constexpr (N == 32) tmem_ld_x32(taddr, r);
+  else tmem_ld_x16(taddr, r);
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_half(uint32_t taddr, const uint32_t *r) {
+  if constexpr (N == 32) tmem_st_x32(taddr, r);
+  else tmem_st_x16(taddr, r);
+}
+
+// Role map (12 warps):
+//   warp 0    : TMA producer (Q once, K/V through a 3-stage ring)
+//   warp 1    : TMEM owner and MMA issuer
+//   warps 2-3 : idle
+//   warps 4-11: softmax, one thread per query row; warps 4-7 take key columns 0-63 of
+//               each 128-column tile and warps 8-11 columns 64-127, so each SM
+//               sub-partition interleaves two softmax warps. The two halves of a row
+//               exchange their partial maxima through shared memory each tile.
+// TMEM columns: S double buffer [0,128) [128,256) fp32 | O [256,256+HD) fp32 |
+//               P double buffer [320,384) [384,448) bf16
 template <int HD>
-__global__ void __launch_bounds__(kFwdThreads, 1)
+__global__ void __maxnreg__(168)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, __nv_bfloat16 *__restrict__ o,
                     float *__restrict__ lse, int B, int S, int nh, int nkv, float scale_log2,
                     int *status, unsigned long long timeout_ns) {
   using L = FwdLayout<HD>;
+  constexpr int kHalf = HD / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -75,6 +99,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sK = smem_u32(smem + L::kK);
   const uint32_t sV = smem_u32(smem + L::kV);
+  float *red_max = reinterpret_cast<float *>(smem + L::kRed);          // [2 tiles][2 halves][128]
+  float *red_l = reinterpret_cast<float *>(smem + L::kRed + 2048);     // [2 halves][128]
   const uint32_t bar0 = smem_u32(smem + L::kBars);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const uint32_t q_full = bar(0);
@@ -84,6 +110,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   auto p_full = [&](int x) { return bar(3 + 2 * kFwdStages + x); };
   const uint32_t o_done = bar(5 + 2 * kFwdStages);
   const uint32_t mma_final = bar(6 + 2 * kFwdStages);
+  auto pair_bar = [&](int q) { return bar(7 + 2 * kFwdStages + q); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -95,12 +122,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    mbar_init(s_full(0), 1);
-    mbar_init(s_full(1), 1);
-    mbar_init(p_full(0), 128);
-    mbar_init(p_full(1), 128);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(s_full(x), 1);
+      mbar_init(p_full(x), 256);
+    }
     mbar_init(o_done, 1);
     mbar_init(mma_final, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(pair_bar(q), 64);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -118,6 +146,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS[2] = {tmem, tmem + 128};
   const uint32_t tO = tmem + 256;
+  const uint32_t tP[2] = {tmem + 320, tmem + 384};
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -160,12 +189,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       for (int n = 0; ok && n < n_kv; ++n) {
         if (n + 1 < n_kv) {
+          // S(n+1) goes into the buffer of S(n-1), which the softmax finished reading
+          // before it signalled P(n-1) (waited for in the previous iteration).
           const int s1 = (n + 1) % kFwdStages;
           if (!mbar_wait(full(s1), ((n + 1) / kFwdStages) & 1, ctl)) break;
-          // S(n+1) overwrites the TMEM buffer that holds P(n-1). MMAs into different
-          // accumulators are not ordered by issue, so P(n-1)'s reader, PV(n-1), must
-          // have completed first.
-          if (n > 0 && !mbar_wait(o_done, (n - 1) & 1, ctl)) break;
           tc_fence_after();
           issue_qk(tS[(n + 1) & 1], s1);
           mma_commit(s_full((n + 1) & 1));
@@ -173,12 +200,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         if (!mbar_wait(p_full(n & 1), (n >> 1) & 1, ctl)) break;
         tc_fence_after();
         const int s = n % kFwdStages;
-        const uint32_t tP = tS[n & 1];
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk) {
           const uint64_t bdesc = smem_desc(sV + s * L::kTileBytes + kk * 16 * L::kRowBytes,
                                            8192, 8 * L::kRowBytes, L::kSwizzle);
-          mma_ts(tO, tP + kk * 8, bdesc, idesc_pv, (n > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tO, tP[n & 1] + kk * 8, bdesc, idesc_pv, (n > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(empty(s));
         mma_commit(o_done);
@@ -187,69 +213,78 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_drain(mma_final, 0, ctl);
     }
   } else if (warp >= 4) {
-    // ---------------- softmax + epilogue (one thread per query row) ----------------
+    // ---------------- softmax + epilogue ----------------
+    const int g = (warp - 4) >> 2;           // key-column half of every tile
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float mrow = -INFINITY, lrow = 0.f;
+    const uint32_t pbar = pair_bar(quarter);
+    uint32_t pair_phase = 0;
+    float mrow = -INFINITY, lpart = 0.f;
     bool ok = true;
     for (int n = 0; n < n_kv; ++n) {
       if (!warp_wait(s_full(n & 1), (n >> 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[128];
-      tmem_ld_x32(tS[n & 1] + lane_off + 0, r);
-      tmem_ld_x32(tS[n & 1] + lane_off + 32, r + 32);
-      tmem_ld_x32(tS[n & 1] + lane_off + 64, r + 64);
-      tmem_ld_x32(tS[n & 1] + lane_off + 96, r + 96);
+      uint32_t r[64];
+      tmem_ld_x32(tS[n & 1] + lane_off + 64 * g, r);
+      tmem_ld_x32(tS[n & 1] + lane_off + 64 * g + 32, r + 32);
       tmem_wait_ld();
-      reg_fence<128>(r);
+      reg_fence<64>(r);
       const bool diag = (n == m);
-      float mx = -INFINITY;
+      const int col0 = 64 * g;
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
+      for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
         float x = __uint_as_float(r[c]) * scale_log2;
-        if (diag && c > row) x = -INFINITY;
+        if (diag && col0 + c > row) x = -INFINITY;
         r[c] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+        mx8[c & 7] = fmaxf(mx8[c & 7], x);
       }
+      float pmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // Row maximum across the two column halves (double-buffered by tile parity).
+      red_max[((n & 1) * 2 + g) * 128 + row] = pmax;
+      mbar_arrive(pbar);
+      if (!warp_wait(pbar, pair_phase & 1, ctl)) { ok = false; break; }
+      ++pair_phase;
+      const float mx = fmaxf(pmax, red_max[((n & 1) * 2 + (g ^ 1)) * 128 + row]);
       // Conditional rescaling: keep the stale max unless some row of the warp grew by
-      // more than 2^8; the decision is per warp because TMEM loads/stores are collective.
+      // more than 2^8; the decision is per warp because TMEM loads/stores are collective,
+      // and both halves of a row reach the same decision from the same maxima.
       const float mnew = fmaxf(mrow, mx);
       const bool rescale = __any_sync(0xffffffffu, mnew > mrow + 8.0f);
       const float m_use = rescale ? mnew : mrow;
       const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
-      float psum = 0.f;
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2_approx(__uint_as_float(r[c + 2 * e]) - m_use);
-          const float p1 = ex2_approx(__uint_as_float(r[c + 2 * e + 1]) - m_use);
-          psum += p0 + p1;
-          pk[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_x16(tS[n & 1] + lane_off + c / 2, pk);
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = ex2_approx(__uint_as_float(r[2 * e]) - m_use);
+        const float p1 = ex2_approx(__uint_as_float(r[2 * e + 1]) - m_use);
+        ps[e & 3] += p0 + p1;
+        pk[e] = pack_bf16x2(p0, p1);
       }
+      // P(n) goes into the buffer PV(n-2) read; that PV was waited for last iteration.
+      tmem_st_x16(tP[n & 1] + lane_off + 32 * g, pk);
+      tmem_st_x16(tP[n & 1] + lane_off + 32 * g + 16, pk + 16);
       // PV(n-1) is waited for on every tile, not only when rescaling: a parity wait is
       // only unambiguous if the waiter has seen every earlier phase of the barrier.
       if (n > 0) {
         if (!warp_wait(o_done, (n - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
         if (rescale) {
+          uint32_t ov[kHalf];
+          tmem_ld_half<kHalf>(tO + lane_off + kHalf * g, ov);
+          tmem_wait_ld();
+          reg_fence<kHalf>(ov);
 #pragma unroll
-          for (int c = 0; c < HD; c += 32) {
-            uint32_t ov[32];
-            tmem_ld_x32(tO + lane_off + c, ov);
-            tmem_wait_ld();
-            reg_fence<32>(ov);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st_x32(tO + lane_off + c, ov);
-          }
+          for (int e = 0; e < kHalf; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st_half<kHalf>(tO + lane_off + kHalf * g, ov);
         }
       }
-      lrow = lrow * alpha + psum;
+      lpart = lpart * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       mrow = m_use;
       tmem_wait_st();
       tc_fence_before();
@@ -257,27 +292,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     if (ok && warp_wait(o_done, (n_kv - 1) & 1, ctl)) {
       tc_fence_after();
-      const int i = m * kTileRows + row;
-      const float inv = 1.f / lrow;
-      __nv_bfloat16 *orow = o + (static_cast<size_t>(b) * S + i) * nh * HD + static_cast<size_t>(h) * HD;
-#pragma unroll
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t ov[32];
-        tmem_ld_x32(tO + lane_off + c, ov);
+      red_l[g * 128 + row] = lpart;
+      mbar_arrive(pbar);
+      if (warp_wait(pbar, pair_phase & 1, ctl)) {
+        const float l = lpart + red_l[(g ^ 1) * 128 + row];
+        const int i = m * kTileRows + row;
+        const float inv = 1.f / l;
+        uint32_t ov[kHalf];
+        tmem_ld_half<kHalf>(tO + lane_off + kHalf * g, ov);
         tmem_wait_ld();
-        reg_fence<32>(ov);
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-          pk[e] = pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+        reg_fence<kHalf>(ov);
         if (i < S) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+          __nv_bfloat16 *orow = o + (static_cast<size_t>(b) * S + i) * nh * HD +
+                                static_cast<size_t>(h) * HD + kHalf * g;
+          uint4 *dst = reinterpret_cast<uint4 *>(orow);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+          for (int e = 0; e < kHalf / 8; ++e)
+            dst[e] = make_uint4(
+                pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv),
+                pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv));
+          if (g == 0) lse[(static_cast<size_t>(b) * S + i) * nh + h] = (mrow + __log2f(l)) * kLn2;
         }
       }
-      if (i < S) lse[(static_cast<size_t>(b) * S + i) * nh + h] = (mrow + __log2f(lrow)) * kLn2;
     }
   }
 

@@ -4,10 +4,11 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdio>
 #include <cstdlib>
 #include <mutex>
 
-#include "../../include/xattn.h"
+#include "xattn.h"
 #include "xattn_internal.h"
 
 namespace xattn {
@@ -98,7 +99,13 @@ xattn_status check_shape(int B, int S, int nh, int nkv, int hd, float scale) {
 
 xattn_status check_bf16(int hd) { return (hd == 32 || hd == 64) ? XATTN_OK : XATTN_ERR_UNSUPPORTED_HD; }
 
-xattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? XATTN_OK : XATTN_ERR_CUDA; }
+// With XATTN_VERBOSE set in the environment, CUDA failures are also reported on stderr.
+xattn_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return XATTN_OK;
+  static const bool verbose = std::getenv("XATTN_VERBOSE") != nullptr;
+  if (verbose) std::fprintf(stderr, "libxattn: CUDA error %d: %s\n", static_cast<int>(e), cudaGetErrorString(e));
+  return XATTN_ERR_CUDA;
+}
 
 #define XATTN_TRY(expr)                          \
   do {                                           \

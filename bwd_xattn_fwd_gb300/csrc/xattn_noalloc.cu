@@ -16,7 +16,7 @@
 #include <cmath>
 #include <mutex>
 
-#include "../../include/xattn.h"
+#include "xattn.h"
 #include "xattn_internal.h"
 
 namespace xattn {
