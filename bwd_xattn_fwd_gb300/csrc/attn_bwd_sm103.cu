@@ -256,95 +256,92 @@ __global__ void __maxnreg__(168)
   const uint32_t tdV = tmem + 320, tdK = tmem + 384, tdQ = tmem + 448;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      mbar_expect_tx(kv_full, 2 * L::kTileBytes);
-      tma_load_4d(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
-      tma_load_4d(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
-      int issued = 0;
-      for (int t = 0; t < T; ++t) {
-        const int r = t / per_head, m = n + t % per_head;
-        const int h = kvh * group + r;
-        const int s = t & 1;
-        if (!mbar_wait(empty(s), ((t >> 1) & 1) ^ 1, ctl)) break;
-        mbar_expect_tx(full(s), 2 * L::kTileBytes + 2 * 512);
-        tma_load_4d(sQ + s * L::kTileBytes, &mq, full(s), 0, h, m * kTileRows, b);
-        tma_load_4d(sdO + s * L::kTileBytes, &mdo, full(s), 0, h, m * kTileRows, b);
-        const size_t vec = (static_cast<size_t>(b) * nh + h) * S_pad + static_cast<size_t>(m) * kTileRows;
-        bulk_load(smem_u32(sLSE + s * 128), lse2 + vec, 512, full(s));
-        bulk_load(smem_u32(sD + s * 128), Dvec + vec, 512, full(s));
-        issued = t + 1;
-      }
-      mbar_drain(kv_full, 0, ctl);
-      for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
-        mbar_drain(full(t & 1), (t >> 1) & 1, ctl);
+    // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
+    mbar_expect_tx_elect(kv_full, 2 * L::kTileBytes);
+    tma_load_4d_elect(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
+    tma_load_4d_elect(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
+    int issued = 0;
+    for (int t = 0, r = 0, m = n; t < T; ++t) {
+      const int h = kvh * group + r;
+      const int s = t & 1;
+      if (!warp_wait(empty(s), ((t >> 1) & 1) ^ 1, ctl)) break;
+      mbar_expect_tx_elect(full(s), 2 * L::kTileBytes + 2 * 512);
+      tma_load_4d_elect(sQ + s * L::kTileBytes, &mq, full(s), 0, h, m * kTileRows, b);
+      tma_load_4d_elect(sdO + s * L::kTileBytes, &mdo, full(s), 0, h, m * kTileRows, b);
+      const size_t vec = (static_cast<size_t>(b) * nh + h) * S_pad + static_cast<size_t>(m) * kTileRows;
+      bulk_load_elect(smem_u32(sLSE + s * 128), lse2 + vec, 512, full(s));
+      bulk_load_elect(smem_u32(sD + s * 128), Dvec + vec, 512, full(s));
+      issued = t + 1;
+      if (++m == num_m) { m = n; ++r; }
     }
+    mbar_drain(kv_full, 0, ctl);
+    for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
+      mbar_drain(full(t & 1), (t >> 1) & 1, ctl);
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A in TMEM)
-      constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);    // dQ (A = dS, MN-major)
-      auto issue_kmajor = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
+    // ---------------- MMA issuer (converged warp, one elected lane issues) ----------------
+    constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A in TMEM)
+    constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);    // dQ (A = dS, MN-major)
+    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // stage stride, descriptor units
+    constexpr uint32_t kRowStep = (16 * L::kRowBytes) >> 4;  // 16 rows of an MN-major tile
+    // Descriptors are built once. K-major operands (Q, K, V, dO as K-major) advance
+    // +32 bytes (+2) per 16-element K step; MN-major ones advance 16 rows.
+    const uint64_t kK_k = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kV_k = smem_desc(sV, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kQ_k = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kdO_k = smem_desc(sdO, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kQ_mn = smem_desc(sQ, 8192, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kdO_mn = smem_desc(sdO, 8192, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kdS_mn = smem_desc(sdS, 16384, 1024, kSwizzle128);
+    auto issue_kmajor = [&](uint32_t d, uint64_t a, uint64_t bdesc) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t a = smem_desc(a_base + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
-          const uint64_t bd = smem_desc(b_base + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
-          mma_ss(d, a, bd, idesc_t, kk > 0);
-        }
-      };
-      auto issue_acc = [&](uint32_t d, uint32_t b_base, bool first) {
+      for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a + 2 * kk, bdesc + 2 * kk, idesc_t, kk > 0);
+    };
+    auto issue_acc = [&](uint32_t d, uint64_t bdesc, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {
-          const uint64_t bd = smem_desc(b_base + kk * 16 * L::kRowBytes, 8192, 8 * L::kRowBytes,
-                                        L::kSwizzle);
-          mma_ts(d, tP + kk * 8, bd, idesc_acc, (!first || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(kv_full, 0, ctl) && mbar_wait(full(0), 0, ctl);
-      if (ok) {
-        tc_fence_after();
-        issue_kmajor(tS, sK, sQ);
-        mma_commit(s_full);
-        issue_kmajor(tdP, sV, sdO);
-        mma_commit(dp_full);
-      }
-      for (int t = 0; ok && t < T; ++t) {
-        const int s = t & 1;
-        const bool more = t + 1 < T;
-        if (!mbar_wait(p_full, t & 1, ctl)) break;
-        tc_fence_after();
-        issue_acc(tdV, sdO + s * L::kTileBytes, t == 0);                   // dV += P^T dO
-        mma_commit(dv_done);
-        if (more) {
-          if (!mbar_wait(full(s ^ 1), ((t + 1) >> 1) & 1, ctl)) break;
-          tc_fence_after();
-          issue_kmajor(tS, sK, sQ + (s ^ 1) * L::kTileBytes);               // S^T(t+1)
-          mma_commit(s_full);
-        }
-        if (!mbar_wait(ds_full, t & 1, ctl)) break;
-        tc_fence_after();
-        issue_acc(tdK, sQ + s * L::kTileBytes, t == 0);                    // dK += dS^T Q
-        mma_commit(empty(s));
-        mma_commit(dk_done);
-        if (!mbar_wait(dq_empty, (t & 1) ^ 1, ctl)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {                      // dQ = dS K
-          const uint64_t a = smem_desc(sdS + kk * 2048, 16384, 1024, kSwizzle128);
-          const uint64_t bd = smem_desc(sK + kk * 16 * L::kRowBytes, 8192, 8 * L::kRowBytes,
-                                        L::kSwizzle);
-          mma_ss(tdQ, a, bd, idesc_dq, kk > 0);
-        }
-        mma_commit(dq_full);
-        if (more) {
-          issue_kmajor(tdP, sV, sdO + (s ^ 1) * L::kTileBytes);             // dP^T(t+1)
-          mma_commit(dp_full);
-        }
-      }
-      mma_commit(acc_done);
-      mbar_drain(acc_done, 0, ctl);
+      for (int kk = 0; kk < kTileRows / 16; ++kk)
+        mma_ts_elect(d, tP + kk * 8, bdesc + kk * kRowStep, idesc_acc, (!first || kk > 0) ? 1u : 0u);
+    };
+    bool ok = warp_wait(kv_full, 0, ctl) && warp_wait(full(0), 0, ctl);
+    if (ok) {
+      tc_fence_after();
+      issue_kmajor(tS, kK_k, kQ_k);
+      mma_commit_elect(s_full);
+      issue_kmajor(tdP, kV_k, kdO_k);
+      mma_commit_elect(dp_full);
     }
+    for (int t = 0; ok && t < T; ++t) {
+      const int s = t & 1;
+      const bool more = t + 1 < T;
+      if (!warp_wait(p_full, t & 1, ctl)) break;
+      tc_fence_after();
+      issue_acc(tdV, kdO_mn + s * kStageDesc, t == 0);                       // dV += P^T dO
+      mma_commit_elect(dv_done);
+      if (more) {
+        if (!warp_wait(full(s ^ 1), ((t + 1) >> 1) & 1, ctl)) break;
+        tc_fence_after();
+        issue_kmajor(tS, kK_k, kQ_k + (s ^ 1) * kStageDesc);                 // S^T(t+1)
+        mma_commit_elect(s_full);
+      }
+      if (!warp_wait(ds_full, t & 1, ctl)) break;
+      tc_fence_after();
+      issue_acc(tdK, kQ_mn + s * kStageDesc, t == 0);                        // dK += dS^T Q
+      mma_commit_elect(empty(s));
+      mma_commit_elect(dk_done);
+      if (!warp_wait(dq_empty, (t & 1) ^ 1, ctl)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTileRows / 16; ++kk)                            // dQ = dS K
+        mma_ss_elect(tdQ, kdS_mn + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
+      mma_commit_elect(dq_full);
+      if (more) {
+        issue_kmajor(tdP, kV_k, kdO_k + (s ^ 1) * kStageDesc);               // dP^T(t+1)
+        mma_commit_elect(dp_full);
+      }
+    }
+    mma_commit_elect(acc_done);
+    mbar_drain(acc_done, 0, ctl);
   } else if (warp >= 4) {
     // ---------------- P^T and dS^T: one thread per key row, half the query columns -----
     const int g = (warp - 4) >> 2;           // column half

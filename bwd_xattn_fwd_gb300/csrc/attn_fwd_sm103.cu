@@ -149,69 +149,66 @@ __global__ void __maxnreg__(168)
   const uint32_t tP[2] = {tmem + 320, tmem + 384};
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      mbar_expect_tx(q_full, L::kTileBytes);
-      tma_load_4d(sQ, &mq, q_full, 0, h, m * kTileRows, b);
-      int issued = 0;
-      for (int n = 0; n < n_kv; ++n) {
-        const int s = n % kFwdStages;
-        if (!mbar_wait(empty(s), ((n / kFwdStages) & 1) ^ 1, ctl)) break;
-        mbar_expect_tx(full(s), 2 * L::kTileBytes);
-        tma_load_4d(sK + s * L::kTileBytes, &mk, full(s), 0, kvh, n * kTileRows, b);
-        tma_load_4d(sV + s * L::kTileBytes, &mv, full(s), 0, kvh, n * kTileRows, b);
-        issued = n + 1;
-      }
-      // Let every copy in flight land before the CTA can exit.
-      mbar_drain(q_full, 0, ctl);
-      for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
-        mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
+    // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
+    mbar_expect_tx_elect(q_full, L::kTileBytes);
+    tma_load_4d_elect(sQ, &mq, q_full, 0, h, m * kTileRows, b);
+    int issued = 0;
+    for (int n = 0, s = 0, ph = 0; n < n_kv; ++n) {
+      if (!warp_wait(empty(s), ph ^ 1, ctl)) break;
+      mbar_expect_tx_elect(full(s), 2 * L::kTileBytes);
+      tma_load_4d_elect(sK + s * L::kTileBytes, &mk, full(s), 0, kvh, n * kTileRows, b);
+      tma_load_4d_elect(sV + s * L::kTileBytes, &mv, full(s), 0, kvh, n * kTileRows, b);
+      issued = n + 1;
+      if (++s == kFwdStages) { s = 0; ph ^= 1; }
     }
+    // Let every copy in flight land before the CTA can exit.
+    mbar_drain(q_full, 0, ctl);
+    for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
+      mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
   } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
-      constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
-      auto issue_qk = [&](uint32_t d, int s) {
+    // ---------------- MMA issuer (converged warp, one elected lane issues) ----------------
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;        // stage stride, descriptor units
+    constexpr uint32_t kVStep = (16 * L::kRowBytes) >> 4;      // 16 key rows of V
+    // Descriptors are built once; a K step of 16 elements is +32 bytes (+2) within the
+    // swizzled K-major rows of Q and K, and +16 rows of the MN-major V tile.
+    const uint64_t dQ = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t dK = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t dV = smem_desc(sV, 8192, 8 * L::kRowBytes, L::kSwizzle);
+    auto issue_qk = [&](uint32_t d, int s) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t a = smem_desc(sQ + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
-          const uint64_t bdesc =
-              smem_desc(sK + s * L::kTileBytes + kk * 32, 16, 8 * L::kRowBytes, L::kSwizzle);
-          mma_ss(d, a, bdesc, idesc_qk, kk > 0);
-        }
-      };
-      bool ok = mbar_wait(q_full, 0, ctl) && mbar_wait(full(0), 0, ctl);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(tS[0], 0);
-        mma_commit(s_full(0));
-      }
-      for (int n = 0; ok && n < n_kv; ++n) {
-        if (n + 1 < n_kv) {
-          // S(n+1) goes into the buffer of S(n-1), which the softmax finished reading
-          // before it signalled P(n-1) (waited for in the previous iteration).
-          const int s1 = (n + 1) % kFwdStages;
-          if (!mbar_wait(full(s1), ((n + 1) / kFwdStages) & 1, ctl)) break;
-          tc_fence_after();
-          issue_qk(tS[(n + 1) & 1], s1);
-          mma_commit(s_full((n + 1) & 1));
-        }
-        if (!mbar_wait(p_full(n & 1), (n >> 1) & 1, ctl)) break;
-        tc_fence_after();
-        const int s = n % kFwdStages;
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk) {
-          const uint64_t bdesc = smem_desc(sV + s * L::kTileBytes + kk * 16 * L::kRowBytes,
-                                           8192, 8 * L::kRowBytes, L::kSwizzle);
-          mma_ts(tO, tP[n & 1] + kk * 8, bdesc, idesc_pv, (n > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(empty(s));
-        mma_commit(o_done);
-      }
-      mma_commit(mma_final);
-      mbar_drain(mma_final, 0, ctl);
+      for (int kk = 0; kk < HD / 16; ++kk)
+        mma_ss_elect(d, dQ + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
+    };
+    bool ok = warp_wait(q_full, 0, ctl) && warp_wait(full(0), 0, ctl);
+    if (ok) {
+      tc_fence_after();
+      issue_qk(tS[0], 0);
+      mma_commit_elect(s_full(0));
     }
+    for (int n = 0, s = 0, s1 = 1 % kFwdStages, ph1 = (1 / kFwdStages) & 1; ok && n < n_kv; ++n) {
+      if (n + 1 < n_kv) {
+        // S(n+1) goes into the buffer of S(n-1), which the softmax finished reading
+        // before it signalled P(n-1) (waited for in the previous iteration).
+        if (!warp_wait(full(s1), ph1, ctl)) break;
+        tc_fence_after();
+        issue_qk(tS[(n + 1) & 1], s1);
+        mma_commit_elect(s_full((n + 1) & 1));
+      }
+      if (!warp_wait(p_full(n & 1), (n >> 1) & 1, ctl)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTileRows / 16; ++kk)
+        mma_ts_elect(tO, tP[n & 1] + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv,
+                     (n > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_elect(empty(s));
+      mma_commit_elect(o_done);
+      if (++s == kFwdStages) s = 0;
+      if (++s1 == kFwdStages) { s1 = 0; ph1 ^= 1; }
+    }
+    mma_commit_elect(mma_final);
+    mbar_drain(mma_final, 0, ctl);
   } else if (warp >= 4) {
     // ---------------- softmax + epilogue ----------------
     const int g = (warp - 4) >> 2;           // key-column half of every tile
@@ -230,26 +227,28 @@ __global__ void __maxnreg__(168)
       tmem_ld_x32(tS[n & 1] + lane_off + 64 * g + 32, r + 32);
       tmem_wait_ld();
       reg_fence<64>(r);
-      const bool diag = (n == m);
-      const int col0 = 64 * g;
-      float mx8[8];
+      // Causal mask (diagonal tile only; the branch is uniform across the CTA).
+      if (n == m) {
+        const int col0 = 64 * g;
 #pragma unroll
-      for (int a = 0; a < 8; ++a) mx8[a] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x = __uint_as_float(r[c]) * scale_log2;
-        if (diag && col0 + c > row) x = -INFINITY;
-        r[c] = __float_as_uint(x);
-        mx8[c & 7] = fmaxf(mx8[c & 7], x);
+        for (int c = 0; c < 64; ++c)
+          if (col0 + c > row) r[c] = __float_as_uint(-INFINITY);
       }
-      float pmax = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                         fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      // Row maximum of the raw scores (scale > 0, so the scaled maximum is its image).
+      float mx4[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+        mx4[a] = fmax3(__uint_as_float(r[2 * a]), __uint_as_float(r[2 * a + 1]), -INFINITY);
+#pragma unroll
+      for (int c = 8; c < 64; c += 2)
+        mx4[(c >> 1) & 3] = fmax3(mx4[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+      const float pmax = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
       // Row maximum across the two column halves (double-buffered by tile parity).
       red_max[((n & 1) * 2 + g) * 128 + row] = pmax;
       mbar_arrive(pbar);
       if (!warp_wait(pbar, pair_phase & 1, ctl)) { ok = false; break; }
       ++pair_phase;
-      const float mx = fmaxf(pmax, red_max[((n & 1) * 2 + (g ^ 1)) * 128 + row]);
+      const float mx = fmaxf(pmax, red_max[((n & 1) * 2 + (g ^ 1)) * 128 + row]) * scale_log2;
       // Conditional rescaling: keep the stale max unless some row of the warp grew by
       // more than 2^8; the decision is per warp because TMEM loads/stores are collective,
       // and both halves of a row reach the same decision from the same maxima.
@@ -257,13 +256,17 @@ __global__ void __maxnreg__(168)
       const bool rescale = __any_sync(0xffffffffu, mnew > mrow + 8.0f);
       const float m_use = rescale ? mnew : mrow;
       const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
+      const float neg_m = -m_use;
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[32];
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        const float p0 = ex2_approx(__uint_as_float(r[2 * e]) - m_use);
-        const float p1 = ex2_approx(__uint_as_float(r[2 * e + 1]) - m_use);
-        ps[e & 3] += p0 + p1;
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
+              scale_log2, neg_m, neg_m);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        const int a = (e & 1) * 2;
+        fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
         pk[e] = pack_bf16x2(p0, p1);
       }
       // P(n) goes into the buffer PV(n-2) read; that PV was waited for last iteration.
