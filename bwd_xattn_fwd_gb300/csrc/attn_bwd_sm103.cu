@@ -7,7 +7,8 @@
 //
 // Three kernels, in stream order:
 //   1. preprocess (HBM-bound): D_i = sum_d dO_id O_id in fp32, the log2-domain LSE
-//      rows laid out [B, nh, S_pad], and a zeroed fp32 dQ accumulator.
+//      rows laid out [B, nh, S_pad] (both stored negated), and a zeroed fp32 dQ
+//      accumulator.
 //   2. main (tensor cores). One CTA per (batch, kv head, 128-row key tile n). The K_n
 //      and V_n tiles stay in shared memory; the dK_n / dV_n accumulators stay in TMEM
 //      while the CTA walks every query head r of the group and every query tile m >= n
@@ -19,7 +20,8 @@
 //        dS^T = scale * P^T (dP^T - D_m)            -> bf16 into the same slot, and
 //                                                      into shared memory (MN-major)
 //        dV_n += P^T dO_m ,  dK_n += dS^T Q_m       (A operand from TMEM)
-//        dQ_m  = dS K_n                 (TMEM) -> fp32 atomic adds into the accumulator
+//        dQ_m  = dS K_n                 (TMEM) -> shared memory -> TMA reduce-add into
+//                                                      the fp32 accumulator
 //      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 4-11 = P/dS (one thread
 //      per key row, two warps per row splitting the 128 query columns), which also
 //      drain each dQ tile from TMEM.
@@ -55,7 +57,8 @@ namespace {
 // One group of (hd / 8) lanes per row (b, i, h): each lane reads 8 bf16 of O and dO
 // (16 B each), the group reduces with shuffles. Rows are enumerated in memory order of
 // O/dO, so the loads are fully coalesced. The same lanes zero the row of the dQ
-// accumulator. Pad rows (S <= i < S_pad) get D = 0 and LSE2 = +inf, so that the main
+// accumulator. Both vectors are stored negated (-D and -LSE log2 e), which is the form
+// the main kernel adds. Pad rows (S <= i < S_pad) get 0 and -inf, so that the main
 // kernel's partial query tiles contribute exactly zero.
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
@@ -96,8 +99,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
       const int i = static_cast<int>(bi % S);
       const int b = static_cast<int>(bi / S);
       const size_t dst = (static_cast<size_t>(b) * nh + h) * S_pad + i;
-      D[dst] = acc;
-      lse2[dst] = lse[row] * kLog2e;
+      D[dst] = -acc;
+      lse2[dst] = -lse[row] * kLog2e;
     }
   } else if (row - n_rows < n_pad && sub == 0) {
     const long long p = row - n_rows;
@@ -105,7 +108,7 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
     const long long bh = p / pad;
     const int i = S + static_cast<int>(p % pad);
     D[bh * S_pad + i] = 0.f;
-    lse2[bh * S_pad + i] = INFINITY;
+    lse2[bh * S_pad + i] = -INFINITY;
   }
 }
 
@@ -138,10 +141,15 @@ struct BwdLayout {
   static constexpr uint32_t kQ = kV + kTileBytes;          // 2 stages
   static constexpr uint32_t kdO = kQ + 2 * kTileBytes;     // 2 stages
   static constexpr uint32_t kdS = kdO + 2 * kTileBytes;    // 128 x 128 bf16, MN-major, 32 KB
-  static constexpr uint32_t kVec = kdS + 32768;            // LSE2[2][128], D[2][128] fp32
+  // dQ staging for the TMA reduce-add: 2 buffers x 2 head-dim halves x 128 rows of
+  // HD/2 floats, swizzled like the tensor map's box.
+  static constexpr uint32_t kDqRowBytes = HD / 2 * 4;
+  static constexpr uint32_t kDqHalfBytes = kTileRows * kDqRowBytes;
+  static constexpr uint32_t kdQs = kdS + 32768;
+  static constexpr uint32_t kVec = kdQs + 4 * kDqHalfBytes;  // -LSE2[2][128], -D[2][128] fp32
   // barriers: kv_full, full[2], empty[2], s_full, dp_full, p_full, ds_full, dq_full,
-  //           dq_empty, acc_done, dv_done, dk_done
-  static constexpr int kNumBars = 14;
+  //           dq_empty, acc_done, dv_done, dk_done, dqs_full[2], dqs_empty[2]
+  static constexpr int kNumBars = 18;
   static constexpr uint32_t kBars = kVec + 4 * 512;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
@@ -164,12 +172,14 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
 // warps leave 168 per thread):
 //   warp 0     : TMA producer
 //   warp 1     : TMEM owner and MMA issuer
-//   warps 2-3  : idle
+//   warp 2     : dQ reducer: TMA reduce-adds each staged dQ tile into the fp32
+//                accumulator (2 bulk operations per tile instead of scattered atomics)
+//   warp 3     : idle
 //   warps 4-11 : P^T / dS^T, one thread per key row; warps 4-7 take query columns 0-63
 //                and warps 8-11 columns 64-127 (two warps per lane quarter, so each SM
-//                sub-partition interleaves two of them). They also drain dQ(t-1) from
-//                TMEM into the fp32 accumulator (one query row per thread, each half
-//                taking half of the head dimension).
+//                sub-partition interleaves two of them). They also move dQ(t-1) from
+//                TMEM to a double-buffered shared-memory tile (one query row per thread,
+//                each half taking half of the head dimension).
 // TMEM columns: S^T [0,128) fp32 | dP^T [128,256) fp32 | P^T, then dS^T, bf16 [256,320)
 //               | dV [320,384) | dK [384,448) | dQ [448,512)
 // P^T and dS^T share one slot that no other result overlaps, so the two column halves
@@ -179,8 +189,9 @@ template <int HD>
 __global__ void __maxnreg__(168)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                         const __grid_constant__ CUtensorMap mdq,
                          const float *__restrict__ Dvec, const float *__restrict__ lse2,
-                         float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dk,
+                         __nv_bfloat16 *__restrict__ dk,
                          __nv_bfloat16 *__restrict__ dv, int B, int S, int nh, int nkv,
                          float scale, float scale_log2, int *status, unsigned long long timeout_ns) {
   using L = BwdLayout<HD>;
@@ -206,8 +217,9 @@ __global__ void __maxnreg__(168)
   const uint32_t sdO = smem_u32(smem + L::kdO);
   uint8_t *sdS_ptr = smem + L::kdS;
   const uint32_t sdS = smem_u32(sdS_ptr);
-  float *sLSE = reinterpret_cast<float *>(smem + L::kVec);         // [2][128]
-  float *sD = reinterpret_cast<float *>(smem + L::kVec + 1024);    // [2][128]
+  uint8_t *sdQs_ptr = smem + L::kdQs;
+  float *sLSE = reinterpret_cast<float *>(smem + L::kVec);         // [2][128]  -LSE log2 e
+  float *sD = reinterpret_cast<float *>(smem + L::kVec + 1024);    // [2][128]  -D
   const uint32_t bar0 = smem_u32(smem + L::kBars);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const uint32_t kv_full = bar(0);
@@ -216,6 +228,8 @@ __global__ void __maxnreg__(168)
   const uint32_t s_full = bar(5), dp_full = bar(6), p_full = bar(7), ds_full = bar(8);
   const uint32_t dq_full = bar(9), dq_empty = bar(10), acc_done = bar(11);
   const uint32_t dv_done = bar(12), dk_done = bar(13);
+  auto dqs_full = [&](int x) { return bar(14 + x); };
+  auto dqs_empty = [&](int x) { return bar(16 + x); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -236,6 +250,10 @@ __global__ void __maxnreg__(168)
     mbar_init(acc_done, 1);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(dqs_full(x), 256);
+      mbar_init(dqs_empty(x), 1);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -243,6 +261,7 @@ __global__ void __maxnreg__(168)
     tma_prefetch_desc(&mk);
     tma_prefetch_desc(&mv);
     tma_prefetch_desc(&mdo);
+    tma_prefetch_desc(&mdq);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), 512);
@@ -342,6 +361,24 @@ __global__ void __maxnreg__(168)
     }
     mma_commit_elect(acc_done);
     mbar_drain(acc_done, 0, ctl);
+  } else if (warp == 2) {
+    // ---------------- dQ reducer ----------------
+    for (int k = 0; k < T; ++k) {
+      const int buf = k & 1;
+      if (!warp_wait(dqs_full(buf), (k >> 1) & 1, ctl)) break;
+      if (lane == 0) {
+        const int h = kvh * group + k / per_head, m = n + k % per_head;
+        const uint32_t src = smem_u32(sdQs_ptr + buf * 2 * L::kDqHalfBytes);
+        tma_reduce_add_4d(&mdq, src, 0, h, m * kTileRows, b);
+        tma_reduce_add_4d(&mdq, src + L::kDqHalfBytes, HD / 2, h, m * kTileRows, b);
+        bulk_commit_group();
+        bulk_wait_read_all();          // the staging buffer may be rewritten
+        mbar_arrive(dqs_empty(buf));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();    // every reduce-add has landed before the CTA exits
+    __syncwarp();
   } else if (warp >= 4) {
     // ---------------- P^T and dS^T: one thread per key row, half the query columns -----
     const int g = (warp - 4) >> 2;           // column half
@@ -350,10 +387,10 @@ __global__ void __maxnreg__(168)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t col_f32 = 64u * g, col_bf16 = 32u * g;
     constexpr int kHalf = HD / 2;
-    // dQ(tt) from TMEM (query row j of its tile, head-dim half g) into the accumulator.
-    auto drain_dq = [&](int tt) {
-      const int r_h = tt / per_head, m_t = n + tt % per_head;
-      const int h = kvh * group + r_h;
+    // dQ(k) from TMEM (query row j of its tile, head-dim half g) into staging buffer
+    // k & 1, swizzled like the reduce's tensor-map box; warp 2 then adds it to global.
+    auto drain_dq = [&](int k) -> bool {
+      const int buf = k & 1;
       uint32_t v[kHalf];
       if constexpr (kHalf == 32) tmem_ld_x32(tdQ + lane_off + kHalf * g, v);
       else tmem_ld_x16(tdQ + lane_off + kHalf * g, v);
@@ -361,15 +398,17 @@ __global__ void __maxnreg__(168)
       reg_fence<kHalf>(v);
       tc_fence_before();
       mbar_arrive(dq_empty);
-      const int ig = m_t * kTileRows + j;
-      if (ig < S) {
-        float4 *dst = reinterpret_cast<float4 *>(
-            dqacc + ((static_cast<size_t>(b) * S + ig) * nh + h) * HD + kHalf * g);
+      if (!warp_wait(dqs_empty(buf), ((k >> 1) & 1) ^ 1, ctl)) return false;
+      uint8_t *row = sdQs_ptr + (buf * 2 + g) * L::kDqHalfBytes + j * L::kDqRowBytes;
 #pragma unroll
-        for (int e = 0; e < kHalf / 4; ++e)
-          atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                         __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+      for (int c = 0; c < kHalf / 4; ++c) {
+        const int sw = (HD == 64) ? (c ^ (j & 7)) : (c ^ ((j >> 1) & 3));
+        *reinterpret_cast<uint4 *>(row + (sw << 4)) =
+            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
       }
+      fence_proxy_async_smem();
+      mbar_arrive(dqs_full(buf));
+      return true;
     };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -384,17 +423,19 @@ __global__ void __maxnreg__(168)
       tmem_ld_x32(tS + lane_off + col_f32 + 32, r + 32);
       tmem_wait_ld();
       reg_fence<64>(r);
-      const float4 *lse4 = reinterpret_cast<const float4 *>(sLSE + s * 128 + col_f32);
+      const float4 *nlse4 = reinterpret_cast<const float4 *>(sLSE + s * 128 + col_f32);
       uint32_t pk[32];
 #pragma unroll
       for (int q4 = 0; q4 < 16; ++q4) {
-        const float4 l4 = lse4[q4];
-        const int i = static_cast<int>(col_f32) + 4 * q4;
-        float p0 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 0]), scale_log2, -l4.x));
-        float p1 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 1]), scale_log2, -l4.y));
-        float p2 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 2]), scale_log2, -l4.z));
-        float p3 = ex2_approx(fmaf(__uint_as_float(r[4 * q4 + 3]), scale_log2, -l4.w));
+        const float4 nl = nlse4[q4];
+        float x0, x1, x2, x3;
+        ffma2(x0, x1, __uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]), scale_log2,
+              scale_log2, nl.x, nl.y);
+        ffma2(x2, x3, __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]), scale_log2,
+              scale_log2, nl.z, nl.w);
+        float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         if (diag) {
+          const int i = static_cast<int>(col_f32) + 4 * q4;
           if (i + 0 < j) p0 = 0.f;
           if (i + 1 < j) p1 = 0.f;
           if (i + 2 < j) p2 = 0.f;
@@ -424,25 +465,28 @@ __global__ void __maxnreg__(168)
       if (t > 0) {
         if (!warp_wait(dq_full, (t - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        drain_dq(t - 1);
+        if (!drain_dq(t - 1)) { ok = false; break; }
       }
       if (!warp_wait(dv_done, t & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      const float4 *d4 = reinterpret_cast<const float4 *>(sD + s * 128 + col_f32);
+      const float4 *nd4 = reinterpret_cast<const float4 *>(sD + s * 128 + col_f32);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t dsk[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
           const int c = half * 32 + 4 * q4;
-          const float4 dd = d4[c / 4];
+          const float4 nd = nd4[c / 4];
           const uint32_t pa = pk[c / 2], pb = pk[c / 2 + 1];
-          const float ds0 = bf16lo_to_f32(pa) * (__uint_as_float(r[c + 0]) - dd.x) * scale;
-          const float ds1 = bf16hi_to_f32(pa) * (__uint_as_float(r[c + 1]) - dd.y) * scale;
-          const float ds2 = bf16lo_to_f32(pb) * (__uint_as_float(r[c + 2]) - dd.z) * scale;
-          const float ds3 = bf16hi_to_f32(pb) * (__uint_as_float(r[c + 3]) - dd.w) * scale;
-          dsk[2 * q4] = pack_bf16x2(ds0, ds1);
-          dsk[2 * q4 + 1] = pack_bf16x2(ds2, ds3);
+          float t0, t1, t2, t3;
+          fadd2(t0, t1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), nd.x, nd.y);
+          fadd2(t2, t3, __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]), nd.z, nd.w);
+          fmul2(t0, t1, t0, t1, bf16lo_to_f32(pa), bf16hi_to_f32(pa));
+          fmul2(t2, t3, t2, t3, bf16lo_to_f32(pb), bf16hi_to_f32(pb));
+          fmul2(t0, t1, t0, t1, scale, scale);
+          fmul2(t2, t3, t2, t3, scale, scale);
+          dsk[2 * q4] = pack_bf16x2(t0, t1);
+          dsk[2 * q4 + 1] = pack_bf16x2(t2, t3);
         }
         tmem_st_x16(tP + lane_off + col_bf16 + 16 * half, dsk);
 #pragma unroll
@@ -459,7 +503,7 @@ __global__ void __maxnreg__(168)
     // second dK rows (dK already carries the scale).
     if (ok && warp_wait(dq_full, (T - 1) & 1, ctl)) {
       tc_fence_after();
-      drain_dq(T - 1);
+      ok = drain_dq(T - 1);
     } else {
       ok = false;
     }
@@ -498,7 +542,7 @@ __global__ void __maxnreg__(168)
 
 template <int HD>
 cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mdo, const BwdWorkspace &ws, __nv_bfloat16 *dk,
+                           const CUtensorMap &mdo, const CUtensorMap &mdq, const BwdWorkspace &ws, __nv_bfloat16 *dk,
                            __nv_bfloat16 *dv, int B, int S, int nh, int nkv, float scale,
                            int *status, uint64_t timeout_ns, cudaStream_t stream) {
   using L = BwdLayout<HD>;
@@ -508,7 +552,7 @@ cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const C
   const int num_n = (S + kTileRows - 1) / kTileRows;
   const unsigned grid = static_cast<unsigned>(B) * nkv * num_n;
   attn_bwd_main_kernel<HD><<<grid, kBwdThreads, L::kDynBytes, stream>>>(
-      mq, mk, mv, mdo, ws.D, ws.lse2, ws.dqacc, dk, dv, B, S, nh, nkv, scale, scale * kLog2e,
+      mq, mk, mv, mdo, mdq, ws.D, ws.lse2, dk, dv, B, S, nh, nkv, scale, scale * kLog2e,
       status, timeout_ns);
   return cudaGetLastError();
 }
@@ -534,13 +578,13 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *d
 
 cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
                                  const CUtensorMap &mv, const CUtensorMap &mdo,
-                                 const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
+                                 const CUtensorMap &mdq, const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
                                  int B, int S, int nh, int nkv, int hd, float scale, int *status,
                                  uint64_t timeout_ns, cudaStream_t stream) {
   if (hd == 64)
-    return launch_main_hd<64>(mq, mk, mv, mdo, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return launch_main_hd<64>(mq, mk, mv, mdo, mdq, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
   if (hd == 32)
-    return launch_main_hd<32>(mq, mk, mv, mdo, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return launch_main_hd<32>(mq, mk, mv, mdo, mdq, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -84,6 +84,24 @@ xattn_status make_map(CUtensorMap *map, const void *ptr, int B, int S, int H, in
   return r == CUDA_SUCCESS ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
+// 4-D fp32 map over the [B, S, nh, hd] dQ accumulator. The box is half a head row
+// (hd/2 floats: 128 bytes at hd = 64, 64 bytes at hd = 32, with the matching swizzle)
+// by 128 rows; the backward adds shared-memory tiles into it with TMA reduce-adds.
+// Rows past S are skipped by the TMA unit.
+xattn_status make_map_dq(CUtensorMap *map, float *ptr, int B, int S, int nh, int hd) {
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(nh),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t row = static_cast<cuuint64_t>(hd) * 4;
+  const cuuint64_t strides[3] = {row, row * nh, row * nh * S};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(hd / 2), 1, static_cast<cuuint32_t>(kTileRows), 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, elem,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              hd == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 xattn_status check_shape(int B, int S, int nh, int nkv, int hd, float scale) {
@@ -188,7 +206,9 @@ xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const v
   XATTN_TRY(make_map(&mv, v, B, S, nkv, hd));
   XATTN_TRY(make_map(&mdo, dO, B, S, nh, hd));
   const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
-  return cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, ws, static_cast<__nv_bfloat16 *>(dk),
+  CUtensorMap mdq;
+  XATTN_TRY(make_map_dq(&mdq, ws.dqacc, B, S, nh, hd));
+  return cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, mdq, ws, static_cast<__nv_bfloat16 *>(dk),
                                           static_cast<__nv_bfloat16 *>(dv), B, S, nh, nkv, hd, scale,
                                           dev->status, wait_limit_ns(),
                                           static_cast<cudaStream_t>(stream)));

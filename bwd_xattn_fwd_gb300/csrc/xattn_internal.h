@@ -17,8 +17,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 __host__ __device__ inline int padded_rows(int S) { return (S + kTileRows - 1) / kTileRows * kTileRows; }
 
 struct BwdWorkspace {
-  float *D;      // [B, nh, S_pad]  D_i = dO_i . O_i ; zero in pad rows
-  float *lse2;   // [B, nh, S_pad]  LSE_i * log2(e) ; +inf in pad rows
+  float *D;      // [B, nh, S_pad]  -D_i = -(dO_i . O_i) ; zero in pad rows
+  float *lse2;   // [B, nh, S_pad]  -LSE_i * log2(e) ; -inf in pad rows
   float *dqacc;  // [B, S, nh, hd]  fp32 dQ accumulator
 };
 
@@ -34,8 +34,11 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *d
                                   const float *lse, int B, int S, int nh, int hd,
                                   const BwdWorkspace &ws, cudaStream_t stream);
 
+// mdq: fp32 map over the dQ accumulator (box = half a head row x 128 rows), used for
+// TMA reduce-adds.
 cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
                                  const CUtensorMap &mv, const CUtensorMap &mdo,
+                                 const CUtensorMap &mdq,
                                  const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
                                  int B, int S, int nh, int nkv, int hd, float scale, int *status,
                                  uint64_t timeout_ns, cudaStream_t stream);
