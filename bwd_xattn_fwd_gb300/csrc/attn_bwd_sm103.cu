@@ -129,7 +129,21 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict
 // ------------------------------------------------------------------------------------
 // 2. main kernel
 // ------------------------------------------------------------------------------------
-constexpr int kBwdThreads = 384;  // 12 warps, see the role map in the kernel
+// Column groups of the P/dS work: each group of 4 warps owns 128 / kBwdGroups query
+// columns of every tile. Registers are split evenly over the 4 SM sub-partitions, so the
+// per-thread limit follows from the warp count (4 + 4 * groups warps).
+#ifndef XATTN_BWD_GROUPS
+#define XATTN_BWD_GROUPS 2
+#endif
+#if XATTN_BWD_GROUPS == 4
+#define XATTN_BWD_MAXNREG 96    // 20 warps: 5 per sub-partition
+#elif XATTN_BWD_GROUPS == 2
+#define XATTN_BWD_MAXNREG 168   // 12 warps: 3 per sub-partition
+#else
+#error "XATTN_BWD_GROUPS must be 2 or 4"
+#endif
+constexpr int kBwdGroups = XATTN_BWD_GROUPS;
+constexpr int kBwdThreads = 128 + 128 * kBwdGroups;
 
 template <int HD>
 struct BwdLayout {
@@ -168,25 +182,24 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
   return static_cast<uint32_t>((i >> 6) * 16384 + j * 128 + ((((i & 63) >> 3) ^ (j & 7)) << 4));
 }
 
-// Role map (12 warps; registers are split evenly over the 4 SM sub-partitions, so 12
-// warps leave 168 per thread):
+// Role map (4 + 4 * kBwdGroups warps):
 //   warp 0     : TMA producer
 //   warp 1     : TMEM owner and MMA issuer
 //   warp 2     : dQ reducer: TMA reduce-adds each staged dQ tile into the fp32
 //                accumulator (2 bulk operations per tile instead of scattered atomics)
 //   warp 3     : idle
-//   warps 4-11 : P^T / dS^T, one thread per key row; warps 4-7 take query columns 0-63
-//                and warps 8-11 columns 64-127 (two warps per lane quarter, so each SM
-//                sub-partition interleaves two of them). They also move dQ(t-1) from
-//                TMEM to a double-buffered shared-memory tile (one query row per thread,
-//                each half taking half of the head dimension).
+//   warps 4.. : P^T / dS^T, one thread per key row; warp group g (4 warps, one per TMEM
+//               lane quarter) owns query columns [g*C, (g+1)*C), C = 128 / kBwdGroups, so
+//               each SM sub-partition interleaves kBwdGroups of them. They also move
+//               dQ(t-1) from TMEM to a double-buffered shared-memory tile (one query row
+//               per thread, group g taking head-dim columns [g*HD/G, (g+1)*HD/G)).
 // TMEM columns: S^T [0,128) fp32 | dP^T [128,256) fp32 | P^T, then dS^T, bf16 [256,320)
 //               | dV [320,384) | dK [384,448) | dQ [448,512)
 // P^T and dS^T share one slot that no other result overlaps, so the two column halves
 // never write over values the other half still has to read; the MMA readers of that
 // slot (dV reads P^T, dK reads dS^T) are waited for before it is overwritten.
 template <int HD>
-__global__ void __maxnreg__(168)
+__global__ void __maxnreg__(XATTN_BWD_MAXNREG)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                          const __grid_constant__ CUtensorMap mdq,
@@ -243,15 +256,15 @@ __global__ void __maxnreg__(168)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 256);
-    mbar_init(ds_full, 256);
+    mbar_init(p_full, 128 * kBwdGroups);
+    mbar_init(ds_full, 128 * kBwdGroups);
     mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 256);
+    mbar_init(dq_empty, 128 * kBwdGroups);
     mbar_init(acc_done, 1);
     mbar_init(dv_done, 1);
     mbar_init(dk_done, 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(dqs_full(x), 256);
+      mbar_init(dqs_full(x), 128 * kBwdGroups);
       mbar_init(dqs_empty(x), 1);
     }
     fence_mbar_init();
@@ -380,35 +393,49 @@ __global__ void __maxnreg__(168)
     if (lane == 0) bulk_wait_all();    // every reduce-add has landed before the CTA exits
     __syncwarp();
   } else if (warp >= 4) {
-    // ---------------- P^T and dS^T: one thread per key row, half the query columns -----
-    const int g = (warp - 4) >> 2;           // column half
+    // ---------------- P^T and dS^T: one thread per key row, C query columns ----------------
+    constexpr int C = 128 / kBwdGroups;        // query columns per thread
+    constexpr int kDq = HD / kBwdGroups;       // dQ head-dim columns drained per thread
+    const int g = (warp - 4) >> 2;             // column group
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t col_f32 = 64u * g, col_bf16 = 32u * g;
-    constexpr int kHalf = HD / 2;
-    // dQ(k) from TMEM (query row j of its tile, head-dim half g) into staging buffer
-    // k & 1, swizzled like the reduce's tensor-map box; warp 2 then adds it to global.
+    const int col_f32 = C * g;
+    const uint32_t col_bf16 = static_cast<uint32_t>(C / 2 * g);
+    // dQ(k) from TMEM (query row j of its tile, head-dim columns [g*kDq, (g+1)*kDq)) into
+    // staging buffer k & 1, swizzled like the reduce's tensor-map box (two halves of HD/2
+    // floats per row); warp 2 then adds it to global memory.
     auto drain_dq = [&](int k) -> bool {
       const int buf = k & 1;
-      uint32_t v[kHalf];
-      if constexpr (kHalf == 32) tmem_ld_x32(tdQ + lane_off + kHalf * g, v);
-      else tmem_ld_x16(tdQ + lane_off + kHalf * g, v);
+      uint32_t v[kDq];
+      if constexpr (kDq == 32) tmem_ld_x32(tdQ + lane_off + kDq * g, v);
+      else if constexpr (kDq == 16) tmem_ld_x16(tdQ + lane_off + kDq * g, v);
+      else tmem_ld_x8(tdQ + lane_off + kDq * g, v);
       tmem_wait_ld();
-      reg_fence<kHalf>(v);
+      reg_fence<kDq>(v);
       tc_fence_before();
       mbar_arrive(dq_empty);
       if (!warp_wait(dqs_empty(buf), ((k >> 1) & 1) ^ 1, ctl)) return false;
-      uint8_t *row = sdQs_ptr + (buf * 2 + g) * L::kDqHalfBytes + j * L::kDqRowBytes;
+      const int first = kDq * g;                      // first head-dim column
+      const int half = first / (HD / 2);
+      const int chunk0 = (first % (HD / 2)) / 4;      // 16-byte chunk within the row
+      uint8_t *row = sdQs_ptr + (buf * 2 + half) * L::kDqHalfBytes + j * L::kDqRowBytes;
 #pragma unroll
-      for (int c = 0; c < kHalf / 4; ++c) {
-        const int sw = (HD == 64) ? (c ^ (j & 7)) : (c ^ ((j >> 1) & 3));
+      for (int c = 0; c < kDq / 4; ++c) {
+        const int ch = chunk0 + c;
+        const int sw = (HD == 64) ? (ch ^ (j & 7)) : (ch ^ ((j >> 1) & 3));
         *reinterpret_cast<uint4 *>(row + (sw << 4)) =
             make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
       }
       fence_proxy_async_smem();
       mbar_arrive(dqs_full(buf));
       return true;
+    };
+    auto ld_cols = [&](uint32_t taddr, uint32_t *r) {
+#pragma unroll
+      for (int c = 0; c < C; c += 32) tmem_ld_x32(taddr + c, r + c);
+      tmem_wait_ld();
+      reg_fence<C>(r);
     };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
@@ -418,15 +445,12 @@ __global__ void __maxnreg__(168)
       // Phase 1: P^T = exp2(S^T scale log2e - LSE2), masked above the diagonal.
       if (!warp_wait(s_full, t & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[64];
-      tmem_ld_x32(tS + lane_off + col_f32, r);
-      tmem_ld_x32(tS + lane_off + col_f32 + 32, r + 32);
-      tmem_wait_ld();
-      reg_fence<64>(r);
+      uint32_t r[C];
+      ld_cols(tS + lane_off + col_f32, r);
       const float4 *nlse4 = reinterpret_cast<const float4 *>(sLSE + s * 128 + col_f32);
-      uint32_t pk[32];
+      uint32_t pk[C / 2];
 #pragma unroll
-      for (int q4 = 0; q4 < 16; ++q4) {
+      for (int q4 = 0; q4 < C / 4; ++q4) {
         const float4 nl = nlse4[q4];
         float x0, x1, x2, x3;
         ffma2(x0, x1, __uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]), scale_log2,
@@ -435,7 +459,7 @@ __global__ void __maxnreg__(168)
               scale_log2, nl.z, nl.w);
         float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
         if (diag) {
-          const int i = static_cast<int>(col_f32) + 4 * q4;
+          const int i = col_f32 + 4 * q4;
           if (i + 0 < j) p0 = 0.f;
           if (i + 1 < j) p1 = 0.f;
           if (i + 2 < j) p2 = 0.f;
@@ -447,8 +471,8 @@ __global__ void __maxnreg__(168)
       // The P^T slot still holds dS^T(t-1) until dK(t-1) has read it.
       if (t > 0 && !warp_wait(dk_done, (t - 1) & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      tmem_st_x16(tP + lane_off + col_bf16, pk);
-      tmem_st_x16(tP + lane_off + col_bf16 + 16, pk + 16);
+#pragma unroll
+      for (int c = 0; c < C / 2; c += 16) tmem_st_x16(tP + lane_off + col_bf16 + c, pk + c);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full);
@@ -456,10 +480,7 @@ __global__ void __maxnreg__(168)
       // Phase 2: dS^T = scale P^T (dP^T - D).
       if (!warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      tmem_ld_x32(tdP + lane_off + col_f32, r);
-      tmem_ld_x32(tdP + lane_off + col_f32 + 32, r + 32);
-      tmem_wait_ld();
-      reg_fence<64>(r);
+      ld_cols(tdP + lane_off + col_f32, r);
       // dQ(t-1) must be done reading the shared-memory copy of dS (its result is drained
       // here), and dV(t) must be done reading P^T before dS^T replaces it in TMEM.
       if (t > 0) {
@@ -471,11 +492,11 @@ __global__ void __maxnreg__(168)
       tc_fence_after();
       const float4 *nd4 = reinterpret_cast<const float4 *>(sD + s * 128 + col_f32);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
+      for (int c32 = 0; c32 < C; c32 += 32) {
         uint32_t dsk[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const int c = half * 32 + 4 * q4;
+          const int c = c32 + 4 * q4;
           const float4 nd = nd4[c / 4];
           const uint32_t pa = pk[c / 2], pb = pk[c / 2 + 1];
           float t0, t1, t2, t3;
@@ -488,10 +509,10 @@ __global__ void __maxnreg__(168)
           dsk[2 * q4] = pack_bf16x2(t0, t1);
           dsk[2 * q4 + 1] = pack_bf16x2(t2, t3);
         }
-        tmem_st_x16(tP + lane_off + col_bf16 + 16 * half, dsk);
+        tmem_st_x16(tP + lane_off + col_bf16 + c32 / 2, dsk);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, static_cast<int>(col_f32) + half * 32 + 8 * e)) =
+          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, col_f32 + c32 + 8 * e)) =
               make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
       }
       tmem_wait_st();
@@ -499,8 +520,8 @@ __global__ void __maxnreg__(168)
       tc_fence_before();
       mbar_arrive(ds_full);
     }
-    // Epilogue: drain the last dQ; then the first column half stores dV rows, the
-    // second dK rows (dK already carries the scale).
+    // Epilogue: drain the last dQ; then the groups store the dV and dK rows, each group a
+    // contiguous slice of [dV | dK] (dK already carries the scale).
     if (ok && warp_wait(dq_full, (T - 1) & 1, ctl)) {
       tc_fence_after();
       ok = drain_dq(T - 1);
@@ -509,20 +530,24 @@ __global__ void __maxnreg__(168)
     }
     if (ok && warp_wait(acc_done, 0, ctl)) {
       tc_fence_after();
+      constexpr int kPer = 2 * HD / kBwdGroups;   // output columns per group
+      const int first = kPer * g;                 // in the concatenation [dV | dK]
+      const bool is_dk = first >= HD;
+      const int c0 = first % HD;
       const int jg = n * kTileRows + j;
       const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
-      const uint32_t tsrc = g == 0 ? tdV : tdK;
-      __nv_bfloat16 *dst_row = (g == 0 ? dv : dk) + row_off;
+      const uint32_t tsrc = (is_dk ? tdK : tdV) + c0;
+      __nv_bfloat16 *dst_row = (is_dk ? dk : dv) + row_off + c0;
 #pragma unroll
-      for (int c = 0; c < HD; c += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tsrc + lane_off + c, v);
+      for (int c = 0; c < kPer; c += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tsrc + lane_off + c, v);
         tmem_wait_ld();
-        reg_fence<32>(v);
+        reg_fence<16>(v);
         if (jg < S) {
           uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
+          for (int e = 0; e < 2; ++e)
             dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]), __uint_as_float(v[8 * e + 1])),
                                 pack_bf16x2(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3])),
                                 pack_bf16x2(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5])),

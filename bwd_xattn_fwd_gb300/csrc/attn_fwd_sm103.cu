@@ -5,26 +5,31 @@
 // log-sum-exp is kept for the backward. Grouped KV heads (row T15): query head h reads
 // kv head h / group.
 //
-// GB300 mapping (one CTA per 128-row query tile, 12 warps):
-//   warp 0     : TMA producer. Q tile once; K/V tiles into a 3-stage shared-memory ring.
-//   warp 1     : allocates TMEM; one lane issues tcgen05.mma:
-//                  S_n  = Q K_n^T  (A, B from shared memory)      -> TMEM, double-buffered
-//                  O   += P_n V_n  (A = P from TMEM, B from smem) -> TMEM accumulator
-//   warps 4-11 : softmax, one thread per query row (TMEM lane) and key-column half.
-//                Loads S_n, applies the causal mask on the diagonal tile, keeps the
-//                running max and sum in fp32 (log2 domain), writes P_n (bf16) to TMEM,
-//                and rescales O only when the running max grows by more than 2^8 (the
-//                stale max is exact because the final normalisation uses the same max).
-//                Epilogue: O / l in bf16 and LSE = (m + log2 l) ln 2.
-// Causal tile skipping: query tile m visits key tiles 0..m only. Tiles are issued
-// longest first (m descending) so the last wave holds short tiles.
+// GB300 mapping: one CTA per pair of 128-row query tiles A = 2j and B = 2j+1 of one
+// (batch, head) -- 256 query rows that share every K/V tile they read -- 12 warps:
+//   warp 0     : TMA producer. Q_A and Q_B once; K/V tiles through a 3-stage ring.
+//   warp 1     : TMEM owner and MMA issuer (converged warp, one elected lane issues):
+//                  S_X(n) = Q_X K_n^T  (A, B from shared memory) -> TMEM
+//                  O_X   += P_X(n) V_n (A = P from TMEM)          -> TMEM accumulator
+//                alternating X = A, B, so the tensor core works on one tile while the
+//                other tile's softmax runs.
+//   warps 4-7  : softmax of tile A, one thread per query row (TMEM lane), all 128 key
+//                columns of a tile; warps 8-11 the same for tile B.
+//   warps 2-3  : idle.
+// Softmax per key tile: causal mask on the diagonal tile, running max and sum in fp32
+// (log2 domain), P in bf16 to TMEM, O rescaled only when the running max grows by more
+// than 2^8 (the stale max is exact because the final normalisation uses the same max).
+// Epilogue: O / l in bf16, LSE = (m + log2 l) ln 2.
+// Causal tile skipping: tile m visits key tiles 0..m. CTAs are issued longest first.
+// TMEM columns: S_A [0,128) S_B [128,256) fp32 | O_A [256,256+HD) O_B [320,320+HD) fp32 |
+//               P_A [384,448) P_B [448,512) bf16 pairs.
 #include "sm103_ptx.cuh"
 #include "xattn_internal.h"
 
 namespace xattn {
 namespace {
 
-constexpr int kFwdThreads = 384;  // 12 warps, see the role map in the kernel
+constexpr int kFwdThreads = 384;  // 12 warps
 constexpr int kFwdStages = 3;
 
 template <int HD>
@@ -32,13 +37,12 @@ struct FwdLayout {
   static constexpr uint32_t kRowBytes = HD * 2;
   static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
   static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTileBytes;
+  static constexpr uint32_t kQ = 0;                                  // Q_A, Q_B
+  static constexpr uint32_t kK = kQ + 2 * kTileBytes;
   static constexpr uint32_t kV = kK + kFwdStages * kTileBytes;
-  static constexpr uint32_t kRed = kV + kFwdStages * kTileBytes;  // max [2][2][128], l [2][128]
-  static constexpr uint32_t kBars = kRed + 3 * 1024;
-  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done, mma_final, pair[4]
-  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 4;
+  static constexpr uint32_t kBars = kV + kFwdStages * kTileBytes;
+  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done[2], mma_final
+  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 1;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   // Ask for enough shared memory that one CTA occupies an SM: each CTA holds all 512
@@ -52,28 +56,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(0xffffffffu, ok);
 }
 
-// TMEM <-> registers for half an O row (HD/2 columns).
-template <int N>
-__device__ __forceinline__ void tmem_ld_half(uint32_t taddr, uint32_t *r) {
-  if constexpr (N == 32) tmem_ld_x32(taddr, r);
-  else tmem_ld_x16(taddr, r);
-}
-template <int N>
-__device__ __forceinline__ void tmem_st_half(uint32_t taddr, const uint32_t *r) {
-  if constexpr (N == 32) tmem_st_x32(taddr, r);
-  else tmem_st_x16(taddr, r);
-}
-
-// Role map (12 warps):
-//   warp 0    : TMA producer (Q once, K/V through a 3-stage ring)
-//   warp 1    : TMEM owner and MMA issuer
-//   warps 2-3 : idle
-//   warps 4-11: softmax, one thread per query row; warps 4-7 take key columns 0-63 of
-//               each 128-column tile and warps 8-11 columns 64-127, so each SM
-//               sub-partition interleaves two softmax warps. The two halves of a row
-//               exchange their partial maxima through shared memory each tile.
-// TMEM columns: S double buffer [0,128) [128,256) fp32 | O [256,256+HD) fp32 |
-//               P double buffer [320,384) [384,448) bf16
 template <int HD>
 __global__ void __maxnreg__(168)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -81,26 +63,26 @@ __global__ void __maxnreg__(168)
                     float *__restrict__ lse, int B, int S, int nh, int nkv, float scale_log2,
                     int *status, unsigned long long timeout_ns) {
   using L = FwdLayout<HD>;
-  constexpr int kHalf = HD / 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // Tile of this CTA, longest first.
+  // Tile pair of this CTA, longest first.
   const int num_m = (S + kTileRows - 1) / kTileRows;
+  const int num_pairs = (num_m + 1) / 2;
   const int BH = B * nh;
-  const int m = num_m - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int jp = num_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int b = bh / nh, h = bh % nh;
   const int kvh = h / (nh / nkv);
-  const int n_kv = m + 1;
+  const int mA = 2 * jp, mB = 2 * jp + 1;
+  const bool hasB = mB < num_m;
+  const int n_last = hasB ? mB : mA;       // last key tile of the pair
 
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sK = smem_u32(smem + L::kK);
   const uint32_t sV = smem_u32(smem + L::kV);
-  float *red_max = reinterpret_cast<float *>(smem + L::kRed);          // [2 tiles][2 halves][128]
-  float *red_l = reinterpret_cast<float *>(smem + L::kRed + 2048);     // [2 halves][128]
   const uint32_t bar0 = smem_u32(smem + L::kBars);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const uint32_t q_full = bar(0);
@@ -108,9 +90,8 @@ __global__ void __maxnreg__(168)
   auto empty = [&](int s) { return bar(1 + kFwdStages + s); };
   auto s_full = [&](int x) { return bar(1 + 2 * kFwdStages + x); };
   auto p_full = [&](int x) { return bar(3 + 2 * kFwdStages + x); };
-  const uint32_t o_done = bar(5 + 2 * kFwdStages);
-  const uint32_t mma_final = bar(6 + 2 * kFwdStages);
-  auto pair_bar = [&](int q) { return bar(7 + 2 * kFwdStages + q); };
+  auto o_done = [&](int x) { return bar(5 + 2 * kFwdStages + x); };
+  const uint32_t mma_final = bar(7 + 2 * kFwdStages);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -124,11 +105,10 @@ __global__ void __maxnreg__(168)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full(x), 1);
-      mbar_init(p_full(x), 256);
+      mbar_init(p_full(x), 128);
+      mbar_init(o_done(x), 1);
     }
-    mbar_init(o_done, 1);
     mbar_init(mma_final, 1);
-    for (int q = 0; q < 4; ++q) mbar_init(pair_bar(q), 64);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -144,16 +124,17 @@ __global__ void __maxnreg__(168)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS[2] = {tmem, tmem + 128};
-  const uint32_t tO = tmem + 256;
-  const uint32_t tP[2] = {tmem + 320, tmem + 384};
+  auto tS = [&](int x) { return tmem + 128u * x; };
+  auto tO = [&](int x) { return tmem + 256u + 64u * x; };
+  auto tP = [&](int x) { return tmem + 384u + 64u * x; };
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
-    mbar_expect_tx_elect(q_full, L::kTileBytes);
-    tma_load_4d_elect(sQ, &mq, q_full, 0, h, m * kTileRows, b);
+    mbar_expect_tx_elect(q_full, (hasB ? 2 : 1) * L::kTileBytes);
+    tma_load_4d_elect(sQ, &mq, q_full, 0, h, mA * kTileRows, b);
+    if (hasB) tma_load_4d_elect(sQ + L::kTileBytes, &mq, q_full, 0, h, mB * kTileRows, b);
     int issued = 0;
-    for (int n = 0, s = 0, ph = 0; n < n_kv; ++n) {
+    for (int n = 0, s = 0, ph = 0; n <= n_last; ++n) {
       if (!warp_wait(empty(s), ph ^ 1, ctl)) break;
       mbar_expect_tx_elect(full(s), 2 * L::kTileBytes);
       tma_load_4d_elect(sK + s * L::kTileBytes, &mk, full(s), 0, kvh, n * kTileRows, b);
@@ -166,159 +147,191 @@ __global__ void __maxnreg__(168)
     for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
       mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
   } else if (warp == 1) {
-    // ---------------- MMA issuer (converged warp, one elected lane issues) ----------------
+    // ---------------- MMA issuer ----------------
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
-    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;        // stage stride, descriptor units
+    constexpr uint32_t kStageDesc = L::kTileBytes >> 4;        // tile stride, descriptor units
     constexpr uint32_t kVStep = (16 * L::kRowBytes) >> 4;      // 16 key rows of V
     // Descriptors are built once; a K step of 16 elements is +32 bytes (+2) within the
     // swizzled K-major rows of Q and K, and +16 rows of the MN-major V tile.
     const uint64_t dQ = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t dK = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t dV = smem_desc(sV, 8192, 8 * L::kRowBytes, L::kSwizzle);
-    auto issue_qk = [&](uint32_t d, int s) {
+    auto issue_qk = [&](int x, int s) {
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        mma_ss_elect(d, dQ + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
+        mma_ss_elect(tS(x), dQ + x * kStageDesc + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk,
+                     kk > 0);
+    };
+    auto issue_pv = [&](int x, int s, bool first) {
+#pragma unroll
+      for (int kk = 0; kk < kTileRows / 16; ++kk)
+        mma_ts_elect(tO(x), tP(x) + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv,
+                     (!first || kk > 0) ? 1u : 0u);
     };
     bool ok = warp_wait(q_full, 0, ctl) && warp_wait(full(0), 0, ctl);
     if (ok) {
       tc_fence_after();
-      issue_qk(tS[0], 0);
+      issue_qk(0, 0);
       mma_commit_elect(s_full(0));
-    }
-    for (int n = 0, s = 0, s1 = 1 % kFwdStages, ph1 = (1 / kFwdStages) & 1; ok && n < n_kv; ++n) {
-      if (n + 1 < n_kv) {
-        // S(n+1) goes into the buffer of S(n-1), which the softmax finished reading
-        // before it signalled P(n-1) (waited for in the previous iteration).
-        if (!warp_wait(full(s1), ph1, ctl)) break;
-        tc_fence_after();
-        issue_qk(tS[(n + 1) & 1], s1);
-        mma_commit_elect(s_full((n + 1) & 1));
+      if (hasB) {
+        issue_qk(1, 0);
+        mma_commit_elect(s_full(1));
       }
-      if (!warp_wait(p_full(n & 1), (n >> 1) & 1, ctl)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kTileRows / 16; ++kk)
-        mma_ts_elect(tO, tP[n & 1] + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv,
-                     (n > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_elect(empty(s));
-      mma_commit_elect(o_done);
+    }
+    for (int n = 0, s = 0, s1 = 1 % kFwdStages, ph1 = (1 / kFwdStages) & 1; ok && n <= n_last; ++n) {
+      bool next_loaded = false;
+      // Tile A: PV_A(n), then S_A(n+1) into the S_A buffer the softmax finished reading
+      // before it signalled P_A(n).
+      if (n <= mA) {
+        if (!warp_wait(p_full(0), n & 1, ctl)) break;
+        tc_fence_after();
+        issue_pv(0, s, n == 0);
+        mma_commit_elect(o_done(0));
+        if (n + 1 <= mA) {
+          if (!warp_wait(full(s1), ph1, ctl)) break;
+          next_loaded = true;
+          tc_fence_after();
+          issue_qk(0, s1);
+          mma_commit_elect(s_full(0));
+        }
+      }
+      // Tile B likewise.
+      if (hasB) {
+        if (!warp_wait(p_full(1), n & 1, ctl)) break;
+        tc_fence_after();
+        issue_pv(1, s, n == 0);
+        mma_commit_elect(o_done(1));
+        if (n + 1 <= mB) {
+          if (!next_loaded && !warp_wait(full(s1), ph1, ctl)) break;
+          tc_fence_after();
+          issue_qk(1, s1);
+          mma_commit_elect(s_full(1));
+        }
+      }
+      mma_commit_elect(empty(s));                  // K_n and V_n fully consumed
       if (++s == kFwdStages) s = 0;
       if (++s1 == kFwdStages) { s1 = 0; ph1 ^= 1; }
     }
     mma_commit_elect(mma_final);
     mbar_drain(mma_final, 0, ctl);
   } else if (warp >= 4) {
-    // ---------------- softmax + epilogue ----------------
-    const int g = (warp - 4) >> 2;           // key-column half of every tile
+    // ---------------- softmax + epilogue: one thread per query row of tile X ----------------
+    const int x = (warp - 4) >> 2;          // 0 = tile A, 1 = tile B
+    const int mX = x == 0 ? mA : mB;
+    const bool active = x == 0 || hasB;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t pbar = pair_bar(quarter);
-    uint32_t pair_phase = 0;
-    float mrow = -INFINITY, lpart = 0.f;
-    bool ok = true;
-    for (int n = 0; n < n_kv; ++n) {
-      if (!warp_wait(s_full(n & 1), (n >> 1) & 1, ctl)) { ok = false; break; }
+    const uint32_t tSx = tS(x) + lane_off, tOx = tO(x) + lane_off, tPx = tP(x) + lane_off;
+    float mrow = -INFINITY, lrow = 0.f;
+    bool ok = active;
+    for (int n = 0; ok && n <= mX; ++n) {
+      if (!warp_wait(s_full(x), n & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[64];
-      tmem_ld_x32(tS[n & 1] + lane_off + 64 * g, r);
-      tmem_ld_x32(tS[n & 1] + lane_off + 64 * g + 32, r + 32);
-      tmem_wait_ld();
-      reg_fence<64>(r);
-      // Causal mask (diagonal tile only; the branch is uniform across the CTA).
-      if (n == m) {
-        const int col0 = 64 * g;
+      const bool diag = (n == mX);
+      // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0, so the
+      // scaled maximum is the image of the raw one).
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int c64 = 0; c64 < 128; c64 += 64) {
+        uint32_t r[64];
+        tmem_ld_x32(tSx + c64, r);
+        tmem_ld_x32(tSx + c64 + 32, r + 32);
+        tmem_wait_ld();
+        reg_fence<64>(r);
+        if (diag) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c)
-          if (col0 + c > row) r[c] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < 64; ++c)
+            if (c64 + c > row) r[c] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 2)
+          mx4[(c >> 1) & 3] = fmax3(mx4[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
       }
-      // Row maximum of the raw scores (scale > 0, so the scaled maximum is its image).
-      float mx4[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-        mx4[a] = fmax3(__uint_as_float(r[2 * a]), __uint_as_float(r[2 * a + 1]), -INFINITY);
-#pragma unroll
-      for (int c = 8; c < 64; c += 2)
-        mx4[(c >> 1) & 3] = fmax3(mx4[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
-      const float pmax = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]));
-      // Row maximum across the two column halves (double-buffered by tile parity).
-      red_max[((n & 1) * 2 + g) * 128 + row] = pmax;
-      mbar_arrive(pbar);
-      if (!warp_wait(pbar, pair_phase & 1, ctl)) { ok = false; break; }
-      ++pair_phase;
-      const float mx = fmaxf(pmax, red_max[((n & 1) * 2 + (g ^ 1)) * 128 + row]) * scale_log2;
+      const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * scale_log2;
       // Conditional rescaling: keep the stale max unless some row of the warp grew by
-      // more than 2^8; the decision is per warp because TMEM loads/stores are collective,
-      // and both halves of a row reach the same decision from the same maxima.
+      // more than 2^8; the decision is per warp because TMEM loads/stores are collective.
       const float mnew = fmaxf(mrow, mx);
       const bool rescale = __any_sync(0xffffffffu, mnew > mrow + 8.0f);
       const float m_use = rescale ? mnew : mrow;
       const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
       const float neg_m = -m_use;
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t pk[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        float x0, x1;
-        ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
-              scale_log2, neg_m, neg_m);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        const int a = (e & 1) * 2;
-        fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
-        pk[e] = pack_bf16x2(p0, p1);
-      }
-      // P(n) goes into the buffer PV(n-2) read; that PV was waited for last iteration.
-      tmem_st_x16(tP[n & 1] + lane_off + 32 * g, pk);
-      tmem_st_x16(tP[n & 1] + lane_off + 32 * g + 16, pk + 16);
-      // PV(n-1) is waited for on every tile, not only when rescaling: a parity wait is
-      // only unambiguous if the waiter has seen every earlier phase of the barrier.
+      // P_X(n) overwrites P_X(n-1), and O_X may be rescaled: PV_X(n-1) must be done.
+      // Every phase of o_done is waited for in order, so the parity wait is unambiguous.
       if (n > 0) {
-        if (!warp_wait(o_done, (n - 1) & 1, ctl)) { ok = false; break; }
+        if (!warp_wait(o_done(x), (n - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        if (rescale) {
-          uint32_t ov[kHalf];
-          tmem_ld_half<kHalf>(tO + lane_off + kHalf * g, ov);
-          tmem_wait_ld();
-          reg_fence<kHalf>(ov);
+      }
+      // Pass 2: exponentials, row sum and bf16 P, 64 columns at a time.
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int c64 = 0; c64 < 128; c64 += 64) {
+        uint32_t r[64];
+        tmem_ld_x32(tSx + c64, r);
+        tmem_ld_x32(tSx + c64 + 32, r + 32);
+        tmem_wait_ld();
+        reg_fence<64>(r);
+        if (diag) {
 #pragma unroll
-          for (int e = 0; e < kHalf; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st_half<kHalf>(tO + lane_off + kHalf * g, ov);
+          for (int c = 0; c < 64; ++c)
+            if (c64 + c > row) r[c] = __float_as_uint(-INFINITY);
+        }
+        uint32_t pk[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
+                scale_log2, neg_m, neg_m);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const int a = (e & 1) * 2;
+          fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
+          pk[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_x16(tPx + c64 / 2, pk);
+        tmem_st_x16(tPx + c64 / 2 + 16, pk + 16);
+      }
+      if (rescale && n > 0) {
+#pragma unroll
+        for (int c = 0; c < HD; c += 32) {
+          uint32_t ov[32];
+          tmem_ld_x32(tOx + c, ov);
+          tmem_wait_ld();
+          reg_fence<32>(ov);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st_x32(tOx + c, ov);
         }
       }
-      lpart = lpart * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+      lrow = lrow * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
       mrow = m_use;
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full(n & 1));
+      mbar_arrive(p_full(x));
     }
-    if (ok && warp_wait(o_done, (n_kv - 1) & 1, ctl)) {
+    if (ok && warp_wait(o_done(x), mX & 1, ctl)) {
       tc_fence_after();
-      red_l[g * 128 + row] = lpart;
-      mbar_arrive(pbar);
-      if (warp_wait(pbar, pair_phase & 1, ctl)) {
-        const float l = lpart + red_l[(g ^ 1) * 128 + row];
-        const int i = m * kTileRows + row;
-        const float inv = 1.f / l;
-        uint32_t ov[kHalf];
-        tmem_ld_half<kHalf>(tO + lane_off + kHalf * g, ov);
-        tmem_wait_ld();
-        reg_fence<kHalf>(ov);
-        if (i < S) {
-          __nv_bfloat16 *orow = o + (static_cast<size_t>(b) * S + i) * nh * HD +
-                                static_cast<size_t>(h) * HD + kHalf * g;
-          uint4 *dst = reinterpret_cast<uint4 *>(orow);
+      const int i = mX * kTileRows + row;
+      const float inv = 1.f / lrow;
+      __nv_bfloat16 *orow = o + (static_cast<size_t>(b) * S + i) * nh * HD + static_cast<size_t>(h) * HD;
 #pragma unroll
-          for (int e = 0; e < kHalf / 8; ++e)
+      for (int c = 0; c < HD; c += 32) {
+        uint32_t ov[32];
+        tmem_ld_x32(tOx + c, ov);
+        tmem_wait_ld();
+        reg_fence<32>(ov);
+        if (i < S) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
             dst[e] = make_uint4(
                 pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv),
                 pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv));
-          if (g == 0) lse[(static_cast<size_t>(b) * S + i) * nh + h] = (mrow + __log2f(l)) * kLn2;
         }
       }
+      if (i < S) lse[(static_cast<size_t>(b) * S + i) * nh + h] = (mrow + __log2f(lrow)) * kLn2;
     }
   }
 
@@ -339,7 +352,7 @@ cudaError_t launch_fwd_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CU
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
   if (err != cudaSuccess) return err;
   const int num_m = (S + kTileRows - 1) / kTileRows;
-  const unsigned grid = static_cast<unsigned>(B) * nh * num_m;
+  const unsigned grid = static_cast<unsigned>(B) * nh * ((num_m + 1) / 2);
   attn_fwd_kernel<HD><<<grid, kFwdThreads, L::kDynBytes, stream>>>(
       mq, mk, mv, o, lse, B, S, nh, nkv, scale * kLog2e, status, timeout_ns);
   return cudaGetLastError();

@@ -344,6 +344,12 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 #define XATTN_W8(i) "r"(r[i]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
                     "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
 
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t *r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : XATTN_R8(0)
+               : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t *r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "

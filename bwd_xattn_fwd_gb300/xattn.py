@@ -18,7 +18,8 @@ import os
 
 from . import build as _build
 
-_LIB_PATH = _build.LIB
+# XATTN_LIBRARY may name another build of libxattn (for example an instrumented one).
+_LIB_PATH = os.environ.get("XATTN_LIBRARY") or _build.LIB
 
 if not os.path.exists(_LIB_PATH):
     raise ImportError(
