@@ -12,7 +12,8 @@
 //                  S_X(n) = Q_X K_n^T  (A, B from shared memory) -> TMEM
 //                  O_X   += P_X(n) V_n (A = P from TMEM)          -> TMEM accumulator
 //                alternating X = A, B, so the tensor core works on one tile while the
-//                other tile's softmax runs.
+//                other tile's softmax runs; S_X(n+1) is issued as soon as the softmax has
+//                read S_X(n), before it finishes P_X(n).
 //   warps 4-7  : softmax of tile A, one thread per query row (TMEM lane), all 128 key
 //                columns of a tile; warps 8-11 the same for tile B.
 //   warps 2-3  : idle.
@@ -41,8 +42,9 @@ struct FwdLayout {
   static constexpr uint32_t kK = kQ + 2 * kTileBytes;
   static constexpr uint32_t kV = kK + kFwdStages * kTileBytes;
   static constexpr uint32_t kBars = kV + kFwdStages * kTileBytes;
-  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done[2], mma_final
-  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 1;
+  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done[2], mma_final,
+  //           s_free[2]
+  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 1 + 2;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   // Ask for enough shared memory that one CTA occupies an SM: each CTA holds all 512
@@ -92,6 +94,7 @@ __global__ void __maxnreg__(168)
   auto p_full = [&](int x) { return bar(3 + 2 * kFwdStages + x); };
   auto o_done = [&](int x) { return bar(5 + 2 * kFwdStages + x); };
   const uint32_t mma_final = bar(7 + 2 * kFwdStages);
+  auto s_free = [&](int x) { return bar(8 + 2 * kFwdStages + x); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -107,6 +110,7 @@ __global__ void __maxnreg__(168)
       mbar_init(s_full(x), 1);
       mbar_init(p_full(x), 128);
       mbar_init(o_done(x), 1);
+      mbar_init(s_free(x), 128);
     }
     mbar_init(mma_final, 1);
     fence_mbar_init();
@@ -179,36 +183,31 @@ __global__ void __maxnreg__(168)
         mma_commit_elect(s_full(1));
       }
     }
+    // Per key tile n and query tile X: S_X(n+1) as soon as the softmax has loaded the
+    // last of S_X(n) (s_free, signalled half-way through its exponentials), then PV_X(n)
+    // once P_X(n) is in TMEM (p_full). The next scores are thus computed while the
+    // softmax is still producing P_X(n).
     for (int n = 0, s = 0, s1 = 1 % kFwdStages, ph1 = (1 / kFwdStages) & 1; ok && n <= n_last; ++n) {
       bool next_loaded = false;
-      // Tile A: PV_A(n), then S_A(n+1) into the S_A buffer the softmax finished reading
-      // before it signalled P_A(n).
-      if (n <= mA) {
-        if (!warp_wait(p_full(0), n & 1, ctl)) break;
-        tc_fence_after();
-        issue_pv(0, s, n == 0);
-        mma_commit_elect(o_done(0));
-        if (n + 1 <= mA) {
-          if (!warp_wait(full(s1), ph1, ctl)) break;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int mX = x == 0 ? mA : mB;
+        if (x == 1 && !hasB) break;
+        if (n > mX) continue;
+        if (n + 1 <= mX) {
+          if (!warp_wait(s_free(x), n & 1, ctl)) { ok = false; break; }
+          if (!next_loaded && !warp_wait(full(s1), ph1, ctl)) { ok = false; break; }
           next_loaded = true;
           tc_fence_after();
-          issue_qk(0, s1);
-          mma_commit_elect(s_full(0));
+          issue_qk(x, s1);
+          mma_commit_elect(s_full(x));
         }
-      }
-      // Tile B likewise.
-      if (hasB) {
-        if (!warp_wait(p_full(1), n & 1, ctl)) break;
+        if (!warp_wait(p_full(x), n & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-        issue_pv(1, s, n == 0);
-        mma_commit_elect(o_done(1));
-        if (n + 1 <= mB) {
-          if (!next_loaded && !warp_wait(full(s1), ph1, ctl)) break;
-          tc_fence_after();
-          issue_qk(1, s1);
-          mma_commit_elect(s_full(1));
-        }
+        issue_pv(x, s, n == 0);
+        mma_commit_elect(o_done(x));
       }
+      if (!ok) break;
       mma_commit_elect(empty(s));                  // K_n and V_n fully consumed
       if (++s == kFwdStages) s = 0;
       if (++s1 == kFwdStages) { s1 = 0; ph1 ^= 1; }
@@ -272,6 +271,10 @@ __global__ void __maxnreg__(168)
         tmem_ld_x32(tSx + c64 + 32, r + 32);
         tmem_wait_ld();
         reg_fence<64>(r);
+        if (c64 == 64) {                   // S_X(n) fully read: its buffer may be refilled
+          tc_fence_before();
+          mbar_arrive(s_free(x));
+        }
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
