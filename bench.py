@@ -267,14 +267,14 @@ def run_ours(args, w: W.Workload):
         xattn.xattn_fwd(x["q"], x["k"], x["v"], B, S, nh, nkv, hd, scale, o, lse, stream)
         if evs:
             evs[1].record(stream)
-        xattn.xattn_bwd_preprocess(o, x["dO"], lse, B, S, nh, hd, ws, ws_bytes, stream)
+        xattn.xattn_bwd_preprocess(o, x["dO"], lse, B, S, nh, hd, scale, ws, ws_bytes, stream)
         if evs:
             evs[2].record(stream)
         xattn.xattn_bwd_main(x["q"], x["k"], x["v"], x["dO"], B, S, nh, nkv, hd, scale, dk, dv,
                              ws, ws_bytes, stream)
         if evs:
             evs[3].record(stream)
-        xattn.xattn_bwd_dq_convert(B, S, nh, hd, dq, ws, ws_bytes, stream)
+        xattn.xattn_bwd_dq_convert(B, S, nh, hd, scale, dq, ws, ws_bytes, stream)
         if evs:
             evs[4].record(stream)
 

@@ -16,16 +16,17 @@
 //      dK/dV, and a fixed order, so they are reproducible. Per (r, m):
 //        S^T  = K_n Q_m^T               (TMEM, 128 x 128 fp32)
 //        dP^T = V_n dO_m^T              (TMEM, 128 x 128 fp32)
-//        P^T  = exp2(S^T scale log2e - LSE2_m)      -> bf16 into a TMEM slot
-//        dS^T = scale * P^T (dP^T - D_m)            -> bf16 into the same slot, and
-//                                                      into shared memory (MN-major)
-//        dV_n += P^T dO_m ,  dK_n += dS^T Q_m       (A operand from TMEM)
+//        P^T  = exp2(S^T scale log2e - LSE2_m)      -> bf16 into TMEM
+//        dS^T = P^T (dP^T - D_m)                    -> bf16 into shared memory
+//        dV_n += P^T dO_m                           (A operand from TMEM)
+//        dK_n += dS^T Q_m                           (A operand from shared memory)
 //        dQ_m  = dS K_n                 (TMEM) -> shared memory -> TMA reduce-add into
 //                                                      the fp32 accumulator
-//      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 4-11 = P/dS (one thread
-//      per key row, two warps per row splitting the 128 query columns), which also
-//      drain each dQ tile from TMEM.
-//   3. dq convert: dq = bf16(accumulator).
+//      The softmax scale of dS is applied once at the end, to dK_n in the epilogue and
+//      to dQ in step 3, instead of to every element of every dS tile.
+//      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2 = dQ reducer,
+//      4-7 = P (one thread per key row), 8-11 = dS and the dQ drain.
+//   3. dq convert: dq = bf16(scale * accumulator).
 #include "sm103_ptx.cuh"
 #include "xattn_internal.h"
 
@@ -34,7 +35,7 @@ namespace xattn {
 size_t bwd_workspace_bytes(int B, int S, int nh, int hd) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t rows = static_cast<size_t>(B) * nh * padded_rows(S);
-  return up(rows * 4) * 2 + up(static_cast<size_t>(B) * S * nh * hd * 4);
+  return up(rows * kAuxCols * 2) + up(static_cast<size_t>(B) * S * nh * hd * 4);
 }
 
 BwdWorkspace bwd_workspace_carve(void *base, int B, int S, int nh, int hd) {
@@ -43,9 +44,8 @@ BwdWorkspace bwd_workspace_carve(void *base, int B, int S, int nh, int hd) {
   const size_t rows = static_cast<size_t>(B) * nh * padded_rows(S);
   uint8_t *p = static_cast<uint8_t *>(base);
   BwdWorkspace ws;
-  ws.D = reinterpret_cast<float *>(p);
-  ws.lse2 = reinterpret_cast<float *>(p + up(rows * 4));
-  ws.dqacc = reinterpret_cast<float *>(p + 2 * up(rows * 4));
+  ws.aux = reinterpret_cast<__nv_bfloat16 *>(p);
+  ws.dqacc = reinterpret_cast<float *>(p + up(rows * kAuxCols * 2));
   return ws;
 }
 
@@ -54,17 +54,30 @@ namespace {
 // ------------------------------------------------------------------------------------
 // 1. preprocess
 // ------------------------------------------------------------------------------------
+// v ~= hi + mid + lo with three bf16 terms (each rounded to nearest); the residual is
+// below 2^-26 |v|.
+__device__ __forceinline__ void split3_bf16(float v, uint16_t out[3]) {
+  const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+  out[0] = __bfloat16_as_ushort(hi);
+  out[1] = __bfloat16_as_ushort(mid);
+  out[2] = __bfloat16_as_ushort(lo);
+}
+
 // One group of (hd / 8) lanes per row (b, i, h): each lane reads 8 bf16 of O and dO
 // (16 B each), the group reduces with shuffles. Rows are enumerated in memory order of
 // O/dO, so the loads are fully coalesced. The same lanes zero the row of the dQ
-// accumulator. Both vectors are stored negated (-D and -LSE log2 e), which is the form
-// the main kernel adds. Pad rows (S <= i < S_pad) get 0 and -inf, so that the main
-// kernel's partial query tiles contribute exactly zero.
+// accumulator, and the group's first lane writes the row's auxiliary operand: -LSE/scale
+// and -D, the two per-query terms that the main kernel's tensor-core products add to
+// S^T and dP^T. Pad rows (S <= i < S_pad) are all zero: their Q and dO rows are zero
+// too, so they contribute nothing whatever P is there.
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
     const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dO,
-    const float *__restrict__ lse, float *__restrict__ D, float *__restrict__ lse2,
-    float *__restrict__ dqacc, int B, int S, int nh) {
+    const float *__restrict__ lse, uint4 *__restrict__ aux, float *__restrict__ dqacc,
+    int B, int S, int nh, float lse_mult) {
   constexpr int kLanesPerRow = HD / 8;
   const int S_pad = padded_rows(S);
   const long long n_rows = static_cast<long long>(B) * S * nh;
@@ -99,51 +112,46 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
       const int i = static_cast<int>(bi % S);
       const int b = static_cast<int>(bi / S);
       const size_t dst = (static_cast<size_t>(b) * nh + h) * S_pad + i;
-      D[dst] = -acc;
-      lse2[dst] = -lse[row] * kLog2e;
+      uint16_t l[3], d[3];
+      split3_bf16(-lse[row] * lse_mult, l);
+      split3_bf16(-acc, d);
+      aux[2 * dst] = make_uint4(l[0] | (static_cast<uint32_t>(l[1]) << 16), l[2] | (static_cast<uint32_t>(d[0]) << 16),
+                                d[1] | (static_cast<uint32_t>(d[2]) << 16), 0u);
+      aux[2 * dst + 1] = make_uint4(0u, 0u, 0u, 0u);
     }
   } else if (row - n_rows < n_pad && sub == 0) {
     const long long p = row - n_rows;
     const int pad = S_pad - S;
     const long long bh = p / pad;
     const int i = S + static_cast<int>(p % pad);
-    D[bh * S_pad + i] = 0.f;
-    lse2[bh * S_pad + i] = -INFINITY;
+    aux[2 * (bh * S_pad + i)] = make_uint4(0u, 0u, 0u, 0u);
+    aux[2 * (bh * S_pad + i) + 1] = make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
 // ------------------------------------------------------------------------------------
-// 3. dq convert: 8 elements per thread (two 16-byte loads, one 16-byte store).
+// 3. dq convert: 8 elements per thread (two 16-byte loads, one 16-byte store). The
+// accumulator holds dS K without the softmax scale.
 // ------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
                                                          __nv_bfloat16 *__restrict__ dq,
-                                                         size_t n8) {
+                                                         size_t n8, float scale) {
   const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n8) return;
   const float4 a = reinterpret_cast<const float4 *>(acc)[2 * t];
   const float4 c = reinterpret_cast<const float4 *>(acc)[2 * t + 1];
-  reinterpret_cast<uint4 *>(dq)[t] = make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w),
-                                                pack_bf16x2(c.x, c.y), pack_bf16x2(c.z, c.w));
+  reinterpret_cast<uint4 *>(dq)[t] =
+      make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                 pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
 }
 
 // ------------------------------------------------------------------------------------
 // 2. main kernel
 // ------------------------------------------------------------------------------------
-// Column groups of the P/dS work: each group of 4 warps owns 128 / kBwdGroups query
-// columns of every tile. Registers are split evenly over the 4 SM sub-partitions, so the
-// per-thread limit follows from the warp count (4 + 4 * groups warps).
-#ifndef XATTN_BWD_GROUPS
-#define XATTN_BWD_GROUPS 2
-#endif
-#if XATTN_BWD_GROUPS == 4
-#define XATTN_BWD_MAXNREG 96    // 20 warps: 5 per sub-partition
-#elif XATTN_BWD_GROUPS == 2
-#define XATTN_BWD_MAXNREG 168   // 12 warps: 3 per sub-partition
-#else
-#error "XATTN_BWD_GROUPS must be 2 or 4"
-#endif
-constexpr int kBwdGroups = XATTN_BWD_GROUPS;
-constexpr int kBwdThreads = 128 + 128 * kBwdGroups;
+// 12 warps. Registers are split evenly over the 4 SM sub-partitions (3 warps each), so
+// the per-thread limit is 65536 / 4 / 96 rounded down to the allocation granule.
+constexpr int kBwdThreads = 384;
+constexpr int kBwdStages = 3;      // Q / dO / LSE / D stages
 
 template <int HD>
 struct BwdLayout {
@@ -152,22 +160,25 @@ struct BwdLayout {
   static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kTileBytes;
-  static constexpr uint32_t kQ = kV + kTileBytes;          // 2 stages
-  static constexpr uint32_t kdO = kQ + 2 * kTileBytes;     // 2 stages
-  static constexpr uint32_t kdS = kdO + 2 * kTileBytes;    // 128 x 128 bf16, MN-major, 32 KB
-  // dQ staging for the TMA reduce-add: 2 buffers x 2 head-dim halves x 128 rows of
-  // HD/2 floats, swizzled like the tensor map's box.
+  static constexpr uint32_t kQ = kV + kTileBytes;                    // kBwdStages stages
+  static constexpr uint32_t kdO = kQ + kBwdStages * kTileBytes;      // kBwdStages stages
+  static constexpr uint32_t kdS = kdO + kBwdStages * kTileBytes;     // 128 x 128 bf16, 32 KB
+  // dQ staging for the TMA reduce-add: 2 head-dim halves x 128 rows of HD/2 floats,
+  // swizzled like the tensor map's box.
   static constexpr uint32_t kDqRowBytes = HD / 2 * 4;
   static constexpr uint32_t kDqHalfBytes = kTileRows * kDqRowBytes;
   static constexpr uint32_t kdQs = kdS + 32768;
-  static constexpr uint32_t kVec = kdQs + 4 * kDqHalfBytes;  // -LSE2[2][128], -D[2][128] fp32
-  // barriers: kv_full, full[2], empty[2], s_full, dp_full, p_full, ds_full, dq_full,
-  //           dq_empty, acc_done, dv_done, dk_done, dqs_full[2], dqs_empty[2]
-  static constexpr int kNumBars = 18;
-  static constexpr uint32_t kBars = kVec + 4 * 512;
+  // Auxiliary K step of S^T and dP^T (128 rows x 16 bf16, 32-byte swizzle, 4 KB each):
+  // two constant key-side tiles (ones under the LSE columns / under the D columns) and
+  // the query-side rows of each stage.
+  static constexpr uint32_t kAuxTileBytes = kTileRows * kAuxCols * 2;
+  static constexpr uint32_t kAuxA = kdQs + 2 * kDqHalfBytes;
+  static constexpr uint32_t kAuxB = kAuxA + 2 * kAuxTileBytes;      // kBwdStages stages
+  static constexpr int kNumBars = 20;
+  static constexpr uint32_t kBars = kAuxB + kBwdStages * kAuxTileBytes;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
-  static constexpr uint32_t kDynBytes = (kUsed + 1024 > 120 * 1024) ? kUsed + 1024 : 120 * 1024;
+  static constexpr uint32_t kDynBytes = kUsed + 1024;
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
@@ -175,38 +186,41 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(0xffffffffu, ok);
 }
 
-// Offset of element (key row j, query column i) of the 128 x 128 dS^T tile, stored as
-// the A operand of dQ = dS K: M = query (contiguous), K = key rows; two 64-column
-// atoms of 128-byte rows with the 128-byte swizzle (16-byte chunk ^= row % 8).
+// Offset of element (key row j, query column i) of the 128 x 128 dS^T tile in shared
+// memory: two 64-column halves of 128-byte rows (one row per key) with the 128-byte
+// swizzle (16-byte chunk ^= row % 8). Read as the A operand of dQ = dS K it is
+// MN-major (M = query, contiguous); read as the A operand of dK = dS^T Q it is
+// K-major (M = key rows, K = query), so one copy serves both products.
 __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
   return static_cast<uint32_t>((i >> 6) * 16384 + j * 128 + ((((i & 63) >> 3) ^ (j & 7)) << 4));
 }
 
-// Role map (4 + 4 * kBwdGroups warps):
+// Role map (12 warps):
 //   warp 0     : TMA producer
 //   warp 1     : TMEM owner and MMA issuer
 //   warp 2     : dQ reducer: TMA reduce-adds each staged dQ tile into the fp32
 //                accumulator (2 bulk operations per tile instead of scattered atomics)
 //   warp 3     : idle
-//   warps 4.. : P^T / dS^T, one thread per key row; warp group g (4 warps, one per TMEM
-//               lane quarter) owns query columns [g*C, (g+1)*C), C = 128 / kBwdGroups, so
-//               each SM sub-partition interleaves kBwdGroups of them. They also move
-//               dQ(t-1) from TMEM to a double-buffered shared-memory tile (one query row
-//               per thread, group g taking head-dim columns [g*HD/G, (g+1)*HD/G)).
-// TMEM columns: S^T [0,128) fp32 | dP^T [128,256) fp32 | P^T, then dS^T, bf16 [256,320)
-//               | dV [320,384) | dK [384,448) | dQ [448,512)
-// P^T and dS^T share one slot that no other result overlaps, so the two column halves
-// never write over values the other half still has to read; the MMA readers of that
-// slot (dV reads P^T, dK reads dS^T) are waited for before it is overwritten.
+//   warps 4-7  : P^T = exp2(S^T scale log2e - LSE2), one thread per key row, all 128
+//                query columns (the special-function work)
+//   warps 8-11 : dS^T = P^T (dP^T - D), one thread per key row (the FMA work), and the
+//                dQ drain (TMEM -> shared-memory staging, one query row per thread)
+// The two compute warpgroups work on consecutive (r, m) iterations at the same time, so
+// each SM sub-partition runs one warp of each and the exponentials of iteration t+1
+// overlap the dS arithmetic of iteration t.
+// TMEM columns: S^T [0,128) fp32 | dP^T [128,256) fp32 | P^T bf16 [256,320) |
+//               dV [320,384) | dK [384,448) | dQ [448,512)
+// Each region has one producer and its readers release it with an mbarrier before it is
+// rewritten: S^T (s_free), dP^T (dp_free), P^T (p_free by the dS warps, dv_done by the
+// dV product), dQ (dq_empty).
 template <int HD>
-__global__ void __maxnreg__(XATTN_BWD_MAXNREG)
+__global__ void __maxnreg__(168)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
-                         const __grid_constant__ CUtensorMap mdq,
-                         const float *__restrict__ Dvec, const float *__restrict__ lse2,
+                         const __grid_constant__ CUtensorMap maux, const __grid_constant__ CUtensorMap mdq,
                          __nv_bfloat16 *__restrict__ dk,
                          __nv_bfloat16 *__restrict__ dv, int B, int S, int nh, int nkv,
-                         float scale, float scale_log2, int *status, unsigned long long timeout_ns) {
+                         float scale, int *status, unsigned long long timeout_ns) {
   using L = BwdLayout<HD>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -231,18 +245,20 @@ __global__ void __maxnreg__(XATTN_BWD_MAXNREG)
   uint8_t *sdS_ptr = smem + L::kdS;
   const uint32_t sdS = smem_u32(sdS_ptr);
   uint8_t *sdQs_ptr = smem + L::kdQs;
-  float *sLSE = reinterpret_cast<float *>(smem + L::kVec);         // [2][128]  -LSE log2 e
-  float *sD = reinterpret_cast<float *>(smem + L::kVec + 1024);    // [2][128]  -D
+  const uint32_t sAuxA = smem_u32(smem + L::kAuxA);
+  const uint32_t sAuxB = smem_u32(smem + L::kAuxB);
+  // scale == 0: S^T is the auxiliary term alone (-LSE log2 e) and is not scaled.
+  const bool qk = (scale != 0.f);
+  const float scale_log2 = qk ? scale * kLog2e : 1.f;
   const uint32_t bar0 = smem_u32(smem + L::kBars);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const uint32_t kv_full = bar(0);
   auto full = [&](int s) { return bar(1 + s); };
-  auto empty = [&](int s) { return bar(3 + s); };
-  const uint32_t s_full = bar(5), dp_full = bar(6), p_full = bar(7), ds_full = bar(8);
-  const uint32_t dq_full = bar(9), dq_empty = bar(10), acc_done = bar(11);
-  const uint32_t dv_done = bar(12), dk_done = bar(13);
-  auto dqs_full = [&](int x) { return bar(14 + x); };
-  auto dqs_empty = [&](int x) { return bar(16 + x); };
+  auto empty = [&](int s) { return bar(1 + kBwdStages + s); };
+  const uint32_t s_full = bar(7), s_free = bar(8), dp_full = bar(9), dp_free = bar(10);
+  const uint32_t p_full = bar(11), p_free = bar(12), dv_done = bar(13), ds_full = bar(14);
+  const uint32_t dq_full = bar(15), dq_empty = bar(16), dqs_full = bar(17), dqs_empty = bar(18);
+  const uint32_t acc_done = bar(19);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -250,30 +266,42 @@ __global__ void __maxnreg__(XATTN_BWD_MAXNREG)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
     mbar_init(s_full, 1);
+    mbar_init(s_free, 128);
     mbar_init(dp_full, 1);
-    mbar_init(p_full, 128 * kBwdGroups);
-    mbar_init(ds_full, 128 * kBwdGroups);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128 * kBwdGroups);
-    mbar_init(acc_done, 1);
+    mbar_init(dp_free, 128);
+    mbar_init(p_full, 128);
+    mbar_init(p_free, 128);
     mbar_init(dv_done, 1);
-    mbar_init(dk_done, 1);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(dqs_full(x), 128 * kBwdGroups);
-      mbar_init(dqs_empty(x), 1);
-    }
+    mbar_init(ds_full, 128);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 128);
+    mbar_init(dqs_full, 128);
+    mbar_init(dqs_empty, 1);
+    mbar_init(acc_done, 1);
     fence_mbar_init();
   }
+  // Constant key-side auxiliary tiles: row r = [1 1 1 0 ...] (S^T) and [0 0 0 1 1 1 0 ...]
+  // (dP^T), stored with the 32-byte swizzle (16-byte chunk ^= (r >> 2) & 1).
+  for (int e = threadIdx.x; e < 2 * kTileRows * 2; e += kBwdThreads) {
+    const int tile = e / (2 * kTileRows), r = (e / 2) % kTileRows, ch = e % 2;
+    const uint32_t one = 0x3F80u;   // bf16 1.0
+    uint4 val = make_uint4(0u, 0u, 0u, 0u);
+    if (ch == 0) val = (tile == 0) ? make_uint4(one | (one << 16), one, 0u, 0u)
+                                   : make_uint4(0u, one << 16, one | (one << 16), 0u);
+    *reinterpret_cast<uint4 *>(smem + L::kAuxA + tile * L::kAuxTileBytes + r * 32 + ((ch ^ ((r >> 2) & 1)) << 4)) = val;
+  }
+  fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&mq);
     tma_prefetch_desc(&mk);
     tma_prefetch_desc(&mv);
     tma_prefetch_desc(&mdo);
+    tma_prefetch_desc(&maux);
     tma_prefetch_desc(&mdq);
   }
   if (warp == 1) {
@@ -293,31 +321,30 @@ __global__ void __maxnreg__(XATTN_BWD_MAXNREG)
     tma_load_4d_elect(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
     tma_load_4d_elect(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
     int issued = 0;
-    for (int t = 0, r = 0, m = n; t < T; ++t) {
+    for (int t = 0, r = 0, m = n, s = 0, use = 0; t < T; ++t) {
       const int h = kvh * group + r;
-      const int s = t & 1;
-      if (!warp_wait(empty(s), ((t >> 1) & 1) ^ 1, ctl)) break;
-      mbar_expect_tx_elect(full(s), 2 * L::kTileBytes + 2 * 512);
+      if (!warp_wait(empty(s), (use & 1) ^ 1, ctl)) break;
+      mbar_expect_tx_elect(full(s), 2 * L::kTileBytes + L::kAuxTileBytes);
       tma_load_4d_elect(sQ + s * L::kTileBytes, &mq, full(s), 0, h, m * kTileRows, b);
       tma_load_4d_elect(sdO + s * L::kTileBytes, &mdo, full(s), 0, h, m * kTileRows, b);
-      const size_t vec = (static_cast<size_t>(b) * nh + h) * S_pad + static_cast<size_t>(m) * kTileRows;
-      bulk_load_elect(smem_u32(sLSE + s * 128), lse2 + vec, 512, full(s));
-      bulk_load_elect(smem_u32(sD + s * 128), Dvec + vec, 512, full(s));
+      tma_load_4d_elect(sAuxB + s * L::kAuxTileBytes, &maux, full(s), 0, m * kTileRows, h, b);
       issued = t + 1;
       if (++m == num_m) { m = n; ++r; }
+      if (++s == kBwdStages) { s = 0; ++use; }
     }
+    // Every load has landed before the CTA can exit (the consumers may have given up).
     mbar_drain(kv_full, 0, ctl);
-    for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t)
-      mbar_drain(full(t & 1), (t >> 1) & 1, ctl);
+    for (int t = (issued > kBwdStages ? issued - kBwdStages : 0); t < issued; ++t)
+      mbar_drain(full(t % kBwdStages), (t / kBwdStages) & 1, ctl);
   } else if (warp == 1) {
     // ---------------- MMA issuer (converged warp, one elected lane issues) ----------------
     constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A in TMEM)
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A K-major)
     constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);    // dQ (A = dS, MN-major)
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // stage stride, descriptor units
     constexpr uint32_t kRowStep = (16 * L::kRowBytes) >> 4;  // 16 rows of an MN-major tile
-    // Descriptors are built once. K-major operands (Q, K, V, dO as K-major) advance
-    // +32 bytes (+2) per 16-element K step; MN-major ones advance 16 rows.
+    // Descriptors are built once. K-major operands advance +32 bytes (+2) per
+    // 16-element K step; MN-major ones advance 16 rows.
     const uint64_t kK_k = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kV_k = smem_desc(sV, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kQ_k = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle);
@@ -326,202 +353,262 @@ __global__ void __maxnreg__(XATTN_BWD_MAXNREG)
     const uint64_t kdO_mn = smem_desc(sdO, 8192, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kdS_mn = smem_desc(sdS, 16384, 1024, kSwizzle128);
-    auto issue_kmajor = [&](uint32_t d, uint64_t a, uint64_t bdesc) {
+    const uint64_t kdS_k = smem_desc(sdS, 16, 1024, kSwizzle128);
+    const uint64_t kAuxS = smem_desc(sAuxA, 16, 256, kSwizzle32);
+    const uint64_t kAuxD = smem_desc(sAuxA + L::kAuxTileBytes, 16, 256, kSwizzle32);
+    const uint64_t kAuxQ = smem_desc(sAuxB, 16, 256, kSwizzle32);
+    constexpr uint32_t kAuxStageDesc = L::kAuxTileBytes >> 4;
+    // S^T = K Q^T - LSE/scale, dP^T = V dO^T - D: the head-dim K steps, then one
+    // auxiliary K step that adds the per-query term (key-side ones x query-side terms).
+    auto issue_t = [&](uint32_t d, uint64_t a, uint64_t bdesc, bool with_qk, uint64_t aux_a, int stage) {
+      if (with_qk) {
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a + 2 * kk, bdesc + 2 * kk, idesc_t, kk > 0);
-    };
-    auto issue_acc = [&](uint32_t d, uint64_t bdesc, bool first) {
-#pragma unroll
-      for (int kk = 0; kk < kTileRows / 16; ++kk)
-        mma_ts_elect(d, tP + kk * 8, bdesc + kk * kRowStep, idesc_acc, (!first || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a + 2 * kk, bdesc + 2 * kk, idesc_t, kk > 0);
+      }
+      mma_ss_elect(d, aux_a, kAuxQ + stage * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
     };
     bool ok = warp_wait(kv_full, 0, ctl) && warp_wait(full(0), 0, ctl);
     if (ok) {
       tc_fence_after();
-      issue_kmajor(tS, kK_k, kQ_k);
+      issue_t(tS, kK_k, kQ_k, qk, kAuxS, 0);
       mma_commit_elect(s_full);
-      issue_kmajor(tdP, kV_k, kdO_k);
+      issue_t(tdP, kV_k, kdO_k, true, kAuxD, 0);
       mma_commit_elect(dp_full);
     }
-    for (int t = 0; ok && t < T; ++t) {
-      const int s = t & 1;
+    for (int t = 0, s = 0; ok && t < T; ++t) {
+      const int s1 = (s + 1 == kBwdStages) ? 0 : s + 1;
       const bool more = t + 1 < T;
-      if (!warp_wait(p_full, t & 1, ctl)) break;
-      tc_fence_after();
-      issue_acc(tdV, kdO_mn + s * kStageDesc, t == 0);                       // dV += P^T dO
-      mma_commit_elect(dv_done);
+      const uint32_t ph = t & 1;
       if (more) {
-        if (!warp_wait(full(s ^ 1), ((t + 1) >> 1) & 1, ctl)) break;
+        // S^T(t+1) as soon as the P warps have read S^T(t).
+        if (!warp_wait(full(s1), ((t + 1) / kBwdStages) & 1, ctl)) break;
+        if (!warp_wait(s_free, ph, ctl)) break;
         tc_fence_after();
-        issue_kmajor(tS, kK_k, kQ_k + (s ^ 1) * kStageDesc);                 // S^T(t+1)
+        issue_t(tS, kK_k, kQ_k + s1 * kStageDesc, qk, kAuxS, s1);
         mma_commit_elect(s_full);
       }
-      if (!warp_wait(ds_full, t & 1, ctl)) break;
+      if (!warp_wait(p_full, ph, ctl)) break;
       tc_fence_after();
-      issue_acc(tdK, kQ_mn + s * kStageDesc, t == 0);                        // dK += dS^T Q
+#pragma unroll
+      for (int kk = 0; kk < kTileRows / 16; ++kk)                            // dV += P^T dO
+        mma_ts_elect(tdV, tP + kk * 8, kdO_mn + s * kStageDesc + kk * kRowStep, idesc_acc,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit_elect(dv_done);
+      if (more) {
+        // dP^T(t+1) as soon as the dS warps have read dP^T(t).
+        if (!warp_wait(dp_free, ph, ctl)) break;
+        tc_fence_after();
+        issue_t(tdP, kV_k, kdO_k + s1 * kStageDesc, true, kAuxD, s1);
+        mma_commit_elect(dp_full);
+      }
+      if (!warp_wait(ds_full, ph, ctl)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kTileRows / 16; ++kk)                            // dK += dS^T Q
+        mma_ss_elect(tdK, kdS_k + (kk >> 2) * 1024 + (kk & 3) * 2,
+                     kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
       mma_commit_elect(empty(s));
-      mma_commit_elect(dk_done);
-      if (!warp_wait(dq_empty, (t & 1) ^ 1, ctl)) break;
+      if (t > 0 && !warp_wait(dq_empty, ph ^ 1, ctl)) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kTileRows / 16; ++kk)                            // dQ = dS K
         mma_ss_elect(tdQ, kdS_mn + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
       mma_commit_elect(dq_full);
-      if (more) {
-        issue_kmajor(tdP, kV_k, kdO_k + (s ^ 1) * kStageDesc);               // dP^T(t+1)
-        mma_commit_elect(dp_full);
-      }
+      s = s1;
     }
     mma_commit_elect(acc_done);
     mbar_drain(acc_done, 0, ctl);
   } else if (warp == 2) {
     // ---------------- dQ reducer ----------------
     for (int k = 0; k < T; ++k) {
-      const int buf = k & 1;
-      if (!warp_wait(dqs_full(buf), (k >> 1) & 1, ctl)) break;
+      if (!warp_wait(dqs_full, k & 1, ctl)) break;
       if (lane == 0) {
         const int h = kvh * group + k / per_head, m = n + k % per_head;
-        const uint32_t src = smem_u32(sdQs_ptr + buf * 2 * L::kDqHalfBytes);
+        const uint32_t src = smem_u32(sdQs_ptr);
         tma_reduce_add_4d(&mdq, src, 0, h, m * kTileRows, b);
         tma_reduce_add_4d(&mdq, src + L::kDqHalfBytes, HD / 2, h, m * kTileRows, b);
         bulk_commit_group();
         bulk_wait_read_all();          // the staging buffer may be rewritten
-        mbar_arrive(dqs_empty(buf));
+        mbar_arrive(dqs_empty);
       }
       __syncwarp();
     }
     if (lane == 0) bulk_wait_all();    // every reduce-add has landed before the CTA exits
     __syncwarp();
-  } else if (warp >= 4) {
-    // ---------------- P^T and dS^T: one thread per key row, C query columns ----------------
-    constexpr int C = 128 / kBwdGroups;        // query columns per thread
-    constexpr int kDq = HD / kBwdGroups;       // dQ head-dim columns drained per thread
-    const int g = (warp - 4) >> 2;             // column group
+  } else if (warp >= 4 && warp < 8) {
+    // ---------------- P^T: one thread per key row j, 4 chunks of 32 query columns ----------------
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int col_f32 = C * g;
-    const uint32_t col_bf16 = static_cast<uint32_t>(C / 2 * g);
-    // dQ(k) from TMEM (query row j of its tile, head-dim columns [g*kDq, (g+1)*kDq)) into
-    // staging buffer k & 1, swizzled like the reduce's tensor-map box (two halves of HD/2
-    // floats per row); warp 2 then adds it to global memory.
-    auto drain_dq = [&](int k) -> bool {
-      const int buf = k & 1;
-      uint32_t v[kDq];
-      if constexpr (kDq == 32) tmem_ld_x32(tdQ + lane_off + kDq * g, v);
-      else if constexpr (kDq == 16) tmem_ld_x16(tdQ + lane_off + kDq * g, v);
-      else tmem_ld_x8(tdQ + lane_off + kDq * g, v);
-      tmem_wait_ld();
-      reg_fence<kDq>(v);
-      tc_fence_before();
-      mbar_arrive(dq_empty);
-      if (!warp_wait(dqs_empty(buf), ((k >> 1) & 1) ^ 1, ctl)) return false;
-      const int first = kDq * g;                      // first head-dim column
-      const int half = first / (HD / 2);
-      const int chunk0 = (first % (HD / 2)) / 4;      // 16-byte chunk within the row
-      uint8_t *row = sdQs_ptr + (buf * 2 + half) * L::kDqHalfBytes + j * L::kDqRowBytes;
-#pragma unroll
-      for (int c = 0; c < kDq / 4; ++c) {
-        const int ch = chunk0 + c;
-        const int sw = (HD == 64) ? (ch ^ (j & 7)) : (ch ^ ((j >> 1) & 3));
-        *reinterpret_cast<uint4 *>(row + (sw << 4)) =
-            make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(dqs_full(buf));
-      return true;
-    };
-    auto ld_cols = [&](uint32_t taddr, uint32_t *r) {
-#pragma unroll
-      for (int c = 0; c < C; c += 32) tmem_ld_x32(taddr + c, r + c);
-      tmem_wait_ld();
-      reg_fence<C>(r);
-    };
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int m = n + t % per_head;
-      const int s = t & 1;
       const bool diag = (m == n);
-      // Phase 1: P^T = exp2(S^T scale log2e - LSE2), masked above the diagonal.
       if (!warp_wait(s_full, t & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r[C];
-      ld_cols(tS + lane_off + col_f32, r);
-      const float4 *nlse4 = reinterpret_cast<const float4 *>(sLSE + s * 128 + col_f32);
-      uint32_t pk[C / 2];
+      uint32_t ra[32], rb[32];
+      tmem_ld_x32(tS + lane_off, ra);
+      tmem_wait_ld();
+      reg_fence<32>(ra);
 #pragma unroll
-      for (int q4 = 0; q4 < C / 4; ++q4) {
-        const float4 nl = nlse4[q4];
-        float x0, x1, x2, x3;
-        ffma2(x0, x1, __uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]), scale_log2,
-              scale_log2, nl.x, nl.y);
-        ffma2(x2, x3, __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]), scale_log2,
-              scale_log2, nl.z, nl.w);
-        float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-        if (diag) {
-          const int i = col_f32 + 4 * q4;
-          if (i + 0 < j) p0 = 0.f;
-          if (i + 1 < j) p1 = 0.f;
-          if (i + 2 < j) p2 = 0.f;
-          if (i + 3 < j) p3 = 0.f;
+      for (int c = 0; c < 4; ++c) {
+        uint32_t *cur = (c & 1) ? rb : ra;
+        uint32_t *nxt = (c & 1) ? ra : rb;
+        if (c < 3) tmem_ld_x32(tS + lane_off + 32 * (c + 1), nxt);    // next chunk in flight
+        uint32_t pk[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          float x0, x1, x2, x3;
+          fmul2(x0, x1, __uint_as_float(cur[4 * q4]), __uint_as_float(cur[4 * q4 + 1]), scale_log2, scale_log2);
+          fmul2(x2, x3, __uint_as_float(cur[4 * q4 + 2]), __uint_as_float(cur[4 * q4 + 3]), scale_log2, scale_log2);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+          if (diag) {
+            const int i = 32 * c + 4 * q4;
+            if (i + 0 < j) p0 = 0.f;
+            if (i + 1 < j) p1 = 0.f;
+            if (i + 2 < j) p2 = 0.f;
+            if (i + 3 < j) p3 = 0.f;
+          }
+          pk[2 * q4] = pack_bf16x2(p0, p1);
+          pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
         }
-        pk[2 * q4] = pack_bf16x2(p0, p1);
-        pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
+        if (c == 0 && t > 0) {
+          // P^T(t-1) must have been read by the dS warps and by dV(t-1).
+          if (!warp_wait(p_free, (t - 1) & 1, ctl) || !warp_wait(dv_done, (t - 1) & 1, ctl)) {
+            tmem_wait_ld();    // the load of chunk 1 is still in flight
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st_x16(tP + lane_off + 16 * c, pk);
+        if (c < 3) {
+          tmem_wait_ld();
+          reg_fence<32>(nxt);
+        }
+        if (c == 2) {          // the last chunk of S^T(t) is in registers
+          tc_fence_before();
+          mbar_arrive(s_free);
+        }
       }
-      // The P^T slot still holds dS^T(t-1) until dK(t-1) has read it.
-      if (t > 0 && !warp_wait(dk_done, (t - 1) & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < C / 2; c += 16) tmem_st_x16(tP + lane_off + col_bf16 + c, pk + c);
+      if (!ok) break;
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full);
-
-      // Phase 2: dS^T = scale P^T (dP^T - D).
-      if (!warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
+    }
+    // Epilogue: dV rows (bf16).
+    if (ok && warp_wait(acc_done, 0, ctl)) {
       tc_fence_after();
-      ld_cols(tdP + lane_off + col_f32, r);
-      // dQ(t-1) must be done reading the shared-memory copy of dS (its result is drained
-      // here), and dV(t) must be done reading P^T before dS^T replaces it in TMEM.
-      if (t > 0) {
-        if (!warp_wait(dq_full, (t - 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
-        if (!drain_dq(t - 1)) { ok = false; break; }
-      }
-      if (!warp_wait(dv_done, t & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      const float4 *nd4 = reinterpret_cast<const float4 *>(sD + s * 128 + col_f32);
+      const int jg = n * kTileRows + j;
+      const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
 #pragma unroll
-      for (int c32 = 0; c32 < C; c32 += 32) {
+      for (int c = 0; c < HD; c += 16) {
+        uint32_t v[16];
+        tmem_ld_x16(tdV + lane_off + c, v);
+        tmem_wait_ld();
+        reg_fence<16>(v);
+        if (jg < S) {
+          uint4 *dst = reinterpret_cast<uint4 *>(dv + row_off + c);
+#pragma unroll
+          for (int e = 0; e < 2; ++e)
+            dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]), __uint_as_float(v[8 * e + 1])),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3])),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5])),
+                                pack_bf16x2(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7])));
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ---------------- dS^T and the dQ drain: one thread per key row j ----------------
+    const int quarter = warp & 3;
+    const int j = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    // dQ(k) from TMEM (query row j of its tile) into the staging buffer, swizzled like
+    // the reduce's tensor-map box (two halves of HD/2 floats per row); warp 2 then adds
+    // it to global memory. The caller has waited for dq_full(k).
+    auto drain_dq = [&](int k) -> bool {
+      uint32_t v[HD];
+#pragma unroll
+      for (int c = 0; c < HD; c += 32) tmem_ld_x32(tdQ + lane_off + c, v + c);
+      tmem_wait_ld();
+      reg_fence<HD>(v);
+      tc_fence_before();
+      mbar_arrive(dq_empty);
+      if (!warp_wait(dqs_empty, (k & 1) ^ 1, ctl)) return false;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint8_t *row = sdQs_ptr + half * L::kDqHalfBytes + j * L::kDqRowBytes;
+#pragma unroll
+        for (int ch = 0; ch < HD / 8; ++ch) {
+          const int sw = (HD == 64) ? (ch ^ (j & 7)) : (ch ^ ((j >> 1) & 3));
+          const uint32_t *x = v + half * (HD / 2) + 4 * ch;
+          *reinterpret_cast<uint4 *>(row + (sw << 4)) = make_uint4(x[0], x[1], x[2], x[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(dqs_full);
+      return true;
+    };
+    bool ok = true;
+    for (int t = 0; t < T; ++t) {
+      if (!warp_wait(p_full, t & 1, ctl) || !warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      // 4 chunks of 32 query columns: P^T bf16 (16 TMEM columns) and dP^T (32 columns).
+      uint32_t pa[16], da[32], pb[16], db[32];
+      tmem_ld_x16(tP + lane_off, pa);
+      tmem_ld_x32(tdP + lane_off, da);
+      tmem_wait_ld();
+      reg_fence<16>(pa);
+      reg_fence<32>(da);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t *pc = (c & 1) ? pb : pa, *dc = (c & 1) ? db : da;
+        uint32_t *pn = (c & 1) ? pa : pb, *dn = (c & 1) ? da : db;
+        if (c < 3) {
+          tmem_ld_x16(tP + lane_off + 16 * (c + 1), pn);
+          tmem_ld_x32(tdP + lane_off + 32 * (c + 1), dn);
+        }
+        if (c == 0 && t > 0) {
+          // dK(t-1) and dQ(t-1) have finished reading the shared-memory dS tile.
+          if (!warp_wait(dq_full, (t - 1) & 1, ctl)) {
+            tmem_wait_ld();    // the loads of chunk 1 are still in flight
+            ok = false;
+            break;
+          }
+        }
         uint32_t dsk[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
-          const int c = c32 + 4 * q4;
-          const float4 nd = nd4[c / 4];
-          const uint32_t pa = pk[c / 2], pb = pk[c / 2 + 1];
+          const uint32_t p01 = pc[2 * q4], p23 = pc[2 * q4 + 1];
           float t0, t1, t2, t3;
-          fadd2(t0, t1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), nd.x, nd.y);
-          fadd2(t2, t3, __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]), nd.z, nd.w);
-          fmul2(t0, t1, t0, t1, bf16lo_to_f32(pa), bf16hi_to_f32(pa));
-          fmul2(t2, t3, t2, t3, bf16lo_to_f32(pb), bf16hi_to_f32(pb));
-          fmul2(t0, t1, t0, t1, scale, scale);
-          fmul2(t2, t3, t2, t3, scale, scale);
+          fmul2(t0, t1, __uint_as_float(dc[4 * q4]), __uint_as_float(dc[4 * q4 + 1]), bf16lo_to_f32(p01),
+                bf16hi_to_f32(p01));
+          fmul2(t2, t3, __uint_as_float(dc[4 * q4 + 2]), __uint_as_float(dc[4 * q4 + 3]), bf16lo_to_f32(p23),
+                bf16hi_to_f32(p23));
           dsk[2 * q4] = pack_bf16x2(t0, t1);
           dsk[2 * q4 + 1] = pack_bf16x2(t2, t3);
         }
-        tmem_st_x16(tP + lane_off + col_bf16 + c32 / 2, dsk);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, col_f32 + c32 + 8 * e)) =
+          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, 32 * c + 8 * e)) =
               make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
+        if (c < 3) {
+          tmem_wait_ld();
+          reg_fence<16>(pn);
+          reg_fence<32>(dn);
+        }
+        if (c == 2) {          // P^T(t) and dP^T(t) are all in registers
+          tc_fence_before();
+          mbar_arrive(p_free);
+          mbar_arrive(dp_free);
+        }
       }
-      tmem_wait_st();
+      if (!ok) break;
       fence_proxy_async_smem();
-      tc_fence_before();
       mbar_arrive(ds_full);
+      if (t > 0 && !drain_dq(t - 1)) { ok = false; break; }
     }
-    // Epilogue: drain the last dQ; then the groups store the dV and dK rows, each group a
-    // contiguous slice of [dV | dK] (dK already carries the scale).
+    // Epilogue: the last dQ, then the dK rows (bf16, times the softmax scale).
     if (ok && warp_wait(dq_full, (T - 1) & 1, ctl)) {
       tc_fence_after();
       ok = drain_dq(T - 1);
@@ -530,28 +617,23 @@ __global__ void __maxnreg__(XATTN_BWD_MAXNREG)
     }
     if (ok && warp_wait(acc_done, 0, ctl)) {
       tc_fence_after();
-      constexpr int kPer = 2 * HD / kBwdGroups;   // output columns per group
-      const int first = kPer * g;                 // in the concatenation [dV | dK]
-      const bool is_dk = first >= HD;
-      const int c0 = first % HD;
       const int jg = n * kTileRows + j;
       const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
-      const uint32_t tsrc = (is_dk ? tdK : tdV) + c0;
-      __nv_bfloat16 *dst_row = (is_dk ? dk : dv) + row_off + c0;
 #pragma unroll
-      for (int c = 0; c < kPer; c += 16) {
+      for (int c = 0; c < HD; c += 16) {
         uint32_t v[16];
-        tmem_ld_x16(tsrc + lane_off + c, v);
+        tmem_ld_x16(tdK + lane_off + c, v);
         tmem_wait_ld();
         reg_fence<16>(v);
         if (jg < S) {
-          uint4 *dst = reinterpret_cast<uint4 *>(dst_row + c);
+          float f[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]) * scale;
+          uint4 *dst = reinterpret_cast<uint4 *>(dk + row_off + c);
 #pragma unroll
           for (int e = 0; e < 2; ++e)
-            dst[e] = make_uint4(pack_bf16x2(__uint_as_float(v[8 * e]), __uint_as_float(v[8 * e + 1])),
-                                pack_bf16x2(__uint_as_float(v[8 * e + 2]), __uint_as_float(v[8 * e + 3])),
-                                pack_bf16x2(__uint_as_float(v[8 * e + 4]), __uint_as_float(v[8 * e + 5])),
-                                pack_bf16x2(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7])));
+            dst[e] = make_uint4(pack_bf16x2(f[8 * e], f[8 * e + 1]), pack_bf16x2(f[8 * e + 2], f[8 * e + 3]),
+                                pack_bf16x2(f[8 * e + 4], f[8 * e + 5]), pack_bf16x2(f[8 * e + 6], f[8 * e + 7]));
         }
       }
     }
@@ -567,7 +649,7 @@ __global__ void __maxnreg__(XATTN_BWD_MAXNREG)
 
 template <int HD>
 cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mdo, const CUtensorMap &mdq, const BwdWorkspace &ws, __nv_bfloat16 *dk,
+                           const CUtensorMap &mdo, const CUtensorMap &maux, const CUtensorMap &mdq, __nv_bfloat16 *dk,
                            __nv_bfloat16 *dv, int B, int S, int nh, int nkv, float scale,
                            int *status, uint64_t timeout_ns, cudaStream_t stream) {
   using L = BwdLayout<HD>;
@@ -577,25 +659,28 @@ cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const C
   const int num_n = (S + kTileRows - 1) / kTileRows;
   const unsigned grid = static_cast<unsigned>(B) * nkv * num_n;
   attn_bwd_main_kernel<HD><<<grid, kBwdThreads, L::kDynBytes, stream>>>(
-      mq, mk, mv, mdo, mdq, ws.D, ws.lse2, dk, dv, B, S, nh, nkv, scale, scale * kLog2e,
-      status, timeout_ns);
+      mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dO,
-                                  const float *lse, int B, int S, int nh, int hd,
+                                  const float *lse, int B, int S, int nh, int hd, float scale,
                                   const BwdWorkspace &ws, cudaStream_t stream) {
+  // -LSE/scale, or -LSE log2 e when scale == 0 (then the main kernel's S^T is the
+  // auxiliary term alone and is used unscaled).
+  const float lse_mult = (scale == 0.f) ? kLog2e : 1.0f / scale;
+  uint4 *aux = reinterpret_cast<uint4 *>(ws.aux);
   const long long n_rows = static_cast<long long>(B) * S * nh;
   const long long n_pad = static_cast<long long>(B) * nh * (padded_rows(S) - S);
   const int lanes = hd / 8;
   const long long threads = (n_rows + n_pad) * lanes;
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
   if (hd == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dO, lse, ws.D, ws.lse2, ws.dqacc, B, S, nh);
+    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.dqacc, B, S, nh, lse_mult);
   else if (hd == 32)
-    bwd_preprocess_kernel<32><<<grid, 256, 0, stream>>>(o, dO, lse, ws.D, ws.lse2, ws.dqacc, B, S, nh);
+    bwd_preprocess_kernel<32><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.dqacc, B, S, nh, lse_mult);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -603,22 +688,23 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *d
 
 cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
                                  const CUtensorMap &mv, const CUtensorMap &mdo,
-                                 const CUtensorMap &mdq, const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
+                                 const CUtensorMap &maux, const CUtensorMap &mdq,
+                                 const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
                                  int B, int S, int nh, int nkv, int hd, float scale, int *status,
                                  uint64_t timeout_ns, cudaStream_t stream) {
   if (hd == 64)
-    return launch_main_hd<64>(mq, mk, mv, mdo, mdq, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return launch_main_hd<64>(mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
   if (hd == 32)
-    return launch_main_hd<32>(mq, mk, mv, mdo, mdq, ws, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return launch_main_hd<32>(mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, size_t n_elems,
-                              cudaStream_t stream) {
+                              float scale, cudaStream_t stream) {
   const size_t n8 = n_elems / 8;
   const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
   if (grid == 0) return cudaSuccess;
-  dq_convert_kernel<<<grid, 256, 0, stream>>>(dqacc, dq, n8);
+  dq_convert_kernel<<<grid, 256, 0, stream>>>(dqacc, dq, n8, scale);
   return cudaGetLastError();
 }
 

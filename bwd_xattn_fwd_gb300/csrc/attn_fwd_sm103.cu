@@ -58,7 +58,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int HD>
+// kNegScale: scale < 0, so the row maximum of the scaled scores is the scaled minimum of
+// the raw ones.
+template <int HD, bool kNegScale>
 __global__ void __maxnreg__(168)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                     const __grid_constant__ CUtensorMap mv, __nv_bfloat16 *__restrict__ o,
@@ -229,9 +231,10 @@ __global__ void __maxnreg__(168)
       if (!warp_wait(s_full(x), n & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const bool diag = (n == mX);
-      // Pass 1: row maximum of the raw scores, 64 columns at a time (scale > 0, so the
-      // scaled maximum is the image of the raw one).
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // Pass 1: the row maximum of the scaled scores, 64 columns at a time: the scaled
+      // maximum of the raw scores (scale >= 0) or their scaled minimum (scale < 0).
+      constexpr float kFill = kNegScale ? INFINITY : -INFINITY;
+      float mx4[4] = {kFill, kFill, kFill, kFill};
 #pragma unroll 1
       for (int c64 = 0; c64 < 128; c64 += 64) {
         uint32_t r[64];
@@ -242,13 +245,17 @@ __global__ void __maxnreg__(168)
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
-            if (c64 + c > row) r[c] = __float_as_uint(-INFINITY);
+            if (c64 + c > row) r[c] = __float_as_uint(kFill);
         }
 #pragma unroll
-        for (int c = 0; c < 64; c += 2)
-          mx4[(c >> 1) & 3] = fmax3(mx4[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+        for (int c = 0; c < 64; c += 2) {
+          float &a = mx4[(c >> 1) & 3];
+          a = kNegScale ? fmin3(a, __uint_as_float(r[c]), __uint_as_float(r[c + 1]))
+                        : fmax3(a, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+        }
       }
-      const float mx = fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3])) * scale_log2;
+      const float mx = (kNegScale ? fmin3(mx4[0], mx4[1], fminf(mx4[2], mx4[3]))
+                                  : fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]))) * scale_log2;
       // Conditional rescaling: keep the stale max unless some row of the warp grew by
       // more than 2^8; the decision is per warp because TMEM loads/stores are collective.
       const float mnew = fmaxf(mrow, mx);
@@ -275,6 +282,16 @@ __global__ void __maxnreg__(168)
           tc_fence_before();
           mbar_arrive(s_free(x));
         }
+        // Exponents in place, then the causal mask on them (-inf -> exact zeros for any
+        // scale, 0 included), then the exponentials.
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
+                scale_log2, neg_m, neg_m);
+          r[2 * e] = __float_as_uint(x0);
+          r[2 * e + 1] = __float_as_uint(x1);
+        }
         if (diag) {
 #pragma unroll
           for (int c = 0; c < 64; ++c)
@@ -283,10 +300,7 @@ __global__ void __maxnreg__(168)
         uint32_t pk[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
-          float x0, x1;
-          ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
-                scale_log2, neg_m, neg_m);
-          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const float p0 = ex2_approx(__uint_as_float(r[2 * e])), p1 = ex2_approx(__uint_as_float(r[2 * e + 1]));
           const int a = (e & 1) * 2;
           fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
           pk[e] = pack_bf16x2(p0, p1);
@@ -346,19 +360,28 @@ __global__ void __maxnreg__(168)
   }
 }
 
-template <int HD>
-cudaError_t launch_fwd_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                          __nv_bfloat16 *o, float *lse, int B, int S, int nh, int nkv, float scale,
-                          int *status, uint64_t timeout_ns, cudaStream_t stream) {
+template <int HD, bool kNegScale>
+cudaError_t launch_fwd_sign(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                            __nv_bfloat16 *o, float *lse, int B, int S, int nh, int nkv, float scale,
+                            int *status, uint64_t timeout_ns, cudaStream_t stream) {
   using L = FwdLayout<HD>;
-  cudaError_t err = cudaFuncSetAttribute(attn_fwd_kernel<HD>,
+  cudaError_t err = cudaFuncSetAttribute(attn_fwd_kernel<HD, kNegScale>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
   if (err != cudaSuccess) return err;
   const int num_m = (S + kTileRows - 1) / kTileRows;
   const unsigned grid = static_cast<unsigned>(B) * nh * ((num_m + 1) / 2);
-  attn_fwd_kernel<HD><<<grid, kFwdThreads, L::kDynBytes, stream>>>(
+  attn_fwd_kernel<HD, kNegScale><<<grid, kFwdThreads, L::kDynBytes, stream>>>(
       mq, mk, mv, o, lse, B, S, nh, nkv, scale * kLog2e, status, timeout_ns);
   return cudaGetLastError();
+}
+
+template <int HD>
+cudaError_t launch_fwd_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                          __nv_bfloat16 *o, float *lse, int B, int S, int nh, int nkv, float scale,
+                          int *status, uint64_t timeout_ns, cudaStream_t stream) {
+  if (scale < 0.f)
+    return launch_fwd_sign<HD, true>(mq, mk, mv, o, lse, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  return launch_fwd_sign<HD, false>(mq, mk, mv, o, lse, B, S, nh, nkv, scale, status, timeout_ns, stream);
 }
 
 }  // namespace

@@ -40,6 +40,12 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed fp32 pair arithmetic (.f32x2): one instruction for two lanes of work.
 __device__ __forceinline__ void ffma2(float &d0, float &d1, float a0, float a1, float b0, float b1,
                                       float c0, float c1) {
@@ -228,6 +234,7 @@ __device__ __forceinline__ void tc_fence_after() {
 // (2 = 128-byte, 4 = 64-byte, 6 = 32-byte, 0 = none).
 constexpr uint32_t kSwizzle128 = 2;
 constexpr uint32_t kSwizzle64 = 4;
+constexpr uint32_t kSwizzle32 = 6;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint32_t swizzle) {

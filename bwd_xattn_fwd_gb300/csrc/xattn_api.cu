@@ -102,6 +102,22 @@ xattn_status make_map_dq(CUtensorMap *map, float *ptr, int B, int S, int nh, int
   return r == CUDA_SUCCESS ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
+// 4-D map over the backward's [B, nh, S_pad, 16] bf16 auxiliary rows; box = 16 columns
+// (32 bytes, 32-byte swizzle) by 128 rows.
+xattn_status make_map_aux(CUtensorMap *map, void *ptr, int B, int S, int nh) {
+  const cuuint64_t S_pad = static_cast<cuuint64_t>(padded_rows(S));
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kAuxCols), S_pad, static_cast<cuuint64_t>(nh),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t row = kAuxCols * 2;
+  const cuuint64_t strides[3] = {row, row * S_pad, row * S_pad * nh};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(kAuxCols), static_cast<cuuint32_t>(kTileRows), 1, 1};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, ptr, dims, strides, box, elem,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? XATTN_OK : XATTN_ERR_CUDA;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 xattn_status check_shape(int B, int S, int nh, int nkv, int hd, float scale) {
@@ -112,6 +128,14 @@ xattn_status check_shape(int B, int S, int nh, int nkv, int hd, float scale) {
     return XATTN_ERR_BAD_SHAPE;
   if (nh % nkv != 0) return XATTN_ERR_GROUP;
   if (!std::isfinite(scale)) return XATTN_ERR_BAD_SCALE;
+  return XATTN_OK;
+}
+
+// The bf16 backward folds -LSE/scale into a tensor-core operand; it takes scale == 0
+// exactly, and any |scale| >= 2^-64 (so that LSE/scale stays far from overflow).
+xattn_status check_bwd_scale(float scale) {
+  if (!std::isfinite(scale)) return XATTN_ERR_BAD_SCALE;
+  if (scale != 0.f && std::fabs(scale) < 0x1p-64f) return XATTN_ERR_BAD_SCALE;
   return XATTN_OK;
 }
 
@@ -173,10 +197,11 @@ size_t xattn_bwd_workspace_bytes(int B, int S, int nh, int hd) {
 }
 
 xattn_status xattn_bwd_preprocess(const void *o, const void *dO, const float *lse, int B, int S,
-                                  int nh, int hd, void *workspace, size_t workspace_bytes,
-                                  void *stream) {
+                                  int nh, int hd, float scale, void *workspace,
+                                  size_t workspace_bytes, void *stream) {
   if (!o || !dO || !lse) return XATTN_ERR_NULL_PTR;
-  XATTN_TRY(check_shape(B, S, nh, nh, hd, 1.0f));
+  XATTN_TRY(check_shape(B, S, nh, nh, hd, scale));
+  XATTN_TRY(check_bwd_scale(scale));
   XATTN_TRY(check_bf16(hd));
   if (!aligned16(o) || !aligned16(dO)) return XATTN_ERR_MISALIGNED;
   XATTN_TRY(check_workspace(workspace, workspace_bytes, B, S, nh, hd));
@@ -185,7 +210,7 @@ xattn_status xattn_bwd_preprocess(const void *o, const void *dO, const float *ls
   const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
   return cuda_status(launch_bwd_preprocess(static_cast<const __nv_bfloat16 *>(o),
                                            static_cast<const __nv_bfloat16 *>(dO), lse, B, S, nh, hd,
-                                           ws, static_cast<cudaStream_t>(stream)));
+                                           scale, ws, static_cast<cudaStream_t>(stream)));
 }
 
 xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const void *dO, int B,
@@ -193,6 +218,7 @@ xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const v
                             void *workspace, size_t workspace_bytes, void *stream) {
   if (!q || !k || !v || !dO || !dk || !dv) return XATTN_ERR_NULL_PTR;
   XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  XATTN_TRY(check_bwd_scale(scale));
   XATTN_TRY(check_bf16(hd));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dO) || !aligned16(dk) ||
       !aligned16(dv))
@@ -206,18 +232,19 @@ xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const v
   XATTN_TRY(make_map(&mv, v, B, S, nkv, hd));
   XATTN_TRY(make_map(&mdo, dO, B, S, nh, hd));
   const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
-  CUtensorMap mdq;
+  CUtensorMap maux, mdq;
+  XATTN_TRY(make_map_aux(&maux, ws.aux, B, S, nh));
   XATTN_TRY(make_map_dq(&mdq, ws.dqacc, B, S, nh, hd));
-  return cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, mdq, ws, static_cast<__nv_bfloat16 *>(dk),
+  return cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, maux, mdq, ws, static_cast<__nv_bfloat16 *>(dk),
                                           static_cast<__nv_bfloat16 *>(dv), B, S, nh, nkv, hd, scale,
                                           dev->status, wait_limit_ns(),
                                           static_cast<cudaStream_t>(stream)));
 }
 
-xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, void *dq, void *workspace,
-                                  size_t workspace_bytes, void *stream) {
+xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, float scale, void *dq,
+                                  void *workspace, size_t workspace_bytes, void *stream) {
   if (!dq) return XATTN_ERR_NULL_PTR;
-  XATTN_TRY(check_shape(B, S, nh, nh, hd, 1.0f));
+  XATTN_TRY(check_shape(B, S, nh, nh, hd, scale));
   XATTN_TRY(check_bf16(hd));
   if (!aligned16(dq)) return XATTN_ERR_MISALIGNED;
   XATTN_TRY(check_workspace(workspace, workspace_bytes, B, S, nh, hd));
@@ -225,7 +252,7 @@ xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, void *dq, void *
   XATTN_TRY(bf16_device(&dev));
   const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
   return cuda_status(launch_dq_convert(ws.dqacc, static_cast<__nv_bfloat16 *>(dq),
-                                       static_cast<size_t>(B) * S * nh * hd,
+                                       static_cast<size_t>(B) * S * nh * hd, scale,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -234,6 +261,7 @@ xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *
                        void *dk, void *dv, void *stream) {
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return XATTN_ERR_NULL_PTR;
   XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  XATTN_TRY(check_bwd_scale(scale));
   XATTN_TRY(check_bf16(hd));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
@@ -244,9 +272,9 @@ xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *
   const size_t bytes = bwd_workspace_bytes(B, S, nh, hd);
   void *ws = nullptr;
   if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return XATTN_ERR_CUDA;
-  xattn_status r = xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, ws, bytes, stream);
+  xattn_status r = xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, scale, ws, bytes, stream);
   if (r == XATTN_OK) r = xattn_bwd_main(q, k, v, dO, B, S, nh, nkv, hd, scale, dk, dv, ws, bytes, stream);
-  if (r == XATTN_OK) r = xattn_bwd_dq_convert(B, S, nh, hd, dq, ws, bytes, stream);
+  if (r == XATTN_OK) r = xattn_bwd_dq_convert(B, S, nh, hd, scale, dq, ws, bytes, stream);
   const cudaError_t fe = cudaFreeAsync(ws, st);
   if (r == XATTN_OK && fe != cudaSuccess) r = XATTN_ERR_CUDA;
   return r;

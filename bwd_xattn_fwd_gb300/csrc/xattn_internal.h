@@ -16,10 +16,16 @@ constexpr float kLn2 = 0.6931471805599453f;
 // Rows of the per-(batch, head) workspace vectors, padded to whole tiles.
 __host__ __device__ inline int padded_rows(int S) { return (S + kTileRows - 1) / kTileRows * kTileRows; }
 
+// Row i of the backward's per-(batch, head) auxiliary operand: 16 bf16 values (one
+// tensor-core K step). Columns 0-2 hold -LSE_i / scale and columns 3-5 hold -D_i, each
+// as a sum of three bf16 terms (hi + mid + lo, about 24 significant bits); the rest are
+// zero, and pad rows (S <= i < S_pad) are all zero. With scale == 0 columns 0-2 hold
+// -LSE_i log2(e) instead (the products then skip Q K^T).
+constexpr int kAuxCols = 16;
+
 struct BwdWorkspace {
-  float *D;      // [B, nh, S_pad]  -D_i = -(dO_i . O_i) ; zero in pad rows
-  float *lse2;   // [B, nh, S_pad]  -LSE_i * log2(e) ; -inf in pad rows
-  float *dqacc;  // [B, S, nh, hd]  fp32 dQ accumulator
+  __nv_bfloat16 *aux;  // [B, nh, S_pad, kAuxCols]
+  float *dqacc;        // [B, S, nh, hd]  fp32 dQ accumulator (dS K, without the scale)
 };
 
 size_t bwd_workspace_bytes(int B, int S, int nh, int hd);
@@ -31,20 +37,21 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &mq, const CUtensorMap &mk, const 
                             float scale, int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dO,
-                                  const float *lse, int B, int S, int nh, int hd,
+                                  const float *lse, int B, int S, int nh, int hd, float scale,
                                   const BwdWorkspace &ws, cudaStream_t stream);
 
+// maux: bf16 map over the auxiliary rows (box = 16 columns x 128 rows, 32-byte swizzle).
 // mdq: fp32 map over the dQ accumulator (box = half a head row x 128 rows), used for
 // TMA reduce-adds.
 cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
                                  const CUtensorMap &mv, const CUtensorMap &mdo,
-                                 const CUtensorMap &mdq,
+                                 const CUtensorMap &maux, const CUtensorMap &mdq,
                                  const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
                                  int B, int S, int nh, int nkv, int hd, float scale, int *status,
                                  uint64_t timeout_ns, cudaStream_t stream);
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, size_t n_elems,
-                              cudaStream_t stream);
+                              float scale, cudaStream_t stream);
 
 // fp32 CUDA-core path (hd <= 128).
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,

@@ -61,6 +61,7 @@ extern "C" xattn_status xattn_bwd_noalloc(const void *q, const void *k, const vo
   if (nh % nkv != 0) return XATTN_ERR_GROUP;
   if (hd != 32 && hd != 64) return XATTN_ERR_UNSUPPORTED_HD;
   if (!std::isfinite(scale)) return XATTN_ERR_BAD_SCALE;
+  if (scale != 0.f && std::fabs(scale) < 0x1p-64f) return XATTN_ERR_BAD_SCALE;
   for (const void *p : {q, k, v, o, dO, static_cast<const void *>(dq), static_cast<const void *>(dk),
                         static_cast<const void *>(dv)})
     if (reinterpret_cast<uintptr_t>(p) & 15u) return XATTN_ERR_MISALIGNED;
@@ -70,12 +71,12 @@ extern "C" xattn_status xattn_bwd_noalloc(const void *q, const void *k, const vo
   void *scratch = nullptr;
   const xattn_status st = xattn::scratch_address(&scratch);
   if (st != XATTN_OK) return st;
-  // The three steps rewrite every scratch byte they read (the preprocess writes all of
-  // D and LSE2, pad rows included, and zeroes the dQ accumulator), so contents left by
+  // The three steps rewrite every scratch byte they read (the preprocess writes every
+  // auxiliary row, pad rows included, and zeroes the dQ accumulator), so contents left by
   // an earlier call never leak into this one.
-  xattn_status r = xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, scratch, need, stream);
+  xattn_status r = xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, scale, scratch, need, stream);
   if (r == XATTN_OK)
     r = xattn_bwd_main(q, k, v, dO, B, S, nh, nkv, hd, scale, dk, dv, scratch, need, stream);
-  if (r == XATTN_OK) r = xattn_bwd_dq_convert(B, S, nh, hd, dq, scratch, need, stream);
+  if (r == XATTN_OK) r = xattn_bwd_dq_convert(B, S, nh, hd, scale, dq, scratch, need, stream);
   return r;
 }

@@ -60,9 +60,9 @@ _SIGS = {
     "xattn_fwd": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp],
     "xattn_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp],
     "xattn_bwd_noalloc": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp],
-    "xattn_bwd_preprocess": [_vp, _vp, _vp, _i, _i, _i, _i, _vp, _sz, _vp],
+    "xattn_bwd_preprocess": [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _sz, _vp],
     "xattn_bwd_main": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _sz, _vp],
-    "xattn_bwd_dq_convert": [_i, _i, _i, _i, _vp, _vp, _sz, _vp],
+    "xattn_bwd_dq_convert": [_i, _i, _i, _i, _f, _vp, _vp, _sz, _vp],
     "xattn_fwd_f32": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp],
     "xattn_bwd_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp],
     "xattn_check_device_status": [_vp],
@@ -135,9 +135,9 @@ def xattn_bwd_workspace_bytes(B, S, nh, hd) -> int:
     return int(_lib.xattn_bwd_workspace_bytes(B, S, nh, hd))
 
 
-def xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, workspace, workspace_bytes, stream=None):
-    _call("xattn_bwd_preprocess", _addr(o), _addr(dO), _addr(lse), B, S, nh, hd, _addr(workspace),
-          workspace_bytes, _stream(stream))
+def xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, scale, workspace, workspace_bytes, stream=None):
+    _call("xattn_bwd_preprocess", _addr(o), _addr(dO), _addr(lse), B, S, nh, hd, scale,
+          _addr(workspace), workspace_bytes, _stream(stream))
 
 
 def xattn_bwd_main(q, k, v, dO, B, S, nh, nkv, hd, scale, dk, dv, workspace, workspace_bytes,
@@ -146,8 +146,8 @@ def xattn_bwd_main(q, k, v, dO, B, S, nh, nkv, hd, scale, dk, dv, workspace, wor
           _addr(dk), _addr(dv), _addr(workspace), workspace_bytes, _stream(stream))
 
 
-def xattn_bwd_dq_convert(B, S, nh, hd, dq, workspace, workspace_bytes, stream=None):
-    _call("xattn_bwd_dq_convert", B, S, nh, hd, _addr(dq), _addr(workspace), workspace_bytes,
+def xattn_bwd_dq_convert(B, S, nh, hd, scale, dq, workspace, workspace_bytes, stream=None):
+    _call("xattn_bwd_dq_convert", B, S, nh, hd, scale, _addr(dq), _addr(workspace), workspace_bytes,
           _stream(stream))
 
 

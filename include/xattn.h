@@ -56,7 +56,8 @@ typedef enum {
     XATTN_ERR_CUDA = 6,               /* a CUDA runtime or driver call failed */
     XATTN_ERR_NO_DEVICE_SUPPORT = 7,  /* the current device is not compute capability 10.3 */
     XATTN_ERR_DEVICE_TIMEOUT = 8,     /* a bounded on-device wait expired (reported later) */
-    XATTN_ERR_BAD_SCALE = 9,          /* scale is not finite */
+    XATTN_ERR_BAD_SCALE = 9,          /* scale is not finite (bf16 backward: or
+                                         0 < |scale| < 2^-64) */
     XATTN_ERR_WORKSPACE = 10,         /* workspace pointer NULL/misaligned or too small */
     XATTN_ERR_SCRATCH_LIMIT = 11      /* xattn_bwd_noalloc: sizes need more than its fixed scratch */
 } xattn_status;
@@ -74,11 +75,14 @@ xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S
 /*
  * Backward, bf16 (row T14: recompute the scores, D = rowsum(dO * O); row T15: dK/dV
  * summed over each kv head's query group without atomics). Takes the forward's o and
- * lse. Writes dq [B,S,nh,hd], dk and dv [B,S,nkv,hd] in bf16.
+ * lse. Writes dq [B,S,nh,hd], dk and dv [B,S,nkv,hd] in bf16. scale == 0 is taken
+ * exactly; a nonzero |scale| below 2^-64 is rejected (XATTN_ERR_BAD_SCALE), because the
+ * recompute adds -LSE/scale to the scores inside a tensor-core product.
  * Scratch (xattn_bwd_workspace_bytes) is taken with cudaMallocAsync on `stream` and
  * released with cudaFreeAsync on the same stream; nothing else is allocated.
- * dQ is accumulated across key tiles with fp32 atomic adds, so its last bits may
- * vary from run to run; dK, dV, o and lse are bit-for-bit reproducible.
+ * dQ is accumulated across key tiles with fp32 reduce-adds whose order is not fixed,
+ * so its last bits may vary from run to run; dK, dV, o and lse are bit-for-bit
+ * reproducible.
  */
 xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *o,
                        const void *dO, const float *lse, int B, int S, int nh, int nkv,
@@ -92,21 +96,24 @@ xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *
  * workspace: device pointer, 256-byte aligned, at least xattn_bwd_workspace_bytes()
  * bytes. Its contents on entry do not matter; the three steps must run in this order
  * on one stream with the same arguments.
- *   xattn_bwd_preprocess : D_i = dO_i . O_i (fp32), the log2-domain LSE rows, and a
- *                          zeroed fp32 dQ accumulator (all inside the workspace).
- *   xattn_bwd_main       : the recompute loop; writes dk, dv and adds into the dQ
- *                          accumulator.
- *   xattn_bwd_dq_convert : dq = bf16(dQ accumulator).
+ *   xattn_bwd_preprocess : D_i = dO_i . O_i (fp32); per query row, -LSE_i/scale and
+ *                          -D_i as bf16 operand rows of the recompute (each the sum
+ *                          of three bf16 terms); a zeroed fp32 dQ accumulator (all
+ *                          inside the workspace).
+ *   xattn_bwd_main       : the recompute loop; writes dk, dv and adds dS K into the
+ *                          dQ accumulator (without the softmax scale).
+ *   xattn_bwd_dq_convert : dq = bf16(scale * dQ accumulator); scale is the one given
+ *                          to xattn_bwd_main.
  */
 size_t xattn_bwd_workspace_bytes(int B, int S, int nh, int hd);
 xattn_status xattn_bwd_preprocess(const void *o, const void *dO, const float *lse, int B,
-                                  int S, int nh, int hd, void *workspace,
+                                  int S, int nh, int hd, float scale, void *workspace,
                                   size_t workspace_bytes, void *stream);
 xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const void *dO,
                             int B, int S, int nh, int nkv, int hd, float scale, void *dk,
                             void *dv, void *workspace, size_t workspace_bytes, void *stream);
-xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, void *dq, void *workspace,
-                                  size_t workspace_bytes, void *stream);
+xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, float scale, void *dq,
+                                  void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * xattn_bwd with no allocation at all. The pages have no counterpart: this entry point

@@ -24,22 +24,25 @@ def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-4))
 
 
-def run_gpu(w: W.Workload, x: dict, device="cuda"):
-    """Forward then backward through the C ABI. Returns float64 numpy outputs."""
+def run_gpu(w: W.Workload, x: dict, device="cuda", scale=None):
+    """Forward then backward through the C ABI (with the workload's scale unless one is
+    given). Returns float64 numpy outputs."""
     from bwd_xattn_fwd_gb300 import xattn
+    scale = w.scale if scale is None else scale
     q, k, v, dO = (x[n].to(device) for n in ("q", "k", "v", "dO"))
-    o, lse = xattn.attention_fwd(q, k, v, w.scale)
-    dq, dk, dv = xattn.attention_bwd(q, k, v, o, dO, lse, w.scale)
+    o, lse = xattn.attention_fwd(q, k, v, scale)
+    dq, dk, dv = xattn.attention_bwd(q, k, v, o, dO, lse, scale)
     torch.cuda.synchronize()
     assert xattn.xattn_check_device_status() == 0
     return {n: W.as_f64(t) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
 
 
-def oracle_full(w: W.Workload, x: dict):
+def oracle_full(w: W.Workload, x: dict, scale=None):
+    scale = w.scale if scale is None else scale
     q, k, v, dO = (W.as_f64(x[n]) for n in ("q", "k", "v", "dO"))
     orc = oracle.default()
-    o, lse = orc.fwd(q, k, v, w.scale)
-    dq, dk, dv = orc.bwd(q, k, v, dO, w.scale)
+    o, lse = orc.fwd(q, k, v, scale)
+    dq, dk, dv = orc.bwd(q, k, v, dO, scale)
     return {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
 
 

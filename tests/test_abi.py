@@ -72,6 +72,26 @@ def test_fwd_argument_checks(lib):
     assert _fwd(lib, scale=float("inf")) == 9
 
 
+def _bwd(lib, scale):
+    f = lib.xattn_bwd
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_float]
+                  + [ctypes.c_void_p] * 4)
+    return f(16, 32, 48, 64, 80, 96, 1, 4, 2, 1, 64, scale, 112, 128, 144, None)
+
+
+def test_bwd_scale_checks(lib):
+    # The bf16 backward adds -LSE/scale inside a tensor-core product: it takes scale == 0
+    # exactly and rejects a nonzero |scale| below 2^-64 on the host.
+    assert _bwd(lib, float("nan")) == 9
+    assert _bwd(lib, 1e-30) == 9
+    assert _bwd(lib, -1e-30) == 9
+    import torch
+    if not torch.cuda.is_available():
+        assert _bwd(lib, 0.0) == 6                     # accepted; fails only for want of a GPU
+        assert _bwd(lib, 2.0 ** -64) == 6
+
+
 def test_f32_head_dim_limit(lib):
     f = lib.xattn_fwd_f32
     f.restype = ctypes.c_int
@@ -83,15 +103,18 @@ def test_workspace_checks(lib):
     lib.xattn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.xattn_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 4
     n = lib.xattn_bwd_workspace_bytes(2, 200, 4, 64)
-    # D and LSE2 rows padded to 256 (=2 tiles): 2*4*256*4 B each; accumulator 2*200*4*64*4 B.
-    assert n == 2 * (2 * 4 * 256 * 4) + 2 * 200 * 4 * 64 * 4
+    # Auxiliary rows padded to 256 (=2 tiles): 2*4*256 rows of 16 bf16; accumulator
+    # 2*200*4*64 fp32.
+    assert n == 2 * 4 * 256 * 16 * 2 + 2 * 200 * 4 * 64 * 4
     assert lib.xattn_bwd_workspace_bytes(0, 200, 4, 64) == 0
     f = lib.xattn_bwd_dq_convert
     f.restype = ctypes.c_int
-    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
-    assert f(2, 200, 4, 64, 256, None, n, None) == 10          # NULL workspace
-    assert f(2, 200, 4, 64, 256, 4096 + 16, n, None) == 10     # not 256-byte aligned
-    assert f(2, 200, 4, 64, 256, 4096, n - 1, None) == 10      # too small
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_size_t, ctypes.c_void_p]
+    assert f(2, 200, 4, 64, 0.125, 256, None, n, None) == 10          # NULL workspace
+    assert f(2, 200, 4, 64, 0.125, 256, 4096 + 16, n, None) == 10     # not 256-byte aligned
+    assert f(2, 200, 4, 64, 0.125, 256, 4096, n - 1, None) == 10      # too small
+    assert f(2, 200, 4, 64, float("nan"), 256, 4096, n, None) == 9    # non-finite scale
 
 
 def test_no_device_is_a_cuda_error(lib):

@@ -65,6 +65,18 @@ def test_edge_shapes_bf16(shape):
     compare(run_gpu(w, x), oracle_full(w, x), "bf16", str(shape))
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("scale", [0.0, 1.0, -0.3, 2.0 ** -40], ids=lambda s: "scale=%g" % s)
+def test_scale_values(scale, dtype):
+    """Scales other than 1/sqrt(hd): zero (uniform attention over the causal prefix; dQ
+    and dK vanish), large, negative (the row maximum of the scaled scores is the scaled
+    minimum of the raw ones) and tiny. The bf16 backward adds -LSE/scale to the scores
+    inside a tensor-core product, with scale == 0 taken as its own case."""
+    w = W.Workload("scale", 2, 200, 4, 2, 64 if dtype == "bf16" else 32, dtype, qkv_scale=0.5)
+    x = W.make_inputs(w, seed=7)
+    compare(run_gpu(w, x, scale=scale), oracle_full(w, x, scale=scale), dtype, "scale=%g" % scale)
+
+
 EDGE_F32 = [(1, 1, 1, 1, 8), (2, 37, 6, 3, 24), (1, 150, 4, 2, 128), (1, 64, 2, 1, 1)]
 
 
@@ -121,10 +133,10 @@ def test_stage_calls_match_bwd():
     nbytes = xattn.xattn_bwd_workspace_bytes(w.B, w.S, w.nh, w.hd)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     dq2, dk2, dv2 = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
-    xattn.xattn_bwd_preprocess(o, x["dO"], lse, w.B, w.S, w.nh, w.hd, ws, nbytes)
+    xattn.xattn_bwd_preprocess(o, x["dO"], lse, w.B, w.S, w.nh, w.hd, w.scale, ws, nbytes)
     xattn.xattn_bwd_main(x["q"], x["k"], x["v"], x["dO"], w.B, w.S, w.nh, w.nkv, w.hd, w.scale,
                          dk2, dv2, ws, nbytes)
-    xattn.xattn_bwd_dq_convert(w.B, w.S, w.nh, w.hd, dq2, ws, nbytes)
+    xattn.xattn_bwd_dq_convert(w.B, w.S, w.nh, w.hd, w.scale, dq2, ws, nbytes)
     torch.cuda.synchronize()
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
     assert (dq.float() - dq2.float()).abs().max() <= TOL_BF16 * dq.float().abs().max()
