@@ -229,7 +229,6 @@ __global__ void __maxnreg__(168)
 
   // Unit of this CTA: key tile n (most work first), batch b, kv head kvh.
   const int num_m = (S + kTileRows - 1) / kTileRows;
-  const int S_pad = num_m * kTileRows;
   const int BK = B * nkv;
   const int n = static_cast<int>(blockIdx.x) / BK;
   const int bk = static_cast<int>(blockIdx.x) % BK;

@@ -24,6 +24,8 @@
 // Causal tile skipping: tile m visits key tiles 0..m. CTAs are issued longest first.
 // TMEM columns: S_A [0,128) S_B [128,256) fp32 | O_A [256,256+HD) O_B [320,320+HD) fp32 |
 //               P_A [384,448) P_B [448,512) bf16 pairs.
+#include <type_traits>
+
 #include "sm103_ptx.cuh"
 #include "xattn_internal.h"
 
@@ -104,9 +106,10 @@ __global__ void __maxnreg__(168)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(q_full, 1);
+    // Each K/V stage is released by both MMA issuers (warp 1 for tile A, warp 3 for B).
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(s_full(x), 1);
@@ -114,7 +117,7 @@ __global__ void __maxnreg__(168)
       mbar_init(o_done(x), 1);
       mbar_init(s_free(x), 128);
     }
-    mbar_init(mma_final, 1);
+    mbar_init(mma_final, 2);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -152,65 +155,64 @@ __global__ void __maxnreg__(168)
     mbar_drain(q_full, 0, ctl);
     for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
       mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- MMA issuers: warp 1 for query tile A, warp 3 for tile B ----------------
+    // Two issuers let the two softmax warpgroups run independently of each other's pace
+    // (a single issuer would impose its own A/B order), and split the issue cost over two
+    // SM sub-partitions. The tensor pipe takes their MMAs in arrival order; the K/V
+    // stages are released by a commit from each (empty counts 2).
+    const int x = warp == 1 ? 0 : 1;
+    const int mX = x == 0 ? mA : mB;
+    const bool active = x == 0 || hasB;
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;        // tile stride, descriptor units
     constexpr uint32_t kVStep = (16 * L::kRowBytes) >> 4;      // 16 key rows of V
     // Descriptors are built once; a K step of 16 elements is +32 bytes (+2) within the
     // swizzled K-major rows of Q and K, and +16 rows of the MN-major V tile.
-    const uint64_t dQ = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t dQ = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle) + x * kStageDesc;
     const uint64_t dK = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t dV = smem_desc(sV, 8192, 8 * L::kRowBytes, L::kSwizzle);
-    auto issue_qk = [&](int x, int s) {
+    const uint32_t tSx = tS(x), tOx = tO(x), tPx = tP(x);
+    auto issue_qk = [&](int s) {
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        mma_ss_elect(tS(x), dQ + x * kStageDesc + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk,
-                     kk > 0);
+        mma_ss_elect(tSx, dQ + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
     };
-    auto issue_pv = [&](int x, int s, bool first) {
+    auto issue_pv = [&](int s, bool first) {
 #pragma unroll
       for (int kk = 0; kk < kTileRows / 16; ++kk)
-        mma_ts_elect(tO(x), tP(x) + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv,
+        mma_ts_elect(tOx, tPx + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv,
                      (!first || kk > 0) ? 1u : 0u);
     };
-    bool ok = warp_wait(q_full, 0, ctl) && warp_wait(full(0), 0, ctl);
+    bool ok = active && warp_wait(q_full, 0, ctl) && warp_wait(full(0), 0, ctl);
     if (ok) {
       tc_fence_after();
-      issue_qk(0, 0);
-      mma_commit_elect(s_full(0));
-      if (hasB) {
-        issue_qk(1, 0);
-        mma_commit_elect(s_full(1));
-      }
+      issue_qk(0);
+      mma_commit_elect(s_full(x));
     }
-    // Per key tile n and query tile X: S_X(n+1) as soon as the softmax has loaded the
-    // last of S_X(n) (s_free, signalled half-way through its exponentials), then PV_X(n)
-    // once P_X(n) is in TMEM (p_full). The next scores are thus computed while the
-    // softmax is still producing P_X(n).
-    for (int n = 0, s = 0, s1 = 1 % kFwdStages, ph1 = (1 / kFwdStages) & 1; ok && n <= n_last; ++n) {
-      bool next_loaded = false;
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        const int mX = x == 0 ? mA : mB;
-        if (x == 1 && !hasB) break;
-        if (n > mX) continue;
-        if (n + 1 <= mX) {
-          if (!warp_wait(s_free(x), n & 1, ctl)) { ok = false; break; }
-          if (!next_loaded && !warp_wait(full(s1), ph1, ctl)) { ok = false; break; }
-          next_loaded = true;
-          tc_fence_after();
-          issue_qk(x, s1);
-          mma_commit_elect(s_full(x));
-        }
-        if (!warp_wait(p_full(x), n & 1, ctl)) { ok = false; break; }
+    // Per key tile n: S_X(n+1) as soon as the softmax has loaded the last of S_X(n)
+    // (s_free, signalled half-way through its exponentials), then PV_X(n) once P_X(n) is
+    // in TMEM (p_full). The next scores are thus computed while the softmax is still
+    // producing P_X(n).
+    // Release of stage s: each issuer that uses key tile n commits once, or twice when it
+    // is the tile's only user (tile mB when there is a tile B; every tile when there is
+    // not). An issuer never arrives for a tile it does not use, so its arrivals cannot
+    // land in an earlier phase of the stage that the other issuer has not released yet.
+    for (int n = 0, s = 0, s1 = 1 % kFwdStages, ph1 = (1 / kFwdStages) & 1; ok && n <= mX; ++n) {
+      if (n + 1 <= mX) {
+        if (!warp_wait(s_free(x), n & 1, ctl) || !warp_wait(full(s1), ph1, ctl)) { ok = false; break; }
         tc_fence_after();
-        issue_pv(x, s, n == 0);
-        mma_commit_elect(o_done(x));
+        issue_qk(s1);
+        mma_commit_elect(s_full(x));
       }
-      if (!ok) break;
-      mma_commit_elect(empty(s));                  // K_n and V_n fully consumed
+      if (!warp_wait(p_full(x), n & 1, ctl)) { ok = false; break; }
+      tc_fence_after();
+      issue_pv(s, n == 0);
+      mma_commit_elect(o_done(x));
+      const bool shared_tile = x == 0 ? hasB : n <= mA;
+      mma_commit_elect(empty(s));                  // this issuer is done with K_n and V_n
+      if (!shared_tile) mma_commit_elect(empty(s));
       if (++s == kFwdStages) s = 0;
       if (++s1 == kFwdStages) { s1 = 0; ph1 ^= 1; }
     }
@@ -282,29 +284,28 @@ __global__ void __maxnreg__(168)
           tc_fence_before();
           mbar_arrive(s_free(x));
         }
-        // Exponents in place, then the causal mask on them (-inf -> exact zeros for any
-        // scale, 0 included), then the exponentials.
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          float x0, x1;
-          ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
-                scale_log2, neg_m, neg_m);
-          r[2 * e] = __float_as_uint(x0);
-          r[2 * e + 1] = __float_as_uint(x1);
-        }
-        if (diag) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c64 + c > row) r[c] = __float_as_uint(-INFINITY);
-        }
+        // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
+        // included), the exponentials, row sums and bf16 P. The diagonal tile has its own
+        // copy of the body, so the common one is a single branch-free block.
         uint32_t pk[32];
+        auto body = [&](auto masked) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const float p0 = ex2_approx(__uint_as_float(r[2 * e])), p1 = ex2_approx(__uint_as_float(r[2 * e + 1]));
-          const int a = (e & 1) * 2;
-          fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
-          pk[e] = pack_bf16x2(p0, p1);
-        }
+          for (int e = 0; e < 32; ++e) {
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
+                  scale_log2, neg_m, neg_m);
+            if (decltype(masked)::value) {
+              if (c64 + 2 * e > row) x0 = -INFINITY;
+              if (c64 + 2 * e + 1 > row) x1 = -INFINITY;
+            }
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const int a = (e & 1) * 2;
+            fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
+            pk[e] = pack_bf16x2(p0, p1);
+          }
+        };
+        if (diag) body(std::true_type{});
+        else body(std::false_type{});
         tmem_st_x16(tPx + c64 / 2, pk);
         tmem_st_x16(tPx + c64 / 2 + 16, pk + 16);
       }
