@@ -197,12 +197,12 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
 
 // Role map (12 warps):
 //   warp 0     : TMA producer
-//   warp 1     : TMEM owner and MMA issuer
+//   warp 1     : TMEM owner; MMA issuer of S^T and dV
 //   warp 2     : dQ reducer: TMA reduce-adds each staged dQ tile into the fp32
 //                accumulator (2 bulk operations per tile instead of scattered atomics)
-//   warp 3     : idle
-//   warps 4-7  : P^T = exp2(S^T scale log2e - LSE2), one thread per key row, all 128
-//                query columns (the special-function work)
+//   warp 3     : MMA issuer of dP^T, dK and dQ
+//   warps 4-7  : P^T = exp2(S^T scale log2e), S^T already holding -LSE/scale, one
+//                thread per key row, all 128 query columns (the special-function work)
 //   warps 8-11 : dS^T = P^T (dP^T - D), one thread per key row (the FMA work), and the
 //                dQ drain (TMEM -> shared-memory staging, one query row per thread)
 // The two compute warpgroups work on consecutive (r, m) iterations at the same time, so
@@ -267,7 +267,7 @@ __global__ void __maxnreg__(168)
     mbar_init(kv_full, 1);
     for (int s = 0; s < kBwdStages; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), 2);                        // one commit from each MMA issuer
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, 128);
@@ -281,7 +281,7 @@ __global__ void __maxnreg__(168)
     mbar_init(dq_empty, 128);
     mbar_init(dqs_full, 128);
     mbar_init(dqs_empty, 1);
-    mbar_init(acc_done, 1);
+    mbar_init(acc_done, 2);
     fence_mbar_init();
   }
   // Constant key-side auxiliary tiles: row r = [1 1 1 0 ...] (S^T) and [0 0 0 1 1 1 0 ...]
@@ -335,8 +335,14 @@ __global__ void __maxnreg__(168)
     mbar_drain(kv_full, 0, ctl);
     for (int t = (issued > kBwdStages ? issued - kBwdStages : 0); t < issued; ++t)
       mbar_drain(full(t % kBwdStages), (t / kBwdStages) & 1, ctl);
-  } else if (warp == 1) {
-    // ---------------- MMA issuer (converged warp, one elected lane issues) ----------------
+  } else if (warp == 1 || warp == 3) {
+    // ---------------- MMA issuers (converged warps, one elected lane issues) ----------------
+    // Warp 1 issues the products the P warps depend on (S^T, dV); warp 3 those of the dS
+    // warps (dP^T, dK, dQ). Each stream is in order, but neither waits behind the other,
+    // so S^T(t+1) never queues behind a dQ that is waiting for the dQ drain. The tensor
+    // pipe takes the two streams' MMAs in arrival order; each stage is released by one
+    // commit from each issuer (empty counts 2), and acc_done gets one from each.
+    const bool p_side = warp == 1;
     constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
     constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A K-major)
     constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);    // dQ (A = dS, MN-major)
@@ -344,75 +350,72 @@ __global__ void __maxnreg__(168)
     constexpr uint32_t kRowStep = (16 * L::kRowBytes) >> 4;  // 16 rows of an MN-major tile
     // Descriptors are built once. K-major operands advance +32 bytes (+2) per
     // 16-element K step; MN-major ones advance 16 rows.
-    const uint64_t kK_k = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kV_k = smem_desc(sV, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kQ_k = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kdO_k = smem_desc(sdO, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kA_k = smem_desc(p_side ? sK : sV, 16, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kB_k = smem_desc(p_side ? sQ : sdO, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kQ_mn = smem_desc(sQ, 8192, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kdO_mn = smem_desc(sdO, 8192, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kdS_mn = smem_desc(sdS, 16384, 1024, kSwizzle128);
     const uint64_t kdS_k = smem_desc(sdS, 16, 1024, kSwizzle128);
-    const uint64_t kAuxS = smem_desc(sAuxA, 16, 256, kSwizzle32);
-    const uint64_t kAuxD = smem_desc(sAuxA + L::kAuxTileBytes, 16, 256, kSwizzle32);
+    const uint64_t kAuxA = smem_desc(sAuxA + (p_side ? 0u : L::kAuxTileBytes), 16, 256, kSwizzle32);
     const uint64_t kAuxQ = smem_desc(sAuxB, 16, 256, kSwizzle32);
     constexpr uint32_t kAuxStageDesc = L::kAuxTileBytes >> 4;
-    // S^T = K Q^T - LSE/scale, dP^T = V dO^T - D: the head-dim K steps, then one
-    // auxiliary K step that adds the per-query term (key-side ones x query-side terms).
-    auto issue_t = [&](uint32_t d, uint64_t a, uint64_t bdesc, bool with_qk, uint64_t aux_a, int stage) {
+    // S^T = K Q^T - LSE/scale (P side) or dP^T = V dO^T - D (dS side): the head-dim K
+    // steps, then one auxiliary K step that adds the per-query term (key-side ones x
+    // query-side terms). With scale == 0 S^T is the auxiliary term alone.
+    const uint32_t tD = p_side ? tS : tdP;
+    const bool with_qk = p_side ? qk : true;
+    auto issue_t = [&](int stage) {
       if (with_qk) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a + 2 * kk, bdesc + 2 * kk, idesc_t, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_ss_elect(tD, kA_k + 2 * kk, kB_k + stage * kStageDesc + 2 * kk, idesc_t, kk > 0);
       }
-      mma_ss_elect(d, aux_a, kAuxQ + stage * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
+      mma_ss_elect(tD, kAuxA, kAuxQ + stage * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
     };
+    const uint32_t t_full = p_side ? s_full : dp_full;    // this side's score product
+    const uint32_t t_free = p_side ? s_free : dp_free;
     bool ok = warp_wait(kv_full, 0, ctl) && warp_wait(full(0), 0, ctl);
     if (ok) {
       tc_fence_after();
-      issue_t(tS, kK_k, kQ_k, qk, kAuxS, 0);
-      mma_commit_elect(s_full);
-      issue_t(tdP, kV_k, kdO_k, true, kAuxD, 0);
-      mma_commit_elect(dp_full);
+      issue_t(0);
+      mma_commit_elect(t_full);
     }
     for (int t = 0, s = 0; ok && t < T; ++t) {
       const int s1 = (s + 1 == kBwdStages) ? 0 : s + 1;
       const bool more = t + 1 < T;
       const uint32_t ph = t & 1;
       if (more) {
-        // S^T(t+1) as soon as the P warps have read S^T(t).
-        if (!warp_wait(full(s1), ((t + 1) / kBwdStages) & 1, ctl)) break;
-        if (!warp_wait(s_free, ph, ctl)) break;
+        // The next score product as soon as this side's warps have read the current one.
+        if (!warp_wait(full(s1), ((t + 1) / kBwdStages) & 1, ctl) || !warp_wait(t_free, ph, ctl)) break;
         tc_fence_after();
-        issue_t(tS, kK_k, kQ_k + s1 * kStageDesc, qk, kAuxS, s1);
-        mma_commit_elect(s_full);
+        issue_t(s1);
+        mma_commit_elect(t_full);
       }
-      if (!warp_wait(p_full, ph, ctl)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kTileRows / 16; ++kk)                            // dV += P^T dO
-        mma_ts_elect(tdV, tP + kk * 8, kdO_mn + s * kStageDesc + kk * kRowStep, idesc_acc,
-                     (t > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_elect(dv_done);
-      if (more) {
-        // dP^T(t+1) as soon as the dS warps have read dP^T(t).
-        if (!warp_wait(dp_free, ph, ctl)) break;
+      if (p_side) {
+        if (!warp_wait(p_full, ph, ctl)) break;
         tc_fence_after();
-        issue_t(tdP, kV_k, kdO_k + s1 * kStageDesc, true, kAuxD, s1);
-        mma_commit_elect(dp_full);
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)                          // dV += P^T dO
+          mma_ts_elect(tdV, tP + kk * 8, kdO_mn + s * kStageDesc + kk * kRowStep, idesc_acc,
+                       (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(dv_done);
+        mma_commit_elect(empty(s));                  // S^T(t) and dV(t) are done with stage s
+      } else {
+        if (!warp_wait(ds_full, ph, ctl)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)                          // dK += dS^T Q
+          mma_ss_elect(tdK, kdS_k + (kk >> 2) * 1024 + (kk & 3) * 2,
+                       kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_elect(empty(s));                  // dP^T(t) and dK(t) are done with stage s
+        if (t > 0 && !warp_wait(dq_empty, ph ^ 1, ctl)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)                          // dQ = dS K
+          mma_ss_elect(tdQ, kdS_mn + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
+        mma_commit_elect(dq_full);
       }
-      if (!warp_wait(ds_full, ph, ctl)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kTileRows / 16; ++kk)                            // dK += dS^T Q
-        mma_ss_elect(tdK, kdS_k + (kk >> 2) * 1024 + (kk & 3) * 2,
-                     kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-      mma_commit_elect(empty(s));
-      if (t > 0 && !warp_wait(dq_empty, ph ^ 1, ctl)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kTileRows / 16; ++kk)                            // dQ = dS K
-        mma_ss_elect(tdQ, kdS_mn + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
-      mma_commit_elect(dq_full);
       s = s1;
     }
     mma_commit_elect(acc_done);
@@ -445,21 +448,24 @@ __global__ void __maxnreg__(168)
       const bool diag = (m == n);
       if (!warp_wait(s_full, t & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      uint32_t ra[32], rb[32];
-      tmem_ld_x32(tS + lane_off, ra);
+      // The whole row of S^T(t) comes into registers with one TMEM read and the buffer is
+      // released at once, so S^T(t+1) is computed while these exponentials run.
+      uint32_t r[128];
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) tmem_ld_x32(tS + lane_off + c, r + c);
       tmem_wait_ld();
-      reg_fence<32>(ra);
+      reg_fence<128>(r);
+      tc_fence_before();
+      mbar_arrive(s_free);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t *cur = (c & 1) ? rb : ra;
-        uint32_t *nxt = (c & 1) ? ra : rb;
-        if (c < 3) tmem_ld_x32(tS + lane_off + 32 * (c + 1), nxt);    // next chunk in flight
         uint32_t pk[16];
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4) {
+          const uint32_t *cur = r + 32 * c + 4 * q4;
           float x0, x1, x2, x3;
-          fmul2(x0, x1, __uint_as_float(cur[4 * q4]), __uint_as_float(cur[4 * q4 + 1]), scale_log2, scale_log2);
-          fmul2(x2, x3, __uint_as_float(cur[4 * q4 + 2]), __uint_as_float(cur[4 * q4 + 3]), scale_log2, scale_log2);
+          fmul2(x0, x1, __uint_as_float(cur[0]), __uint_as_float(cur[1]), scale_log2, scale_log2);
+          fmul2(x2, x3, __uint_as_float(cur[2]), __uint_as_float(cur[3]), scale_log2, scale_log2);
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
           if (diag) {
             const int i = 32 * c + 4 * q4;
@@ -474,21 +480,12 @@ __global__ void __maxnreg__(168)
         if (c == 0 && t > 0) {
           // P^T(t-1) must have been read by the dS warps and by dV(t-1).
           if (!warp_wait(p_free, (t - 1) & 1, ctl) || !warp_wait(dv_done, (t - 1) & 1, ctl)) {
-            tmem_wait_ld();    // the load of chunk 1 is still in flight
             ok = false;
             break;
           }
           tc_fence_after();
         }
         tmem_st_x16(tP + lane_off + 16 * c, pk);
-        if (c < 3) {
-          tmem_wait_ld();
-          reg_fence<32>(nxt);
-        }
-        if (c == 2) {          // the last chunk of S^T(t) is in registers
-          tc_fence_before();
-          mbar_arrive(s_free);
-        }
       }
       if (!ok) break;
       tmem_wait_st();
