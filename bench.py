@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="time xattn_bwd_deterministic (bit-reproducible dQ) as the backward")
     return ap.parse_args()
 
 
@@ -260,6 +262,10 @@ def run_ours(args, w: W.Workload):
     stream = torch.cuda.current_stream(dev)
 
     names = ["attn_fwd_kernel", "bwd_preprocess_kernel", "attn_bwd_main_kernel", "dq_convert_kernel"]
+    if args.deterministic:
+        # xattn_bwd_deterministic runs its three kernels (preprocess, dK/dV recompute, dQ
+        # recompute) inside one call: it is timed as one segment.
+        names = ["attn_fwd_kernel", "bwd_deterministic"]
 
     def step(evs=None):
         if evs:
@@ -267,6 +273,12 @@ def run_ours(args, w: W.Workload):
         xattn.xattn_fwd(x["q"], x["k"], x["v"], B, S, nh, nkv, hd, scale, o, lse, stream)
         if evs:
             evs[1].record(stream)
+        if args.deterministic:
+            xattn.xattn_bwd_deterministic(x["q"], x["k"], x["v"], o, x["dO"], lse, B, S, nh, nkv, hd,
+                                          scale, dq, dk, dv, stream)
+            if evs:
+                evs[2].record(stream)
+            return
         xattn.xattn_bwd_preprocess(o, x["dO"], lse, B, S, nh, hd, scale, ws, ws_bytes, stream)
         if evs:
             evs[2].record(stream)
@@ -286,7 +298,8 @@ def run_ours(args, w: W.Workload):
     if status != 0:
         raise RuntimeError(f"device status {status} during warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+              for _ in range(args.steps)]
     barrier(pg)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
@@ -300,7 +313,7 @@ def run_ours(args, w: W.Workload):
         raise RuntimeError(f"device status {status} in the timed region")
 
     per_kernel = {n: [ev[j].elapsed_time(ev[j + 1]) for ev in events] for j, n in enumerate(names)}
-    step_ms = [ev[0].elapsed_time(ev[4]) for ev in events]
+    step_ms = [ev[0].elapsed_time(ev[len(names)]) for ev in events]
     total_ms = max_over_ranks(pg, sum(step_ms), dev)
     ms_per_step = total_ms / args.steps
     flops_step = w.fwd_flops + w.bwd_flops
@@ -311,11 +324,17 @@ def run_ours(args, w: W.Workload):
     kavg = {n: statistics.mean(v) for n, v in per_kernel.items()}
     S_pad = (S + 127) // 128 * 128
     elems = B * S * nh * hd
+    # Algorithmic work per launch: the forward's 2 products and the backward's 5 (2 hd
+    # flops per causal pair and head each); the preprocess reads O, dO and lse and
+    # writes the auxiliary rows, D and the zeroed dQ accumulator; the convert reads the
+    # accumulator and writes dq.
     kernel_work = {
         "attn_fwd_kernel": ("tensor", w.fwd_flops),
         "attn_bwd_main_kernel": ("tensor", w.bwd_flops),
-        "bwd_preprocess_kernel": ("hbm", 2 * elems * 2 + B * S * nh * 4 + 2 * B * nh * S_pad * 4 + elems * 4),
+        "bwd_preprocess_kernel": ("hbm", 2 * elems * 2 + B * S * nh * 4 + B * nh * S_pad * 32
+                                  + B * S * nh * 4 + elems * 4),
         "dq_convert_kernel": ("hbm", elems * 4 + elems * 2),
+        "bwd_deterministic": ("tensor", w.bwd_flops),
     }
     kernels = {}
     for n in names:
@@ -353,8 +372,9 @@ def run_ours(args, w: W.Workload):
             for n in h_in:
                 d_in[n].copy_(h_in[n], non_blocking=True)
             xattn.xattn_fwd(d_in["q"], d_in["k"], d_in["v"], B, S, nh, nkv, hd, scale, o, lse, stream)
-            xattn.xattn_bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["dO"], lse, B, S, nh, nkv, hd,
-                            scale, dq, dk, dv, stream)
+            bwd = xattn.xattn_bwd_deterministic if args.deterministic else xattn.xattn_bwd
+            bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["dO"], lse, B, S, nh, nkv, hd, scale, dq, dk,
+                dv, stream)
             for n in h_out:
                 h_out[n].copy_(d_out[n], non_blocking=True)
 
@@ -390,6 +410,7 @@ def run_ours(args, w: W.Workload):
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "S": w.S, "nh": w.nh, "nkv": w.nkv,
                        "hd": w.hd, "scale": scale,
+                       "backward": "deterministic dQ" if args.deterministic else "default",
                        "parallelism": f"{world} rank(s), each its own batch of (batch, kv-head) units; no collective",
                        "l2": "flushed before every step (256 MiB device write, outside the timed events)"},
             "tok_per_s": tok_s,

@@ -6,36 +6,38 @@
 // sum over its query group, taken deterministically without atomics.
 //
 // Three kernels, in stream order:
-//   1. preprocess (HBM-bound): D_i = sum_d dO_id O_id in fp32, the log2-domain LSE
-//      rows laid out [B, nh, S_pad] (both stored negated), and a zeroed fp32 dQ
-//      accumulator.
-//   2. main (tensor cores). One CTA per (batch, kv head, 128-row key tile n). The K_n
-//      and V_n tiles stay in shared memory; the dK_n / dV_n accumulators stay in TMEM
-//      while the CTA walks every query head r of the group and every query tile m >= n
-//      (causal tile skipping). That walk *is* the group sum of row T15: no atomics on
-//      dK/dV, and a fixed order, so they are reproducible. Per (r, m):
-//        S^T  = K_n Q_m^T               (TMEM, 128 x 128 fp32)
-//        dP^T = V_n dO_m^T              (TMEM, 128 x 128 fp32)
-//        P^T  = exp2(S^T scale log2e - LSE2_m)      -> bf16 into TMEM
-//        dS^T = P^T (dP^T - D_m)                    -> bf16 into shared memory
-//        dV_n += P^T dO_m                           (A operand from TMEM)
-//        dK_n += dS^T Q_m                           (A operand from shared memory)
-//        dQ_m  = dS K_n                 (TMEM) -> shared memory -> TMA reduce-add into
-//                                                      the fp32 accumulator
-//      The softmax scale of dS is applied once at the end, to dK_n in the epilogue and
-//      to dQ in step 3, instead of to every element of every dS tile.
-//      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer, 2 = dQ reducer,
-//      4-7 = P (one thread per key row), 8-11 = dS and the dQ drain.
-//   3. dq convert: dq = bf16(scale * accumulator).
+//   1. preprocess (HBM-bound): D_i = sum_d dO_id O_id in fp32, and per query row the
+//      bf16 auxiliary operand row holding -LSE_i/scale and -D_i.
+//   2. main, this file (tensor cores): dK and dV. One CTA per (batch, kv head, 128-row
+//      key tile n). The K_n and V_n tiles stay in shared memory; the dK_n / dV_n
+//      accumulators stay in TMEM while the CTA walks every query head r of the group and
+//      every query tile m >= n (causal tile skipping). That walk *is* the group sum of
+//      row T15: no atomics on dK/dV, and a fixed order, so they are reproducible. Per
+//      (r, m):
+//        S^T  = K_n Q_m^T - LSE/scale   (TMEM, 128 x 128 fp32; the per-query term is one
+//        dP^T = V_n dO_m^T - D          extra tensor-core K step over the auxiliary rows)
+//        P^T  = exp2(S^T scale log2e)               -> bf16 into TMEM
+//        dS^T = P^T dP^T                            -> bf16 into TMEM
+//        dV_n += P^T dO_m ,  dK_n += dS^T Q_m       (A operands from TMEM)
+//      The softmax scale of dS is applied once, to dK_n in the epilogue.
+//      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer of S^T and dV,
+//      3 = MMA issuer of dP^T and dK, 4-7 = P, 8-11 = dS (one thread per key row).
+//   3. dQ: by default the main kernel also computes dQ_m = dS K_n per iteration and
+//      adds it into an fp32 accumulator with TMA reduce-adds, and a convert kernel
+//      writes dq = bf16(scale * accumulator); the deterministic backward instead runs
+//      the query-stationary dQ kernel of attn_bwd_dq_sm103.cu (dQ accumulated in TMEM
+//      over the key tiles, written once).
 #include "sm103_ptx.cuh"
 #include "xattn_internal.h"
 
 namespace xattn {
 
-size_t bwd_workspace_bytes(int B, int S, int nh, int hd) {
+// Workspace: auxiliary rows | D | (fused dQ only) the fp32 dQ accumulator.
+size_t bwd_workspace_bytes(int B, int S, int nh, int hd, bool fused_dq) {
   auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
   const size_t rows = static_cast<size_t>(B) * nh * padded_rows(S);
-  return up(rows * kAuxCols * 2) + up(static_cast<size_t>(B) * S * nh * hd * 4);
+  const size_t base = up(rows * kAuxCols * 2) + up(static_cast<size_t>(B) * S * nh * 4);
+  return fused_dq ? base + up(static_cast<size_t>(B) * S * nh * hd * 4) : base;
 }
 
 BwdWorkspace bwd_workspace_carve(void *base, int B, int S, int nh, int hd) {
@@ -45,7 +47,8 @@ BwdWorkspace bwd_workspace_carve(void *base, int B, int S, int nh, int hd) {
   uint8_t *p = static_cast<uint8_t *>(base);
   BwdWorkspace ws;
   ws.aux = reinterpret_cast<__nv_bfloat16 *>(p);
-  ws.dqacc = reinterpret_cast<float *>(p + up(rows * kAuxCols * 2));
+  ws.D = reinterpret_cast<float *>(p + up(rows * kAuxCols * 2));
+  ws.dqacc = reinterpret_cast<float *>(p + up(rows * kAuxCols * 2) + up(static_cast<size_t>(B) * S * nh * 4));
   return ws;
 }
 
@@ -68,16 +71,17 @@ __device__ __forceinline__ void split3_bf16(float v, uint16_t out[3]) {
 
 // One group of (hd / 8) lanes per row (b, i, h): each lane reads 8 bf16 of O and dO
 // (16 B each), the group reduces with shuffles. Rows are enumerated in memory order of
-// O/dO, so the loads are fully coalesced. The same lanes zero the row of the dQ
-// accumulator, and the group's first lane writes the row's auxiliary operand: -LSE/scale
-// and -D, the two per-query terms that the main kernel's tensor-core products add to
-// S^T and dP^T. Pad rows (S <= i < S_pad) are all zero: their Q and dO rows are zero
-// too, so they contribute nothing whatever P is there.
+// O/dO, so the loads are fully coalesced. The same lanes zero the row of the fused dQ
+// accumulator when there is one (dqacc non-null). The group's first lane writes D_i in
+// fp32 (read by the dQ kernel, [B, S, nh] like lse) and the row's auxiliary operand:
+// -LSE/scale and -D, the two per-query terms that the dK/dV kernel's tensor-core
+// products add to S^T and dP^T. Pad rows (S <= i < S_pad) are all zero: their Q and dO
+// rows are zero too, so they contribute nothing whatever P is there.
 template <int HD>
 __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
     const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dO,
-    const float *__restrict__ lse, uint4 *__restrict__ aux, float *__restrict__ dqacc,
-    int B, int S, int nh, float lse_mult) {
+    const float *__restrict__ lse, uint4 *__restrict__ aux, float *__restrict__ D,
+    float *__restrict__ dqacc, int B, int S, int nh, float lse_mult) {
   constexpr int kLanesPerRow = HD / 8;
   const int S_pad = padded_rows(S);
   const long long n_rows = static_cast<long long>(B) * S * nh;
@@ -103,10 +107,13 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
 #pragma unroll
   for (int off = kLanesPerRow / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (is_row) {
-    float4 *z = reinterpret_cast<float4 *>(dqacc + row * HD + sub * 8);
-    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (dqacc != nullptr) {
+      float4 *z = reinterpret_cast<float4 *>(dqacc + row * HD + sub * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     if (sub == 0) {
+      D[row] = acc;
       const int h = static_cast<int>(row % nh);
       const long long bi = row / nh;
       const int i = static_cast<int>(bi % S);
@@ -130,41 +137,31 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
 }
 
 // ------------------------------------------------------------------------------------
-// 3. dq convert: 8 elements per thread (two 16-byte loads, one 16-byte store). The
-// accumulator holds dS K without the softmax scale.
-// ------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
-                                                         __nv_bfloat16 *__restrict__ dq,
-                                                         size_t n8, float scale) {
-  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n8) return;
-  const float4 a = reinterpret_cast<const float4 *>(acc)[2 * t];
-  const float4 c = reinterpret_cast<const float4 *>(acc)[2 * t + 1];
-  reinterpret_cast<uint4 *>(dq)[t] =
-      make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
-                 pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
-}
-
-// ------------------------------------------------------------------------------------
 // 2. main kernel
 // ------------------------------------------------------------------------------------
 // 12 warps. Registers are split evenly over the 4 SM sub-partitions (3 warps each), so
 // the per-thread limit is 65536 / 4 / 96 rounded down to the allocation granule.
 constexpr int kBwdThreads = 384;
-constexpr int kBwdStages = 3;      // Q / dO / LSE / D stages
 
-template <int HD>
+// kFusedDq: the kernel also computes dQ = dS K per iteration and adds it into the fp32
+// accumulator with TMA reduce-adds (the default backward). Without it the kernel writes
+// dK and dV only and the query-stationary dQ kernel produces dQ (the deterministic
+// backward); dS^T then stays in TMEM, so dK reads it there and the shared memory of the
+// dS tile and the dQ staging goes to a fourth Q / dO stage.
+template <int HD, bool kFusedDq>
 struct BwdLayout {
+  static constexpr int kStages = kFusedDq ? 3 : 4;                  // Q / dO / aux-row stages
   static constexpr uint32_t kRowBytes = HD * 2;
   static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
   static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kTileBytes;
-  static constexpr uint32_t kQ = kV + kTileBytes;                    // kBwdStages stages
-  static constexpr uint32_t kdO = kQ + kBwdStages * kTileBytes;      // kBwdStages stages
-  static constexpr uint32_t kdS = kdO + kBwdStages * kTileBytes;     // 128 x 128 bf16, 32 KB
-  // dQ staging for the TMA reduce-add: 2 head-dim halves x 128 rows of HD/2 floats,
-  // swizzled like the tensor map's box.
+  static constexpr uint32_t kQ = kV + kTileBytes;                    // kStages stages
+  static constexpr uint32_t kdO = kQ + kStages * kTileBytes;         // kStages stages
+  // Fused dQ only: the 128 x 128 bf16 dS tile (32 KB) and the dQ staging for the TMA
+  // reduce-add (2 head-dim halves x 128 rows of HD/2 floats, swizzled like the tensor
+  // map's box).
+  static constexpr uint32_t kdS = kdO + kStages * kTileBytes;
   static constexpr uint32_t kDqRowBytes = HD / 2 * 4;
   static constexpr uint32_t kDqHalfBytes = kTileRows * kDqRowBytes;
   static constexpr uint32_t kdQs = kdS + 32768;
@@ -172,10 +169,10 @@ struct BwdLayout {
   // two constant key-side tiles (ones under the LSE columns / under the D columns) and
   // the query-side rows of each stage.
   static constexpr uint32_t kAuxTileBytes = kTileRows * kAuxCols * 2;
-  static constexpr uint32_t kAuxA = kdQs + 2 * kDqHalfBytes;
-  static constexpr uint32_t kAuxB = kAuxA + 2 * kAuxTileBytes;      // kBwdStages stages
-  static constexpr int kNumBars = 20;
-  static constexpr uint32_t kBars = kAuxB + kBwdStages * kAuxTileBytes;
+  static constexpr uint32_t kAuxA = kFusedDq ? kdQs + 2 * kDqHalfBytes : kdS;
+  static constexpr uint32_t kAuxB = kAuxA + 2 * kAuxTileBytes;      // kStages stages
+  static constexpr int kNumBars = 1 + 2 * kStages + (kFusedDq ? 13 : 10);
+  static constexpr uint32_t kBars = kAuxB + kStages * kAuxTileBytes;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   static constexpr uint32_t kDynBytes = kUsed + 1024;
@@ -187,10 +184,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 }
 
 // Offset of element (key row j, query column i) of the 128 x 128 dS^T tile in shared
-// memory: two 64-column halves of 128-byte rows (one row per key) with the 128-byte
-// swizzle (16-byte chunk ^= row % 8). Read as the A operand of dQ = dS K it is
-// MN-major (M = query, contiguous); read as the A operand of dK = dS^T Q it is
-// K-major (M = key rows, K = query), so one copy serves both products.
+// memory (fused dQ): two 64-column halves of 128-byte rows (one row per key) with the
+// 128-byte swizzle (16-byte chunk ^= row % 8). Read as the A operand of dQ = dS K it is
+// MN-major (M = query, contiguous); read as the A operand of dK = dS^T Q it is K-major
+// (M = key rows, K = query), so one copy serves both products.
 __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
   return static_cast<uint32_t>((i >> 6) * 16384 + j * 128 + ((((i & 63) >> 3) ^ (j & 7)) << 4));
 }
@@ -198,22 +195,25 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
 // Role map (12 warps):
 //   warp 0     : TMA producer
 //   warp 1     : TMEM owner; MMA issuer of S^T and dV
-//   warp 2     : dQ reducer: TMA reduce-adds each staged dQ tile into the fp32
-//                accumulator (2 bulk operations per tile instead of scattered atomics)
-//   warp 3     : MMA issuer of dP^T, dK and dQ
+//   warp 2     : fused dQ: the dQ reducer, TMA reduce-adds of each staged dQ tile into
+//                the fp32 accumulator (2 bulk operations per tile instead of scattered
+//                atomics); otherwise idle
+//   warp 3     : MMA issuer of dP^T, dK (and dQ)
 //   warps 4-7  : P^T = exp2(S^T scale log2e), S^T already holding -LSE/scale, one
 //                thread per key row, all 128 query columns (the special-function work)
-//   warps 8-11 : dS^T = P^T (dP^T - D), one thread per key row (the FMA work), and the
-//                dQ drain (TMEM -> shared-memory staging, one query row per thread)
+//   warps 8-11 : dS^T = P^T (dP^T - D), dP^T already holding -D, one thread per key
+//                row (the FMA work); fused dQ: also the dQ drain (TMEM -> shared-memory
+//                staging, one query row per thread)
 // The two compute warpgroups work on consecutive (r, m) iterations at the same time, so
 // each SM sub-partition runs one warp of each and the exponentials of iteration t+1
 // overlap the dS arithmetic of iteration t.
 // TMEM columns: S^T [0,128) fp32 | dP^T [128,256) fp32 | P^T bf16 [256,320) |
-//               dV [320,384) | dK [384,448) | dQ [448,512)
+//               dV [320,384) | dK [384,448) | dQ fp32 (fused) or dS^T bf16 [448,512)
 // Each region has one producer and its readers release it with an mbarrier before it is
 // rewritten: S^T (s_free), dP^T (dp_free), P^T (p_free by the dS warps, dv_done by the
-// dV product), dQ (dq_empty).
-template <int HD>
+// dV product), dQ (dq_empty) or dS^T (dk_done).
+// mdq (fused dQ only): fp32 map over the dQ accumulator.
+template <int HD, bool kFusedDq>
 __global__ void __maxnreg__(168)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -221,7 +221,8 @@ __global__ void __maxnreg__(168)
                          __nv_bfloat16 *__restrict__ dk,
                          __nv_bfloat16 *__restrict__ dv, int B, int S, int nh, int nkv,
                          float scale, int *status, unsigned long long timeout_ns) {
-  using L = BwdLayout<HD>;
+  using L = BwdLayout<HD, kFusedDq>;
+  constexpr int kBwdStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -241,7 +242,7 @@ __global__ void __maxnreg__(168)
   const uint32_t sV = smem_u32(smem + L::kV);
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sdO = smem_u32(smem + L::kdO);
-  uint8_t *sdS_ptr = smem + L::kdS;
+  uint8_t *sdS_ptr = smem + L::kdS;          // fused dQ only
   const uint32_t sdS = smem_u32(sdS_ptr);
   uint8_t *sdQs_ptr = smem + L::kdQs;
   const uint32_t sAuxA = smem_u32(smem + L::kAuxA);
@@ -254,10 +255,13 @@ __global__ void __maxnreg__(168)
   const uint32_t kv_full = bar(0);
   auto full = [&](int s) { return bar(1 + s); };
   auto empty = [&](int s) { return bar(1 + kBwdStages + s); };
-  const uint32_t s_full = bar(7), s_free = bar(8), dp_full = bar(9), dp_free = bar(10);
-  const uint32_t p_full = bar(11), p_free = bar(12), dv_done = bar(13), ds_full = bar(14);
-  const uint32_t dq_full = bar(15), dq_empty = bar(16), dqs_full = bar(17), dqs_empty = bar(18);
-  const uint32_t acc_done = bar(19);
+  constexpr int kB = 1 + 2 * kBwdStages;
+  const uint32_t s_full = bar(kB + 0), s_free = bar(kB + 1), dp_full = bar(kB + 2), dp_free = bar(kB + 3);
+  const uint32_t p_full = bar(kB + 4), p_free = bar(kB + 5), dv_done = bar(kB + 6), ds_full = bar(kB + 7);
+  const uint32_t acc_done = bar(kB + 8);
+  const uint32_t dk_done = bar(kB + 9);                               // dK(t) read dS^T(t)
+  const uint32_t dq_full = bar(kB + 9), dq_empty = bar(kB + 10);      // fused dQ
+  const uint32_t dqs_full = bar(kB + 11), dqs_empty = bar(kB + 12);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -277,11 +281,15 @@ __global__ void __maxnreg__(168)
     mbar_init(p_free, 128);
     mbar_init(dv_done, 1);
     mbar_init(ds_full, 128);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_empty, 128);
-    mbar_init(dqs_full, 128);
-    mbar_init(dqs_empty, 1);
     mbar_init(acc_done, 2);
+    if constexpr (kFusedDq) {
+      mbar_init(dq_full, 1);
+      mbar_init(dq_empty, 128);
+      mbar_init(dqs_full, 128);
+      mbar_init(dqs_empty, 1);
+    } else {
+      mbar_init(dk_done, 1);
+    }
     fence_mbar_init();
   }
   // Constant key-side auxiliary tiles: row r = [1 1 1 0 ...] (S^T) and [0 0 0 1 1 1 0 ...]
@@ -301,7 +309,7 @@ __global__ void __maxnreg__(168)
     tma_prefetch_desc(&mv);
     tma_prefetch_desc(&mdo);
     tma_prefetch_desc(&maux);
-    tma_prefetch_desc(&mdq);
+    if constexpr (kFusedDq) tma_prefetch_desc(&mdq);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_holder), 512);
@@ -312,7 +320,8 @@ __global__ void __maxnreg__(168)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tdP = tmem + 128, tP = tmem + 256;
-  const uint32_t tdV = tmem + 320, tdK = tmem + 384, tdQ = tmem + 448;
+  const uint32_t tdV = tmem + 320, tdK = tmem + 384;
+  const uint32_t tdQ = tmem + 448, tdS = tmem + 448;   // fused dQ: dQ; otherwise dS^T
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
@@ -338,14 +347,14 @@ __global__ void __maxnreg__(168)
   } else if (warp == 1 || warp == 3) {
     // ---------------- MMA issuers (converged warps, one elected lane issues) ----------------
     // Warp 1 issues the products the P warps depend on (S^T, dV); warp 3 those of the dS
-    // warps (dP^T, dK, dQ). Each stream is in order, but neither waits behind the other,
-    // so S^T(t+1) never queues behind a dQ that is waiting for the dQ drain. The tensor
+    // warps (dP^T, dK, and dQ when fused). Each stream is in order, but neither waits
+    // behind the other, so S^T(t+1) never queues behind a dQ that is waiting for the dQ
+    // drain. The tensor
     // pipe takes the two streams' MMAs in arrival order; each stage is released by one
     // commit from each issuer (empty counts 2), and acc_done gets one from each.
     const bool p_side = warp == 1;
     constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
     constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A K-major)
-    constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);    // dQ (A = dS, MN-major)
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // stage stride, descriptor units
     constexpr uint32_t kRowStep = (16 * L::kRowBytes) >> 4;  // 16 rows of an MN-major tile
     // Descriptors are built once. K-major operands advance +32 bytes (+2) per
@@ -354,9 +363,10 @@ __global__ void __maxnreg__(168)
     const uint64_t kB_k = smem_desc(p_side ? sQ : sdO, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kQ_mn = smem_desc(sQ, 8192, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t kdO_mn = smem_desc(sdO, 8192, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kRowBytes, L::kSwizzle);
+    const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kRowBytes, L::kSwizzle);       // fused dQ
     const uint64_t kdS_mn = smem_desc(sdS, 16384, 1024, kSwizzle128);
     const uint64_t kdS_k = smem_desc(sdS, 16, 1024, kSwizzle128);
+    constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);  // dQ (A = dS, MN-major)
     const uint64_t kAuxA = smem_desc(sAuxA + (p_side ? 0u : L::kAuxTileBytes), 16, 256, kSwizzle32);
     const uint64_t kAuxQ = smem_desc(sAuxB, 16, 256, kSwizzle32);
     constexpr uint32_t kAuxStageDesc = L::kAuxTileBytes >> 4;
@@ -404,23 +414,32 @@ __global__ void __maxnreg__(168)
       } else {
         if (!warp_wait(ds_full, ph, ctl)) break;
         tc_fence_after();
+        if constexpr (kFusedDq) {
 #pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk)                          // dK += dS^T Q
-          mma_ss_elect(tdK, kdS_k + (kk >> 2) * 1024 + (kk & 3) * 2,
-                       kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(empty(s));                  // dP^T(t) and dK(t) are done with stage s
-        if (t > 0 && !warp_wait(dq_empty, ph ^ 1, ctl)) break;
-        tc_fence_after();
+          for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dK += dS^T Q
+            mma_ss_elect(tdK, kdS_k + (kk >> 2) * 1024 + (kk & 3) * 2,
+                         kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_elect(empty(s));                // dP^T(t) and dK(t) are done with stage s
+          if (t > 0 && !warp_wait(dq_empty, ph ^ 1, ctl)) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk)                          // dQ = dS K
-          mma_ss_elect(tdQ, kdS_mn + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
-        mma_commit_elect(dq_full);
+          for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dQ = dS K
+            mma_ss_elect(tdQ, kdS_mn + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
+          mma_commit_elect(dq_full);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dK += dS^T Q
+            mma_ts_elect(tdK, tdS + kk * 8, kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc,
+                         (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_elect(empty(s));                // dP^T(t) and dK(t) are done with stage s
+          mma_commit_elect(dk_done);
+        }
       }
       s = s1;
     }
     mma_commit_elect(acc_done);
     mbar_drain(acc_done, 0, ctl);
-  } else if (warp == 2) {
+  } else if (kFusedDq && warp == 2) {
     // ---------------- dQ reducer ----------------
     for (int k = 0; k < T; ++k) {
       if (!warp_wait(dqs_full, k & 1, ctl)) break;
@@ -515,13 +534,13 @@ __global__ void __maxnreg__(168)
       }
     }
   } else if (warp >= 8) {
-    // ---------------- dS^T and the dQ drain: one thread per key row j ----------------
+    // ---------------- dS^T (and the fused dQ drain): one thread per key row j ----------------
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // dQ(k) from TMEM (query row j of its tile) into the staging buffer, swizzled like
-    // the reduce's tensor-map box (two halves of HD/2 floats per row); warp 2 then adds
-    // it to global memory. The caller has waited for dq_full(k).
+    // Fused dQ: dQ(k) from TMEM (query row j of its tile) into the staging buffer,
+    // swizzled like the reduce's tensor-map box (two halves of HD/2 floats per row); warp
+    // 2 then adds it to global memory. The caller has waited for dq_full(k).
     auto drain_dq = [&](int k) -> bool {
       uint32_t v[HD];
 #pragma unroll
@@ -565,12 +584,14 @@ __global__ void __maxnreg__(168)
           tmem_ld_x32(tdP + lane_off + 32 * (c + 1), dn);
         }
         if (c == 0 && t > 0) {
-          // dK(t-1) and dQ(t-1) have finished reading the shared-memory dS tile.
-          if (!warp_wait(dq_full, (t - 1) & 1, ctl)) {
+          // The previous dS^T has been read: by dK(t-1) and dQ(t-1) from shared memory
+          // (fused dQ), or by dK(t-1) from TMEM.
+          if (!warp_wait(kFusedDq ? dq_full : dk_done, (t - 1) & 1, ctl)) {
             tmem_wait_ld();    // the loads of chunk 1 are still in flight
             ok = false;
             break;
           }
+          tc_fence_after();
         }
         uint32_t dsk[16];
 #pragma unroll
@@ -584,10 +605,14 @@ __global__ void __maxnreg__(168)
           dsk[2 * q4] = pack_bf16x2(t0, t1);
           dsk[2 * q4 + 1] = pack_bf16x2(t2, t3);
         }
+        if constexpr (kFusedDq) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, 32 * c + 8 * e)) =
-              make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
+          for (int e = 0; e < 4; ++e)
+            *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, 32 * c + 8 * e)) =
+                make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
+        } else {
+          tmem_st_x16(tdS + lane_off + 16 * c, dsk);
+        }
         if (c < 3) {
           tmem_wait_ld();
           reg_fence<16>(pn);
@@ -600,16 +625,24 @@ __global__ void __maxnreg__(168)
         }
       }
       if (!ok) break;
-      fence_proxy_async_smem();
-      mbar_arrive(ds_full);
-      if (t > 0 && !drain_dq(t - 1)) { ok = false; break; }
+      if constexpr (kFusedDq) {
+        fence_proxy_async_smem();
+        mbar_arrive(ds_full);
+        if (t > 0 && !drain_dq(t - 1)) { ok = false; break; }
+      } else {
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(ds_full);
+      }
     }
-    // Epilogue: the last dQ, then the dK rows (bf16, times the softmax scale).
-    if (ok && warp_wait(dq_full, (T - 1) & 1, ctl)) {
-      tc_fence_after();
-      ok = drain_dq(T - 1);
-    } else {
-      ok = false;
+    // Epilogue: the last dQ (fused), then the dK rows (bf16, times the softmax scale).
+    if constexpr (kFusedDq) {
+      if (ok && warp_wait(dq_full, (T - 1) & 1, ctl)) {
+        tc_fence_after();
+        ok = drain_dq(T - 1);
+      } else {
+        ok = false;
+      }
     }
     if (ok && warp_wait(acc_done, 0, ctl)) {
       tc_fence_after();
@@ -643,27 +676,42 @@ __global__ void __maxnreg__(168)
   }
 }
 
-template <int HD>
+template <int HD, bool kFusedDq>
 cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                           const CUtensorMap &mdo, const CUtensorMap &maux, const CUtensorMap &mdq, __nv_bfloat16 *dk,
-                           __nv_bfloat16 *dv, int B, int S, int nh, int nkv, float scale,
-                           int *status, uint64_t timeout_ns, cudaStream_t stream) {
-  using L = BwdLayout<HD>;
-  cudaError_t err = cudaFuncSetAttribute(attn_bwd_main_kernel<HD>,
+                           const CUtensorMap &mdo, const CUtensorMap &maux, const CUtensorMap &mdq,
+                           __nv_bfloat16 *dk, __nv_bfloat16 *dv, int B, int S, int nh, int nkv,
+                           float scale, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+  using L = BwdLayout<HD, kFusedDq>;
+  cudaError_t err = cudaFuncSetAttribute(attn_bwd_main_kernel<HD, kFusedDq>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
   if (err != cudaSuccess) return err;
   const int num_n = (S + kTileRows - 1) / kTileRows;
   const unsigned grid = static_cast<unsigned>(B) * nkv * num_n;
-  attn_bwd_main_kernel<HD><<<grid, kBwdThreads, L::kDynBytes, stream>>>(
+  attn_bwd_main_kernel<HD, kFusedDq><<<grid, kBwdThreads, L::kDynBytes, stream>>>(
       mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns);
   return cudaGetLastError();
+}
+
+// 3. dq convert (fused dQ): 8 elements per thread (two 16-byte loads, one 16-byte
+// store). The accumulator holds dS K without the softmax scale.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
+                                                         __nv_bfloat16 *__restrict__ dq,
+                                                         size_t n8, float scale) {
+  const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n8) return;
+  const float4 a = reinterpret_cast<const float4 *>(acc)[2 * t];
+  const float4 c = reinterpret_cast<const float4 *>(acc)[2 * t + 1];
+  reinterpret_cast<uint4 *>(dq)[t] =
+      make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                 pack_bf16x2(c.x * scale, c.y * scale), pack_bf16x2(c.z * scale, c.w * scale));
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dO,
                                   const float *lse, int B, int S, int nh, int hd, float scale,
-                                  const BwdWorkspace &ws, cudaStream_t stream) {
+                                  const BwdWorkspace &ws, bool fused_dq, cudaStream_t stream) {
+  float *dqacc = fused_dq ? ws.dqacc : nullptr;
   // -LSE/scale, or -LSE log2 e when scale == 0 (then the main kernel's S^T is the
   // auxiliary term alone and is used unscaled).
   const float lse_mult = (scale == 0.f) ? kLog2e : 1.0f / scale;
@@ -674,9 +722,9 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *d
   const long long threads = (n_rows + n_pad) * lanes;
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
   if (hd == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.dqacc, B, S, nh, lse_mult);
+    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.D, dqacc, B, S, nh, lse_mult);
   else if (hd == 32)
-    bwd_preprocess_kernel<32><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.dqacc, B, S, nh, lse_mult);
+    bwd_preprocess_kernel<32><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.D, dqacc, B, S, nh, lse_mult);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();
@@ -684,14 +732,19 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *d
 
 cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
                                  const CUtensorMap &mv, const CUtensorMap &mdo,
-                                 const CUtensorMap &maux, const CUtensorMap &mdq,
-                                 const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
+                                 const CUtensorMap &maux, const CUtensorMap *mdq,
+                                 __nv_bfloat16 *dk, __nv_bfloat16 *dv,
                                  int B, int S, int nh, int nkv, int hd, float scale, int *status,
                                  uint64_t timeout_ns, cudaStream_t stream) {
+  // Without a dQ accumulator map the kernel computes dK and dV only; its mdq parameter
+  // is then unused (maux stands in for it).
+  const CUtensorMap &md = mdq ? *mdq : maux;
   if (hd == 64)
-    return launch_main_hd<64>(mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return mdq ? launch_main_hd<64, true>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream)
+               : launch_main_hd<64, false>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
   if (hd == 32)
-    return launch_main_hd<32>(mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return mdq ? launch_main_hd<32, true>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream)
+               : launch_main_hd<32, false>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -163,7 +163,7 @@ xattn_status bf16_device(DeviceInfo **dev) {
 
 xattn_status check_workspace(void *ws, size_t bytes, int B, int S, int nh, int hd) {
   if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return XATTN_ERR_WORKSPACE;
-  if (bytes < bwd_workspace_bytes(B, S, nh, hd)) return XATTN_ERR_WORKSPACE;
+  if (bytes < bwd_workspace_bytes(B, S, nh, hd, true)) return XATTN_ERR_WORKSPACE;
   return XATTN_OK;
 }
 
@@ -193,7 +193,7 @@ xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S
 
 size_t xattn_bwd_workspace_bytes(int B, int S, int nh, int hd) {
   if (B <= 0 || S <= 0 || nh <= 0 || hd <= 0) return 0;
-  return bwd_workspace_bytes(B, S, nh, hd);
+  return bwd_workspace_bytes(B, S, nh, hd, true);
 }
 
 xattn_status xattn_bwd_preprocess(const void *o, const void *dO, const float *lse, int B, int S,
@@ -210,7 +210,7 @@ xattn_status xattn_bwd_preprocess(const void *o, const void *dO, const float *ls
   const BwdWorkspace ws = bwd_workspace_carve(workspace, B, S, nh, hd);
   return cuda_status(launch_bwd_preprocess(static_cast<const __nv_bfloat16 *>(o),
                                            static_cast<const __nv_bfloat16 *>(dO), lse, B, S, nh, hd,
-                                           scale, ws, static_cast<cudaStream_t>(stream)));
+                                           scale, ws, true, static_cast<cudaStream_t>(stream)));
 }
 
 xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const void *dO, int B,
@@ -235,7 +235,7 @@ xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const v
   CUtensorMap maux, mdq;
   XATTN_TRY(make_map_aux(&maux, ws.aux, B, S, nh));
   XATTN_TRY(make_map_dq(&mdq, ws.dqacc, B, S, nh, hd));
-  return cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, maux, mdq, ws, static_cast<__nv_bfloat16 *>(dk),
+  return cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, maux, &mdq, static_cast<__nv_bfloat16 *>(dk),
                                           static_cast<__nv_bfloat16 *>(dv), B, S, nh, nkv, hd, scale,
                                           dev->status, wait_limit_ns(),
                                           static_cast<cudaStream_t>(stream)));
@@ -269,13 +269,54 @@ xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *
   DeviceInfo *dev = nullptr;
   XATTN_TRY(bf16_device(&dev));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t bytes = bwd_workspace_bytes(B, S, nh, hd);
+  const size_t bytes = bwd_workspace_bytes(B, S, nh, hd, true);
   void *ws = nullptr;
   if (cudaMallocAsync(&ws, bytes, st) != cudaSuccess) return XATTN_ERR_CUDA;
   xattn_status r = xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, scale, ws, bytes, stream);
   if (r == XATTN_OK) r = xattn_bwd_main(q, k, v, dO, B, S, nh, nkv, hd, scale, dk, dv, ws, bytes, stream);
   if (r == XATTN_OK) r = xattn_bwd_dq_convert(B, S, nh, hd, scale, dq, ws, bytes, stream);
   const cudaError_t fe = cudaFreeAsync(ws, st);
+  if (r == XATTN_OK && fe != cudaSuccess) r = XATTN_ERR_CUDA;
+  return r;
+}
+
+xattn_status xattn_bwd_deterministic(const void *q, const void *k, const void *v, const void *o,
+                                     const void *dO, const float *lse, int B, int S, int nh,
+                                     int nkv, int hd, float scale, void *dq, void *dk, void *dv,
+                                     void *stream) {
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return XATTN_ERR_NULL_PTR;
+  XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
+  XATTN_TRY(check_bwd_scale(scale));
+  XATTN_TRY(check_bf16(hd));
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return XATTN_ERR_MISALIGNED;
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(bf16_device(&dev));
+  CUtensorMap mq, mk, mv, mdo;
+  XATTN_TRY(make_map(&mq, q, B, S, nh, hd));
+  XATTN_TRY(make_map(&mk, k, B, S, nkv, hd));
+  XATTN_TRY(make_map(&mv, v, B, S, nkv, hd));
+  XATTN_TRY(make_map(&mdo, dO, B, S, nh, hd));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t bytes = bwd_workspace_bytes(B, S, nh, hd, false);
+  void *base = nullptr;
+  if (cudaMallocAsync(&base, bytes, st) != cudaSuccess) return XATTN_ERR_CUDA;
+  const BwdWorkspace ws = bwd_workspace_carve(base, B, S, nh, hd);
+  CUtensorMap maux;
+  xattn_status r = make_map_aux(&maux, ws.aux, B, S, nh);
+  if (r == XATTN_OK)
+    r = cuda_status(launch_bwd_preprocess(static_cast<const __nv_bfloat16 *>(o),
+                                          static_cast<const __nv_bfloat16 *>(dO), lse, B, S, nh, hd,
+                                          scale, ws, false, st));
+  if (r == XATTN_OK)
+    r = cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, maux, nullptr, static_cast<__nv_bfloat16 *>(dk),
+                                         static_cast<__nv_bfloat16 *>(dv), B, S, nh, nkv, hd, scale,
+                                         dev->status, wait_limit_ns(), st));
+  if (r == XATTN_OK)
+    r = cuda_status(launch_bwd_dq_bf16(mq, mk, mv, mdo, lse, ws, static_cast<__nv_bfloat16 *>(dq), B, S,
+                                       nh, nkv, hd, scale, dev->status, wait_limit_ns(), st));
+  const cudaError_t fe = cudaFreeAsync(base, st);
   if (r == XATTN_OK && fe != cudaSuccess) r = XATTN_ERR_CUDA;
   return r;
 }

@@ -25,10 +25,12 @@ constexpr int kAuxCols = 16;
 
 struct BwdWorkspace {
   __nv_bfloat16 *aux;  // [B, nh, S_pad, kAuxCols]
-  float *dqacc;        // [B, S, nh, hd]  fp32 dQ accumulator (dS K, without the scale)
+  float *D;            // [B, S, nh]  D_i = dO_i . O_i in fp32
+  float *dqacc;        // [B, S, nh, hd]  fused dQ only: fp32 accumulator of dS K (no scale)
 };
 
-size_t bwd_workspace_bytes(int B, int S, int nh, int hd);
+// fused_dq: the workspace also holds the fp32 dQ accumulator (default backward).
+size_t bwd_workspace_bytes(int B, int S, int nh, int hd, bool fused_dq);
 BwdWorkspace bwd_workspace_carve(void *base, int B, int S, int nh, int hd);
 
 // bf16 tcgen05 path (hd in {32, 64}).
@@ -38,20 +40,28 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &mq, const CUtensorMap &mk, const 
 
 cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *dO,
                                   const float *lse, int B, int S, int nh, int hd, float scale,
-                                  const BwdWorkspace &ws, cudaStream_t stream);
+                                  const BwdWorkspace &ws, bool fused_dq, cudaStream_t stream);
 
-// maux: bf16 map over the auxiliary rows (box = 16 columns x 128 rows, 32-byte swizzle).
-// mdq: fp32 map over the dQ accumulator (box = half a head row x 128 rows), used for
-// TMA reduce-adds.
+// dK and dV (key-stationary), and with mdq non-null also dQ added into the fp32
+// accumulator. maux: bf16 map over the auxiliary rows (box = 16 columns x 128 rows,
+// 32-byte swizzle); mdq: fp32 map over the dQ accumulator (box = half a head row x 128
+// rows), used for TMA reduce-adds.
 cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
                                  const CUtensorMap &mv, const CUtensorMap &mdo,
-                                 const CUtensorMap &maux, const CUtensorMap &mdq,
-                                 const BwdWorkspace &ws, __nv_bfloat16 *dk, __nv_bfloat16 *dv,
+                                 const CUtensorMap &maux, const CUtensorMap *mdq,
+                                 __nv_bfloat16 *dk, __nv_bfloat16 *dv,
                                  int B, int S, int nh, int nkv, int hd, float scale, int *status,
                                  uint64_t timeout_ns, cudaStream_t stream);
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, size_t n_elems,
                               float scale, cudaStream_t stream);
+
+// dQ of the deterministic backward (query-stationary), written in bf16; lse is the
+// forward's [B, S, nh] output.
+cudaError_t launch_bwd_dq_bf16(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                               const CUtensorMap &mdo, const float *lse, const BwdWorkspace &ws,
+                               __nv_bfloat16 *dq, int B, int S, int nh, int nkv, int hd, float scale,
+                               int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // fp32 CUDA-core path (hd <= 128).
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,

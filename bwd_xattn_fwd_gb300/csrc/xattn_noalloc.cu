@@ -72,8 +72,8 @@ extern "C" xattn_status xattn_bwd_noalloc(const void *q, const void *k, const vo
   const xattn_status st = xattn::scratch_address(&scratch);
   if (st != XATTN_OK) return st;
   // The three steps rewrite every scratch byte they read (the preprocess writes every
-  // auxiliary row, pad rows included, and zeroes the dQ accumulator), so contents left by
-  // an earlier call never leak into this one.
+  // auxiliary row, pad rows included, and every D_i, and zeroes the dQ accumulator), so
+  // contents left by an earlier call never leak into this one.
   xattn_status r = xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, scale, scratch, need, stream);
   if (r == XATTN_OK)
     r = xattn_bwd_main(q, k, v, dO, B, S, nh, nkv, hd, scale, dk, dv, scratch, need, stream);

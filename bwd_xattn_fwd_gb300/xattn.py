@@ -63,6 +63,7 @@ _SIGS = {
     "xattn_bwd_preprocess": [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _sz, _vp],
     "xattn_bwd_main": [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _sz, _vp],
     "xattn_bwd_dq_convert": [_i, _i, _i, _i, _f, _vp, _vp, _sz, _vp],
+    "xattn_bwd_deterministic": [_vp] * 5 + [_vp] + [_i] * 5 + [_f] + [_vp] * 4,
     "xattn_fwd_f32": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp],
     "xattn_bwd_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp],
     "xattn_check_device_status": [_vp],
@@ -118,6 +119,12 @@ def xattn_fwd(q, k, v, B, S, nh, nkv, hd, scale, o, lse, stream=None):
 def xattn_bwd(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream=None):
     _call("xattn_bwd", _addr(q), _addr(k), _addr(v), _addr(o), _addr(dO), _addr(lse), B, S, nh,
           nkv, hd, scale, _addr(dq), _addr(dk), _addr(dv), _stream(stream))
+
+
+def xattn_bwd_deterministic(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream=None):
+    """xattn_bwd with a bit-reproducible dQ (query-stationary dQ recompute, no atomics)."""
+    _call("xattn_bwd_deterministic", _addr(q), _addr(k), _addr(v), _addr(o), _addr(dO), _addr(lse),
+          B, S, nh, nkv, hd, scale, _addr(dq), _addr(dk), _addr(dv), _stream(stream))
 
 
 def xattn_bwd_noalloc(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream=None):
@@ -194,14 +201,16 @@ def attention_fwd(q, k, v, scale=None, stream=None):
     return o, lse
 
 
-def attention_bwd(q, k, v, o, dO, lse, scale=None, stream=None):
-    """(dq, dk, dv) for the tensors of attention_fwd and the output gradient dO."""
+def attention_bwd(q, k, v, o, dO, lse, scale=None, stream=None, deterministic=False):
+    """(dq, dk, dv) for the tensors of attention_fwd and the output gradient dO.
+    deterministic (bf16): dQ bit-reproducible as well, at the cost of a second recompute."""
     import torch
     B, S, nh, nkv, hd = _dims(q, k)
     scale = float(hd ** -0.5 if scale is None else scale)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if q.dtype == torch.bfloat16:
-        xattn_bwd(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream)
+        fn = xattn_bwd_deterministic if deterministic else xattn_bwd
+        fn(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream)
     elif q.dtype == torch.float32:
         xattn_bwd_f32(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream)
     else:

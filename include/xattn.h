@@ -82,7 +82,7 @@ xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S
  * released with cudaFreeAsync on the same stream; nothing else is allocated.
  * dQ is accumulated across key tiles with fp32 reduce-adds whose order is not fixed,
  * so its last bits may vary from run to run; dK, dV, o and lse are bit-for-bit
- * reproducible.
+ * reproducible. xattn_bwd_deterministic gives a dQ that is reproducible too.
  */
 xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *o,
                        const void *dO, const float *lse, int B, int S, int nh, int nkv,
@@ -114,6 +114,21 @@ xattn_status xattn_bwd_main(const void *q, const void *k, const void *v, const v
                             void *dv, void *workspace, size_t workspace_bytes, void *stream);
 xattn_status xattn_bwd_dq_convert(int B, int S, int nh, int hd, float scale, void *dq,
                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward with a reproducible dQ: the same arguments, results and scale rule as
+ * xattn_bwd, but every output is bit-for-bit the same from run to run. dK and dV come
+ * from the same key-stationary recompute as in xattn_bwd (without dQ there); dQ comes
+ * from a query-stationary recompute that accumulates dQ_i = scale sum_j dS_ij k_j over
+ * the key tiles of its query tile in a fixed order, with no atomics (row T14's
+ * recompute, done a second time: 7 tensor-core products per tile pair instead of 5).
+ * Scratch (D and the recompute's operand rows) is taken with cudaMallocAsync on
+ * `stream` and released with cudaFreeAsync on the same stream.
+ */
+xattn_status xattn_bwd_deterministic(const void *q, const void *k, const void *v,
+                                     const void *o, const void *dO, const float *lse, int B,
+                                     int S, int nh, int nkv, int hd, float scale, void *dq,
+                                     void *dk, void *dv, void *stream);
 
 /*
  * xattn_bwd with no allocation at all. The pages have no counterpart: this entry point

@@ -24,14 +24,14 @@ def rel_err(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.abs(got - ref).max() / max(np.abs(ref).max(), 1e-4))
 
 
-def run_gpu(w: W.Workload, x: dict, device="cuda", scale=None):
+def run_gpu(w: W.Workload, x: dict, device="cuda", scale=None, deterministic=False):
     """Forward then backward through the C ABI (with the workload's scale unless one is
-    given). Returns float64 numpy outputs."""
+    given; the deterministic backward on request). Returns float64 numpy outputs."""
     from bwd_xattn_fwd_gb300 import xattn
     scale = w.scale if scale is None else scale
     q, k, v, dO = (x[n].to(device) for n in ("q", "k", "v", "dO"))
     o, lse = xattn.attention_fwd(q, k, v, scale)
-    dq, dk, dv = xattn.attention_bwd(q, k, v, o, dO, lse, scale)
+    dq, dk, dv = xattn.attention_bwd(q, k, v, o, dO, lse, scale, deterministic=deterministic)
     torch.cuda.synchronize()
     assert xattn.xattn_check_device_status() == 0
     return {n: W.as_f64(t) for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}

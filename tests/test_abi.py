@@ -103,9 +103,9 @@ def test_workspace_checks(lib):
     lib.xattn_bwd_workspace_bytes.restype = ctypes.c_size_t
     lib.xattn_bwd_workspace_bytes.argtypes = [ctypes.c_int] * 4
     n = lib.xattn_bwd_workspace_bytes(2, 200, 4, 64)
-    # Auxiliary rows padded to 256 (=2 tiles): 2*4*256 rows of 16 bf16; accumulator
-    # 2*200*4*64 fp32.
-    assert n == 2 * 4 * 256 * 16 * 2 + 2 * 200 * 4 * 64 * 4
+    # Auxiliary rows padded to 256 (=2 tiles): 2*4*256 rows of 16 bf16; D: 2*200*4 fp32;
+    # dQ accumulator: 2*200*4*64 fp32.
+    assert n == 2 * 4 * 256 * 16 * 2 + 2 * 200 * 4 * 4 + 2 * 200 * 4 * 64 * 4
     assert lib.xattn_bwd_workspace_bytes(0, 200, 4, 64) == 0
     f = lib.xattn_bwd_dq_convert
     f.restype = ctypes.c_int

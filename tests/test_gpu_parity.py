@@ -113,14 +113,56 @@ def test_gqa_equals_repeated_mha(dtype):
 
 
 def test_reproducible():
-    """O, LSE, dK and dV are bit-identical run to run; dQ (fp32 atomic accumulation
-    across key tiles) agrees within the bf16 tolerance."""
+    """O, LSE, dK and dV are bit-identical run to run; dQ (fp32 reduce-adds across key
+    tiles, in no fixed order) agrees within the bf16 tolerance."""
     w = W.WORKLOADS["gqa"].with_(B=2)
     x = W.make_inputs(w, seed=6)
     a, b = run_gpu(w, x), run_gpu(w, x)
     for name in ("o", "lse", "dk", "dv"):
         assert np.array_equal(a[name], b[name]), name
     assert np.abs(a["dq"] - b["dq"]).max() <= TOL_BF16 * np.abs(a["dq"]).max()
+
+
+DET_EDGE = [(1, 1, 2, 1, 64), (2, 77, 4, 2, 64), (2, 200, 6, 3, 32), (1, 513, 2, 2, 64)]
+
+
+@pytest.mark.parametrize("shape", DET_EDGE, ids=lambda s: "B%d_S%d_nh%d_nkv%d_hd%d" % s)
+def test_deterministic_edge_shapes(shape):
+    """The deterministic backward (query-stationary dQ recompute) against the oracle."""
+    B, S, nh, nkv, hd = shape
+    w = W.Workload("det", B, S, nh, nkv, hd, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=8)
+    compare(run_gpu(w, x, deterministic=True), oracle_full(w, x), "bf16", "det " + str(shape))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.3], ids=lambda s: "scale=%g" % s)
+def test_deterministic_scales(scale):
+    w = W.Workload("det", 2, 200, 4, 2, 64, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=7)
+    compare(run_gpu(w, x, scale=scale, deterministic=True), oracle_full(w, x, scale=scale), "bf16",
+            "det scale=%g" % scale)
+
+
+def test_deterministic_workload_units():
+    w = W.WORKLOADS["gqa"]
+    x = W.make_inputs(w)
+    out = run_gpu(w, x, deterministic=True)
+    for b, kvh in _units(w):
+        compare(gpu_unit(w, out, b, kvh), oracle_unit(w, x, b, kvh), "bf16", f"det gqa unit ({b}, {kvh})")
+
+
+def test_deterministic_is_bit_reproducible():
+    """Every output of the deterministic backward is bit-identical run to run, and its dK
+    and dV equal the default backward's (the same key-stationary recompute)."""
+    w = W.WORKLOADS["gqa"].with_(B=2)
+    x = W.make_inputs(w, seed=6)
+    a, b = run_gpu(w, x, deterministic=True), run_gpu(w, x, deterministic=True)
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(a[name], b[name]), name
+    c = run_gpu(w, x)
+    for name in ("dk", "dv"):
+        assert np.array_equal(a[name], c[name]), name
+    assert np.abs(a["dq"] - c["dq"]).max() <= TOL_BF16 * np.abs(c["dq"]).max()
 
 
 def test_stage_calls_match_bwd():

@@ -45,7 +45,7 @@ def test_noalloc_matches_bwd_on_two_calls_in_a_row():
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     from bwd_xattn_fwd_gb300 import xattn
-    B, S, nh, nkv, hd = 32, 1024, 12, 12, 64      # needs ~100 MB of scratch
+    B, S, nh, nkv, hd = 32, 1024, 12, 12, 64      # needs ~115 MB of scratch
     assert xattn.xattn_bwd_workspace_bytes(B, S, nh, hd) > xattn.NOALLOC_SCRATCH_BYTES
     # Small stand-in buffers: the call must refuse before it touches any of them.
     t = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
