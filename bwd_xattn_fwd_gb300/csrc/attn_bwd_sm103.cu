@@ -150,32 +150,42 @@ constexpr int kBwdThreads = 384;
 // dS tile and the dQ staging goes to a fourth Q / dO stage.
 template <int HD, bool kFusedDq>
 struct BwdLayout {
-  static constexpr int kStages = kFusedDq ? 3 : 4;                  // Q / dO / aux-row stages
+  // Two rings of query-tile operands, each sized by how long a stage is held: Q and the
+  // auxiliary rows are read until dK(t), at the very end of an iteration; dO only until
+  // dP^T(t) and dV(t).
+  static constexpr int kQStages = kFusedDq ? 3 : 4;                 // Q + auxiliary rows
+  static constexpr int kOStages = kFusedDq ? 2 : 4;                 // dO
   static constexpr uint32_t kRowBytes = HD * 2;
   static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
   static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kTileBytes;
-  static constexpr uint32_t kQ = kV + kTileBytes;                    // kStages stages
-  static constexpr uint32_t kdO = kQ + kStages * kTileBytes;         // kStages stages
-  // Fused dQ only: the 128 x 128 bf16 dS tile (32 KB) and the dQ staging for the TMA
-  // reduce-add (2 head-dim halves x 128 rows of HD/2 floats, swizzled like the tensor
-  // map's box).
-  static constexpr uint32_t kdS = kdO + kStages * kTileBytes;
+  static constexpr uint32_t kQ = kV + kTileBytes;                    // kQStages stages
+  static constexpr uint32_t kdO = kQ + kQStages * kTileBytes;        // kOStages stages
+  // Fused dQ only: two 128 x 128 bf16 dS tiles (32 KB each; iteration t uses tile t % 2,
+  // so dS(t+1) is written while dK(t) and dQ(t) still read dS(t)) and the dQ staging for
+  // the TMA reduce-add (2 head-dim halves x 128 rows of HD/2 floats, swizzled like the
+  // tensor map's box).
+  static constexpr uint32_t kdS = kdO + kOStages * kTileBytes;
+  static constexpr uint32_t kdSBytes = 32768;
   static constexpr uint32_t kDqRowBytes = HD / 2 * 4;
   static constexpr uint32_t kDqHalfBytes = kTileRows * kDqRowBytes;
-  static constexpr uint32_t kdQs = kdS + 32768;
-  // Auxiliary K step of S^T and dP^T (128 rows x 16 bf16, 32-byte swizzle, 4 KB each):
-  // two constant key-side tiles (ones under the LSE columns / under the D columns) and
-  // the query-side rows of each stage.
+  static constexpr uint32_t kdQs = kdS + 2 * kdSBytes;
+  // Auxiliary K step of S^T and dP^T: the key-side operand is constant (ones under the
+  // LSE columns, or under the D columns, of every row), so it is three 8-row x 16-byte
+  // core matrices read without swizzle and with a zero row-group stride: [1 1 1 0 ...],
+  // [0 0 0 1 1 1 0 0] and zeros. The query-side rows (128 x 16 bf16, 32-byte swizzle,
+  // 4 KB) come with each stage.
   static constexpr uint32_t kAuxTileBytes = kTileRows * kAuxCols * 2;
   static constexpr uint32_t kAuxA = kFusedDq ? kdQs + 2 * kDqHalfBytes : kdS;
-  static constexpr uint32_t kAuxB = kAuxA + 2 * kAuxTileBytes;      // kStages stages
-  static constexpr int kNumBars = 1 + 2 * kStages + (kFusedDq ? 13 : 10);
-  static constexpr uint32_t kBars = kAuxB + kStages * kAuxTileBytes;
+  static constexpr uint32_t kAuxB = kAuxA + 1024;                    // kQStages stages
+  static constexpr int kNumBars = 1 + 2 * (kQStages + kOStages) + (kFusedDq ? 13 : 10);
+  static constexpr uint32_t kBars = kAuxB + kQStages * kAuxTileBytes;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   static constexpr uint32_t kDynBytes = kUsed + 1024;
+  static_assert(kDynBytes <= 227 * 1024, "exceeds the opt-in shared memory of one CTA");
+  static_assert(kAuxB % 1024 == 0 && kdS % 1024 == 0, "tile alignment");
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
@@ -222,7 +232,7 @@ __global__ void __maxnreg__(168)
                          __nv_bfloat16 *__restrict__ dv, int B, int S, int nh, int nkv,
                          float scale, int *status, unsigned long long timeout_ns) {
   using L = BwdLayout<HD, kFusedDq>;
-  constexpr int kBwdStages = L::kStages;
+  constexpr int kQS = L::kQStages, kOS = L::kOStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -253,9 +263,11 @@ __global__ void __maxnreg__(168)
   const uint32_t bar0 = smem_u32(smem + L::kBars);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   const uint32_t kv_full = bar(0);
-  auto full = [&](int s) { return bar(1 + s); };
-  auto empty = [&](int s) { return bar(1 + kBwdStages + s); };
-  constexpr int kB = 1 + 2 * kBwdStages;
+  auto q_full = [&](int s) { return bar(1 + s); };
+  auto q_empty = [&](int s) { return bar(1 + kQS + s); };
+  auto o_full = [&](int s) { return bar(1 + 2 * kQS + s); };
+  auto o_empty = [&](int s) { return bar(1 + 2 * kQS + kOS + s); };
+  constexpr int kB = 1 + 2 * (kQS + kOS);
   const uint32_t s_full = bar(kB + 0), s_free = bar(kB + 1), dp_full = bar(kB + 2), dp_free = bar(kB + 3);
   const uint32_t p_full = bar(kB + 4), p_free = bar(kB + 5), dv_done = bar(kB + 6), ds_full = bar(kB + 7);
   const uint32_t acc_done = bar(kB + 8);
@@ -269,9 +281,13 @@ __global__ void __maxnreg__(168)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(kv_full, 1);
-    for (int s = 0; s < kBwdStages; ++s) {
-      mbar_init(full(s), 1);
-      mbar_init(empty(s), 2);                        // one commit from each MMA issuer
+    for (int s = 0; s < kQS; ++s) {
+      mbar_init(q_full(s), 1);
+      mbar_init(q_empty(s), 2);                      // one commit from each MMA issuer
+    }
+    for (int s = 0; s < kOS; ++s) {
+      mbar_init(o_full(s), 1);
+      mbar_init(o_empty(s), 2);
     }
     mbar_init(s_full, 1);
     mbar_init(s_free, 128);
@@ -292,15 +308,15 @@ __global__ void __maxnreg__(168)
     }
     fence_mbar_init();
   }
-  // Constant key-side auxiliary tiles: row r = [1 1 1 0 ...] (S^T) and [0 0 0 1 1 1 0 ...]
-  // (dP^T), stored with the 32-byte swizzle (16-byte chunk ^= (r >> 2) & 1).
-  for (int e = threadIdx.x; e < 2 * kTileRows * 2; e += kBwdThreads) {
-    const int tile = e / (2 * kTileRows), r = (e / 2) % kTileRows, ch = e % 2;
+  // Constant key-side auxiliary core matrices (8 rows of 16 bytes each): [1 1 1 0 0 0 0 0]
+  // (S^T), [0 0 0 1 1 1 0 0] (dP^T), zeros (the second 8 columns of the K step).
+  if (threadIdx.x < 24) {
+    const int cm = threadIdx.x / 8, r = threadIdx.x % 8;
     const uint32_t one = 0x3F80u;   // bf16 1.0
-    uint4 val = make_uint4(0u, 0u, 0u, 0u);
-    if (ch == 0) val = (tile == 0) ? make_uint4(one | (one << 16), one, 0u, 0u)
-                                   : make_uint4(0u, one << 16, one | (one << 16), 0u);
-    *reinterpret_cast<uint4 *>(smem + L::kAuxA + tile * L::kAuxTileBytes + r * 32 + ((ch ^ ((r >> 2) & 1)) << 4)) = val;
+    const uint4 val = (cm == 0) ? make_uint4(one | (one << 16), one, 0u, 0u)
+                    : (cm == 1) ? make_uint4(0u, one << 16, one | (one << 16), 0u)
+                                : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4 *>(smem + L::kAuxA + cm * 128 + r * 16) = val;
   }
   fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
@@ -328,22 +344,28 @@ __global__ void __maxnreg__(168)
     mbar_expect_tx_elect(kv_full, 2 * L::kTileBytes);
     tma_load_4d_elect(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
     tma_load_4d_elect(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
-    int issued = 0;
-    for (int t = 0, r = 0, m = n, s = 0, use = 0; t < T; ++t) {
+    int issued_q = 0, issued_o = 0;
+    for (int t = 0, r = 0, m = n, sq = 0, uq = 0, so = 0, uo = 0; t < T; ++t) {
       const int h = kvh * group + r;
-      if (!warp_wait(empty(s), (use & 1) ^ 1, ctl)) break;
-      mbar_expect_tx_elect(full(s), 2 * L::kTileBytes + L::kAuxTileBytes);
-      tma_load_4d_elect(sQ + s * L::kTileBytes, &mq, full(s), 0, h, m * kTileRows, b);
-      tma_load_4d_elect(sdO + s * L::kTileBytes, &mdo, full(s), 0, h, m * kTileRows, b);
-      tma_load_4d_elect(sAuxB + s * L::kAuxTileBytes, &maux, full(s), 0, m * kTileRows, h, b);
-      issued = t + 1;
+      if (!warp_wait(q_empty(sq), (uq & 1) ^ 1, ctl)) break;
+      mbar_expect_tx_elect(q_full(sq), L::kTileBytes + L::kAuxTileBytes);
+      tma_load_4d_elect(sQ + sq * L::kTileBytes, &mq, q_full(sq), 0, h, m * kTileRows, b);
+      tma_load_4d_elect(sAuxB + sq * L::kAuxTileBytes, &maux, q_full(sq), 0, m * kTileRows, h, b);
+      issued_q = t + 1;
+      if (!warp_wait(o_empty(so), (uo & 1) ^ 1, ctl)) break;
+      mbar_expect_tx_elect(o_full(so), L::kTileBytes);
+      tma_load_4d_elect(sdO + so * L::kTileBytes, &mdo, o_full(so), 0, h, m * kTileRows, b);
+      issued_o = t + 1;
       if (++m == num_m) { m = n; ++r; }
-      if (++s == kBwdStages) { s = 0; ++use; }
+      if (++sq == kQS) { sq = 0; ++uq; }
+      if (++so == kOS) { so = 0; ++uo; }
     }
     // Every load has landed before the CTA can exit (the consumers may have given up).
     mbar_drain(kv_full, 0, ctl);
-    for (int t = (issued > kBwdStages ? issued - kBwdStages : 0); t < issued; ++t)
-      mbar_drain(full(t % kBwdStages), (t / kBwdStages) & 1, ctl);
+    for (int t = (issued_q > kQS ? issued_q - kQS : 0); t < issued_q; ++t)
+      mbar_drain(q_full(t % kQS), (t / kQS) & 1, ctl);
+    for (int t = (issued_o > kOS ? issued_o - kOS : 0); t < issued_o; ++t)
+      mbar_drain(o_full(t % kOS), (t / kOS) & 1, ctl);
   } else if (warp == 1 || warp == 3) {
     // ---------------- MMA issuers (converged warps, one elected lane issues) ----------------
     // Warp 1 issues the products the P warps depend on (S^T, dV); warp 3 those of the dS
@@ -367,7 +389,8 @@ __global__ void __maxnreg__(168)
     const uint64_t kdS_mn = smem_desc(sdS, 16384, 1024, kSwizzle128);
     const uint64_t kdS_k = smem_desc(sdS, 16, 1024, kSwizzle128);
     constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);  // dQ (A = dS, MN-major)
-    const uint64_t kAuxA = smem_desc(sAuxA + (p_side ? 0u : L::kAuxTileBytes), 16, 256, kSwizzle32);
+    // No swizzle: LBO = the distance to the zero core matrix (second K chunk), SBO = 0.
+    const uint64_t kAuxA = p_side ? smem_desc(sAuxA, 256, 0, 0) : smem_desc(sAuxA + 128, 128, 0, 0);
     const uint64_t kAuxQ = smem_desc(sAuxB, 16, 256, kSwizzle32);
     constexpr uint32_t kAuxStageDesc = L::kAuxTileBytes >> 4;
     // S^T = K Q^T - LSE/scale (P side) or dP^T = V dO^T - D (dS side): the head-dim K
@@ -375,72 +398,88 @@ __global__ void __maxnreg__(168)
     // query-side terms). With scale == 0 S^T is the auxiliary term alone.
     const uint32_t tD = p_side ? tS : tdP;
     const bool with_qk = p_side ? qk : true;
-    auto issue_t = [&](int stage) {
+    // The score product of iteration u reads Q ring stage sq (Q, or only the auxiliary
+    // rows on the dS side) and, on the dS side, dO ring stage so.
+    auto issue_t = [&](int sq, int so) {
       if (with_qk) {
+        const uint64_t b_k = kB_k + (p_side ? sq : so) * kStageDesc;
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss_elect(tD, kA_k + 2 * kk, kB_k + stage * kStageDesc + 2 * kk, idesc_t, kk > 0);
+          mma_ss_elect(tD, kA_k + 2 * kk, b_k + 2 * kk, idesc_t, kk > 0);
       }
-      mma_ss_elect(tD, kAuxA, kAuxQ + stage * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
+      mma_ss_elect(tD, kAuxA, kAuxQ + sq * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
+    };
+    // Each issuer waits for the stages it reads, phase by phase: the P side for Q before
+    // S^T and for dO before dV, the dS side for both before dP^T.
+    auto wait_operands = [&](int u, int sq, int so) {
+      return warp_wait(q_full(sq), (u / kQS) & 1, ctl) &&
+             (p_side || warp_wait(o_full(so), (u / kOS) & 1, ctl));
     };
     const uint32_t t_full = p_side ? s_full : dp_full;    // this side's score product
     const uint32_t t_free = p_side ? s_free : dp_free;
-    bool ok = warp_wait(kv_full, 0, ctl) && warp_wait(full(0), 0, ctl);
+    bool ok = warp_wait(kv_full, 0, ctl) && wait_operands(0, 0, 0);
     if (ok) {
       tc_fence_after();
-      issue_t(0);
+      issue_t(0, 0);
       mma_commit_elect(t_full);
+      if (!p_side) mma_commit_elect(o_empty(0));     // dP^T(0) is the dS side's last dO read
     }
-    for (int t = 0, s = 0; ok && t < T; ++t) {
-      const int s1 = (s + 1 == kBwdStages) ? 0 : s + 1;
+    for (int t = 0, sq = 0, so = 0; ok && t < T; ++t) {
+      const int sq1 = (sq + 1 == kQS) ? 0 : sq + 1;
+      const int so1 = (so + 1 == kOS) ? 0 : so + 1;
       const bool more = t + 1 < T;
       const uint32_t ph = t & 1;
       if (more) {
         // The next score product as soon as this side's warps have read the current one.
-        if (!warp_wait(full(s1), ((t + 1) / kBwdStages) & 1, ctl) || !warp_wait(t_free, ph, ctl)) break;
+        if (!wait_operands(t + 1, sq1, so1) || !warp_wait(t_free, ph, ctl)) break;
         tc_fence_after();
-        issue_t(s1);
+        issue_t(sq1, so1);
         mma_commit_elect(t_full);
+        if (!p_side) mma_commit_elect(o_empty(so1));
       }
       if (p_side) {
-        if (!warp_wait(p_full, ph, ctl)) break;
+        if (!warp_wait(o_full(so), (t / kOS) & 1, ctl) || !warp_wait(p_full, ph, ctl)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)                          // dV += P^T dO
-          mma_ts_elect(tdV, tP + kk * 8, kdO_mn + s * kStageDesc + kk * kRowStep, idesc_acc,
+          mma_ts_elect(tdV, tP + kk * 8, kdO_mn + so * kStageDesc + kk * kRowStep, idesc_acc,
                        (t > 0 || kk > 0) ? 1u : 0u);
         mma_commit_elect(dv_done);
-        mma_commit_elect(empty(s));                  // S^T(t) and dV(t) are done with stage s
+        mma_commit_elect(q_empty(sq));               // S^T(t) and dV(t) are done with both stages
+        mma_commit_elect(o_empty(so));
       } else {
         if (!warp_wait(ds_full, ph, ctl)) break;
         tc_fence_after();
         if constexpr (kFusedDq) {
+          const uint32_t dsb = (t & 1) * (L::kdSBytes >> 4);                 // dS tile t % 2
 #pragma unroll
           for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dK += dS^T Q
-            mma_ss_elect(tdK, kdS_k + (kk >> 2) * 1024 + (kk & 3) * 2,
-                         kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_elect(empty(s));                // dP^T(t) and dK(t) are done with stage s
+            mma_ss_elect(tdK, kdS_k + dsb + (kk >> 2) * 1024 + (kk & 3) * 2,
+                         kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_elect(q_empty(sq));             // dP^T(t) and dK(t) are done with the Q stage
           if (t > 0 && !warp_wait(dq_empty, ph ^ 1, ctl)) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dQ = dS K
-            mma_ss_elect(tdQ, kdS_mn + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
+            mma_ss_elect(tdQ, kdS_mn + dsb + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
           mma_commit_elect(dq_full);
         } else {
 #pragma unroll
           for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dK += dS^T Q
-            mma_ts_elect(tdK, tdS + kk * 8, kQ_mn + s * kStageDesc + kk * kRowStep, idesc_acc,
+            mma_ts_elect(tdK, tdS + kk * 8, kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc,
                          (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_elect(empty(s));                // dP^T(t) and dK(t) are done with stage s
+          mma_commit_elect(q_empty(sq));             // dP^T(t) and dK(t) are done with the Q stage
           mma_commit_elect(dk_done);
         }
       }
-      s = s1;
+      sq = sq1;
+      so = so1;
     }
     mma_commit_elect(acc_done);
     mbar_drain(acc_done, 0, ctl);
   } else if (kFusedDq && warp == 2) {
     // ---------------- dQ reducer ----------------
+    // Both head-dim halves of a staged tile are issued before one wait for their reads.
     for (int k = 0; k < T; ++k) {
       if (!warp_wait(dqs_full, k & 1, ctl)) break;
       if (lane == 0) {
@@ -540,8 +579,11 @@ __global__ void __maxnreg__(168)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     // Fused dQ: dQ(k) from TMEM (query row j of its tile) into the staging buffer,
     // swizzled like the reduce's tensor-map box (two halves of HD/2 floats per row); warp
-    // 2 then adds it to global memory. The caller has waited for dq_full(k).
+    // 2 then adds it to global memory. The phases of dq_full are waited in order, one per
+    // call: dQ(k+1) is only issued after this call has read dQ(k) (dq_empty).
     auto drain_dq = [&](int k) -> bool {
+      if (!warp_wait(dq_full, k & 1, ctl)) return false;
+      tc_fence_after();
       uint32_t v[HD];
 #pragma unroll
       for (int c = 0; c < HD; c += 32) tmem_ld_x32(tdQ + lane_off + c, v + c);
@@ -583,10 +625,11 @@ __global__ void __maxnreg__(168)
           tmem_ld_x16(tP + lane_off + 16 * (c + 1), pn);
           tmem_ld_x32(tdP + lane_off + 32 * (c + 1), dn);
         }
-        if (c == 0 && t > 0) {
-          // The previous dS^T has been read: by dK(t-1) and dQ(t-1) from shared memory
-          // (fused dQ), or by dK(t-1) from TMEM.
-          if (!warp_wait(kFusedDq ? dq_full : dk_done, (t - 1) & 1, ctl)) {
+        // The dS^T buffer about to be written has been read. Fused dQ: tile t % 2 was last
+        // read by dK(t-2) and dQ(t-2), which completed before the drain of dQ(t-2) in the
+        // previous iteration. Otherwise dK(t-1) read dS^T(t-1) from TMEM.
+        if (!kFusedDq && c == 0 && t > 0) {
+          if (!warp_wait(dk_done, (t - 1) & 1, ctl)) {
             tmem_wait_ld();    // the loads of chunk 1 are still in flight
             ok = false;
             break;
@@ -608,7 +651,7 @@ __global__ void __maxnreg__(168)
         if constexpr (kFusedDq) {
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4 *>(sdS_ptr + ds_offset(j, 32 * c + 8 * e)) =
+            *reinterpret_cast<uint4 *>(sdS_ptr + (t & 1) * L::kdSBytes + ds_offset(j, 32 * c + 8 * e)) =
                 make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
         } else {
           tmem_st_x16(tdS + lane_off + 16 * c, dsk);
@@ -636,14 +679,7 @@ __global__ void __maxnreg__(168)
       }
     }
     // Epilogue: the last dQ (fused), then the dK rows (bf16, times the softmax scale).
-    if constexpr (kFusedDq) {
-      if (ok && warp_wait(dq_full, (T - 1) & 1, ctl)) {
-        tc_fence_after();
-        ok = drain_dq(T - 1);
-      } else {
-        ok = false;
-      }
-    }
+    if constexpr (kFusedDq) ok = ok && drain_dq(T - 1);
     if (ok && warp_wait(acc_done, 0, ctl)) {
       tc_fence_after();
       const int jg = n * kTileRows + j;
