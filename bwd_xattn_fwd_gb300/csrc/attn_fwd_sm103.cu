@@ -233,29 +233,33 @@ __global__ void __maxnreg__(168)
       if (!warp_wait(s_full(x), n & 1, ctl)) { ok = false; break; }
       tc_fence_after();
       const bool diag = (n == mX);
-      // Pass 1: the row maximum of the scaled scores, 64 columns at a time: the scaled
-      // maximum of the raw scores (scale >= 0) or their scaled minimum (scale < 0).
+      // The whole row of S_X(n) comes into registers with one TMEM read, and the buffer
+      // is released at once: S_X(n+1) is computed while this softmax runs.
+      uint32_t r[128];
+#pragma unroll
+      for (int c = 0; c < 128; c += 32) tmem_ld_x32(tSx + c, r + c);
+      tmem_wait_ld();
+      reg_fence<128>(r);
+      tc_fence_before();
+      mbar_arrive(s_free(x));
+      // The row maximum of the scaled scores: the scaled maximum of the raw scores
+      // (scale >= 0) or their scaled minimum (scale < 0); masked columns do not count.
       constexpr float kFill = kNegScale ? INFINITY : -INFINITY;
       float mx4[4] = {kFill, kFill, kFill, kFill};
-#pragma unroll 1
-      for (int c64 = 0; c64 < 128; c64 += 64) {
-        uint32_t r[64];
-        tmem_ld_x32(tSx + c64, r);
-        tmem_ld_x32(tSx + c64 + 32, r + 32);
-        tmem_wait_ld();
-        reg_fence<64>(r);
-        if (diag) {
+      auto maxpass = [&](auto masked) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c64 + c > row) r[c] = __float_as_uint(kFill);
-        }
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
+        for (int c = 0; c < 128; c += 2) {
+          float v0 = __uint_as_float(r[c]), v1 = __uint_as_float(r[c + 1]);
+          if (decltype(masked)::value) {
+            if (c > row) v0 = kFill;
+            if (c + 1 > row) v1 = kFill;
+          }
           float &a = mx4[(c >> 1) & 3];
-          a = kNegScale ? fmin3(a, __uint_as_float(r[c]), __uint_as_float(r[c + 1]))
-                        : fmax3(a, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+          a = kNegScale ? fmin3(a, v0, v1) : fmax3(a, v0, v1);
         }
-      }
+      };
+      if (diag) maxpass(std::true_type{});
+      else maxpass(std::false_type{});
       const float mx = (kNegScale ? fmin3(mx4[0], mx4[1], fminf(mx4[2], mx4[3]))
                                   : fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]))) * scale_log2;
       // Conditional rescaling: keep the stale max unless some row of the warp grew by
@@ -271,44 +275,34 @@ __global__ void __maxnreg__(168)
         if (!warp_wait(o_done(x), (n - 1) & 1, ctl)) { ok = false; break; }
         tc_fence_after();
       }
-      // Pass 2: exponentials, row sum and bf16 P, 64 columns at a time.
+      // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
+      // included), the exponentials, row sums and bf16 P, 32 columns at a time. The
+      // diagonal tile has its own copy of the body, so the common one is branch-free.
       float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int c64 = 0; c64 < 128; c64 += 64) {
-        uint32_t r[64];
-        tmem_ld_x32(tSx + c64, r);
-        tmem_ld_x32(tSx + c64 + 32, r + 32);
-        tmem_wait_ld();
-        reg_fence<64>(r);
-        if (c64 == 64) {                   // S_X(n) fully read: its buffer may be refilled
-          tc_fence_before();
-          mbar_arrive(s_free(x));
-        }
-        // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
-        // included), the exponentials, row sums and bf16 P. The diagonal tile has its own
-        // copy of the body, so the common one is a single branch-free block.
-        uint32_t pk[32];
-        auto body = [&](auto masked) {
+      auto body = [&](auto masked) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
+        for (int c32 = 0; c32 < 128; c32 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c32 + 2 * e;
             float x0, x1;
-            ffma2(x0, x1, __uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]), scale_log2,
-                  scale_log2, neg_m, neg_m);
+            ffma2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), scale_log2, scale_log2,
+                  neg_m, neg_m);
             if (decltype(masked)::value) {
-              if (c64 + 2 * e > row) x0 = -INFINITY;
-              if (c64 + 2 * e + 1 > row) x1 = -INFINITY;
+              if (c > row) x0 = -INFINITY;
+              if (c + 1 > row) x1 = -INFINITY;
             }
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             const int a = (e & 1) * 2;
             fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
             pk[e] = pack_bf16x2(p0, p1);
           }
-        };
-        if (diag) body(std::true_type{});
-        else body(std::false_type{});
-        tmem_st_x16(tPx + c64 / 2, pk);
-        tmem_st_x16(tPx + c64 / 2 + 16, pk + 16);
-      }
+          tmem_st_x16(tPx + c32 / 2, pk);
+        }
+      };
+      if (diag) body(std::true_type{});
+      else body(std::false_type{});
       if (rescale && n > 0) {
 #pragma unroll
         for (int c = 0; c < HD; c += 32) {
