@@ -8,12 +8,12 @@
 // Three kernels, in stream order:
 //   1. preprocess (HBM-bound): D_i = sum_d dO_id O_id in fp32, and per query row the
 //      bf16 auxiliary operand row holding -LSE_i/scale and -D_i.
-//   2. main, this file (tensor cores): dK and dV. One CTA per (batch, kv head, 128-row
-//      key tile n). The K_n and V_n tiles stay in shared memory; the dK_n / dV_n
-//      accumulators stay in TMEM while the CTA walks every query head r of the group and
-//      every query tile m >= n (causal tile skipping). That walk *is* the group sum of
-//      row T15: no atomics on dK/dV, and a fixed order, so they are reproducible. Per
-//      (r, m):
+//   2. main, this file (tensor cores): dK and dV. A unit of work is one (batch, kv head,
+//      128-row key tile n); persistent CTAs, one per SM, take the units in turn. The K_n
+//      and V_n tiles stay in shared memory; the dK_n / dV_n accumulators stay in TMEM
+//      while the CTA walks every query head r of the group and every query tile m >= n
+//      (causal tile skipping). That walk *is* the group sum of row T15: no atomics on
+//      dK/dV, and a fixed order, so they are reproducible. Per (r, m):
 //        S^T  = K_n Q_m^T - LSE/scale   (TMEM, 128 x 128 fp32; the per-query term is one
 //        dP^T = V_n dO_m^T - D          extra tensor-core K step over the auxiliary rows)
 //        P^T  = exp2(S^T scale log2e)               -> bf16 into TMEM
@@ -179,7 +179,7 @@ struct BwdLayout {
   static constexpr uint32_t kAuxTileBytes = kTileRows * kAuxCols * 2;
   static constexpr uint32_t kAuxA = kFusedDq ? kdQs + 2 * kDqHalfBytes : kdS;
   static constexpr uint32_t kAuxB = kAuxA + 1024;                    // kQStages stages
-  static constexpr int kNumBars = 1 + 2 * (kQStages + kOStages) + (kFusedDq ? 13 : 10);
+  static constexpr int kNumBars = 1 + 2 * (kQStages + kOStages) + (kFusedDq ? 14 : 11);
   static constexpr uint32_t kBars = kAuxB + kQStages * kAuxTileBytes;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
@@ -236,17 +236,27 @@ __global__ void __maxnreg__(168)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Warp-uniform by construction; the broadcast lets the compiler see it.
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
 
-  // Unit of this CTA: key tile n (most work first), batch b, kv head kvh.
+  // Work units (key tile n, batch b, kv head kvh) are numbered most work first (n
+  // ascending). The CTAs are persistent: CTA c of G takes unit k G + c in even rounds k
+  // and k G + G - 1 - c in odd ones, which evens out the CTAs' total work. Every role
+  // walks the same units; the barriers' phases count iterations over all of them.
   const int num_m = (S + kTileRows - 1) / kTileRows;
   const int BK = B * nkv;
-  const int n = static_cast<int>(blockIdx.x) / BK;
-  const int bk = static_cast<int>(blockIdx.x) % BK;
-  const int b = bk / nkv, kvh = bk % nkv;
   const int group = nh / nkv;
-  const int per_head = num_m - n;         // query tiles m = n .. num_m-1
-  const int T = group * per_head;         // iterations (r, m)
+  const int num_units = num_m * BK;
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  auto unit_at = [&](int k) { return k * G + ((k & 1) ? G - 1 - cta : cta); };
+  int n = 0, b = 0, kvh = 0, per_head = 0, T = 0;
+  auto set_unit = [&](int u) {
+    n = u / BK;
+    b = (u % BK) / nkv;
+    kvh = u % nkv;
+    per_head = num_m - n;                 // query tiles m = n .. num_m-1
+    T = group * per_head;                 // iterations (r, m)
+  };
 
   const uint32_t sK = smem_u32(smem + L::kK);
   const uint32_t sV = smem_u32(smem + L::kV);
@@ -270,10 +280,11 @@ __global__ void __maxnreg__(168)
   constexpr int kB = 1 + 2 * (kQS + kOS);
   const uint32_t s_full = bar(kB + 0), s_free = bar(kB + 1), dp_full = bar(kB + 2), dp_free = bar(kB + 3);
   const uint32_t p_full = bar(kB + 4), p_free = bar(kB + 5), dv_done = bar(kB + 6), ds_full = bar(kB + 7);
-  const uint32_t acc_done = bar(kB + 8);
-  const uint32_t dk_done = bar(kB + 9);                               // dK(t) read dS^T(t)
-  const uint32_t dq_full = bar(kB + 9), dq_empty = bar(kB + 10);      // fused dQ
-  const uint32_t dqs_full = bar(kB + 11), dqs_empty = bar(kB + 12);
+  const uint32_t acc_done = bar(kB + 8);     // a unit's products are done
+  const uint32_t acc_free = bar(kB + 9);     // its epilogue has read dV and dK
+  const uint32_t dk_done = bar(kB + 10);                              // dK(t) read dS^T(t)
+  const uint32_t dq_full = bar(kB + 10), dq_empty = bar(kB + 11);     // fused dQ
+  const uint32_t dqs_full = bar(kB + 12), dqs_empty = bar(kB + 13);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -298,6 +309,7 @@ __global__ void __maxnreg__(168)
     mbar_init(dv_done, 1);
     mbar_init(ds_full, 128);
     mbar_init(acc_done, 2);
+    mbar_init(acc_free, 256);
     if constexpr (kFusedDq) {
       mbar_init(dq_full, 1);
       mbar_init(dq_empty, 128);
@@ -334,34 +346,53 @@ __global__ void __maxnreg__(168)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
   const uint32_t tS = tmem, tdP = tmem + 128, tP = tmem + 256;
   const uint32_t tdV = tmem + 320, tdK = tmem + 384;
   const uint32_t tdQ = tmem + 448, tdS = tmem + 448;   // fused dQ: dQ; otherwise dS^T
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
-    mbar_expect_tx_elect(kv_full, 2 * L::kTileBytes);
-    tma_load_4d_elect(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
-    tma_load_4d_elect(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
-    int issued_q = 0, issued_o = 0;
-    for (int t = 0, r = 0, m = n, sq = 0, uq = 0, so = 0, uo = 0; t < T; ++t) {
-      const int h = kvh * group + r;
-      if (!warp_wait(q_empty(sq), (uq & 1) ^ 1, ctl)) break;
+    // The Q / dO rings run on across units. A unit's first kOStages ring loads only need
+    // stages released by earlier iterations, so they are issued before waiting for the
+    // previous unit's products (acc_done): only then are K and V overwritten. (Waits for
+    // the phase before the first -- parity 1 of a fresh barrier -- return at once, so
+    // the first unit and iteration need no special case in any role.)
+    int issued_q = 0, issued_o = 0, units = 0;
+    int g = 0, sq = 0, uq = 0, so = 0, uo = 0;
+    auto load_ring = [&](int t) -> bool {
+      const int h = kvh * group + t / per_head, m = n + t % per_head;
+      if (!warp_wait(q_empty(sq), (uq & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(q_full(sq), L::kTileBytes + L::kAuxTileBytes);
       tma_load_4d_elect(sQ + sq * L::kTileBytes, &mq, q_full(sq), 0, h, m * kTileRows, b);
       tma_load_4d_elect(sAuxB + sq * L::kAuxTileBytes, &maux, q_full(sq), 0, m * kTileRows, h, b);
-      issued_q = t + 1;
-      if (!warp_wait(o_empty(so), (uo & 1) ^ 1, ctl)) break;
+      issued_q = g + 1;
+      if (!warp_wait(o_empty(so), (uo & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(o_full(so), L::kTileBytes);
       tma_load_4d_elect(sdO + so * L::kTileBytes, &mdo, o_full(so), 0, h, m * kTileRows, b);
-      issued_o = t + 1;
-      if (++m == num_m) { m = n; ++r; }
+      issued_o = g + 1;
+      ++g;
       if (++sq == kQS) { sq = 0; ++uq; }
       if (++so == kOS) { so = 0; ++uo; }
+      return true;
+    };
+    bool ok = true;
+#pragma unroll 1
+    for (int k = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      set_unit(u);
+      const int pre = T < kOS ? T : kOS;
+      for (int t = 0; ok && t < pre; ++t) ok = load_ring(t);
+      if (!ok || !warp_wait(acc_done, (units - 1) & 1, ctl)) break;
+      mbar_expect_tx_elect(kv_full, 2 * L::kTileBytes);
+      tma_load_4d_elect(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
+      tma_load_4d_elect(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
+      ++units;
+      for (int t = pre; ok && t < T; ++t) ok = load_ring(t);
     }
     // Every load has landed before the CTA can exit (the consumers may have given up).
-    mbar_drain(kv_full, 0, ctl);
+    if (units > 0) mbar_drain(kv_full, (units - 1) & 1, ctl);
     for (int t = (issued_q > kQS ? issued_q - kQS : 0); t < issued_q; ++t)
       mbar_drain(q_full(t % kQS), (t / kQS) & 1, ctl);
     for (int t = (issued_o > kOS ? issued_o - kOS : 0); t < issued_o; ++t)
@@ -400,14 +431,22 @@ __global__ void __maxnreg__(168)
     const bool with_qk = p_side ? qk : true;
     // The score product of iteration u reads Q ring stage sq (Q, or only the auxiliary
     // rows on the dS side) and, on the dS side, dO ring stage so.
+    const uint32_t t_full = p_side ? s_full : dp_full;    // this side's score product
+    const uint32_t t_free = p_side ? s_free : dp_free;
+    // Each product's MMAs and commits are issued by one elected lane; the warp then
+    // reconverges.
     auto issue_t = [&](int sq, int so) {
-      if (with_qk) {
-        const uint64_t b_k = kB_k + (p_side ? sq : so) * kStageDesc;
+      if (elect_one()) {
+        if (with_qk) {
+          const uint64_t b_k = kB_k + (p_side ? sq : so) * kStageDesc;
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss_elect(tD, kA_k + 2 * kk, b_k + 2 * kk, idesc_t, kk > 0);
+          for (int kk = 0; kk < HD / 16; ++kk) mma_ss(tD, kA_k + 2 * kk, b_k + 2 * kk, idesc_t, kk > 0);
+        }
+        mma_ss(tD, kAuxA, kAuxQ + sq * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
+        mma_commit(t_full);
+        if (!p_side) mma_commit(o_empty(so));        // dP^T is the dS side's last dO read
       }
-      mma_ss_elect(tD, kAuxA, kAuxQ + sq * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
+      __syncwarp();
     };
     // Each issuer waits for the stages it reads, phase by phase: the P side for Q before
     // S^T and for dO before dV, the dS side for both before dP^T.
@@ -415,83 +454,114 @@ __global__ void __maxnreg__(168)
       return warp_wait(q_full(sq), (u / kQS) & 1, ctl) &&
              (p_side || warp_wait(o_full(so), (u / kOS) & 1, ctl));
     };
-    const uint32_t t_full = p_side ? s_full : dp_full;    // this side's score product
-    const uint32_t t_free = p_side ? s_free : dp_free;
-    bool ok = warp_wait(kv_full, 0, ctl) && wait_operands(0, 0, 0);
-    if (ok) {
+    bool ok = true;
+    int units = 0;
+#pragma unroll 1
+    for (int k = 0, g = 0, sq = 0, so = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      set_unit(u);
+      // The unit's first score product: K and V have landed, and this side's warps have
+      // read the previous score tile (the last one of the previous unit).
+      ok = warp_wait(kv_full, units & 1, ctl) && wait_operands(g, sq, so) &&
+           warp_wait(t_free, (g - 1) & 1, ctl);
+      if (!ok) break;
       tc_fence_after();
-      issue_t(0, 0);
-      mma_commit_elect(t_full);
-      if (!p_side) mma_commit_elect(o_empty(0));     // dP^T(0) is the dS side's last dO read
-    }
-    for (int t = 0, sq = 0, so = 0; ok && t < T; ++t) {
-      const int sq1 = (sq + 1 == kQS) ? 0 : sq + 1;
-      const int so1 = (so + 1 == kOS) ? 0 : so + 1;
-      const bool more = t + 1 < T;
-      const uint32_t ph = t & 1;
-      if (more) {
-        // The next score product as soon as this side's warps have read the current one.
-        if (!wait_operands(t + 1, sq1, so1) || !warp_wait(t_free, ph, ctl)) break;
-        tc_fence_after();
-        issue_t(sq1, so1);
-        mma_commit_elect(t_full);
-        if (!p_side) mma_commit_elect(o_empty(so1));
-      }
-      if (p_side) {
-        if (!warp_wait(o_full(so), (t / kOS) & 1, ctl) || !warp_wait(p_full, ph, ctl)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk)                          // dV += P^T dO
-          mma_ts_elect(tdV, tP + kk * 8, kdO_mn + so * kStageDesc + kk * kRowStep, idesc_acc,
-                       (t > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_elect(dv_done);
-        mma_commit_elect(q_empty(sq));               // S^T(t) and dV(t) are done with both stages
-        mma_commit_elect(o_empty(so));
-      } else {
-        if (!warp_wait(ds_full, ph, ctl)) break;
-        tc_fence_after();
-        if constexpr (kFusedDq) {
-          const uint32_t dsb = (t & 1) * (L::kdSBytes >> 4);                 // dS tile t % 2
-#pragma unroll
-          for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dK += dS^T Q
-            mma_ss_elect(tdK, kdS_k + dsb + (kk >> 2) * 1024 + (kk & 3) * 2,
-                         kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_elect(q_empty(sq));             // dP^T(t) and dK(t) are done with the Q stage
-          if (t > 0 && !warp_wait(dq_empty, ph ^ 1, ctl)) break;
+      issue_t(sq, so);
+      // The unit's first accumulation overwrites dV / dK: the previous unit's epilogue
+      // has read them.
+      if (!warp_wait(acc_free, (units - 1) & 1, ctl)) break;
+#pragma unroll 1
+      for (int t = 0; t < T; ++t, ++g) {
+        const int sq1 = (sq + 1 == kQS) ? 0 : sq + 1;
+        const int so1 = (so + 1 == kOS) ? 0 : so + 1;
+        const bool more = t + 1 < T;
+        const uint32_t ph = g & 1;
+        if (more) {
+          // The next score product as soon as this side's warps have read the current one.
+          if (!wait_operands(g + 1, sq1, so1) || !warp_wait(t_free, ph, ctl)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dQ = dS K
-            mma_ss_elect(tdQ, kdS_mn + dsb + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
-          mma_commit_elect(dq_full);
-        } else {
-#pragma unroll
-          for (int kk = 0; kk < kTileRows / 16; ++kk)                        // dK += dS^T Q
-            mma_ts_elect(tdK, tdS + kk * 8, kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc,
-                         (t > 0 || kk > 0) ? 1u : 0u);
-          mma_commit_elect(q_empty(sq));             // dP^T(t) and dK(t) are done with the Q stage
-          mma_commit_elect(dk_done);
+          issue_t(sq1, so1);
         }
+        if (p_side) {
+          if (!warp_wait(o_full(so), (g / kOS) & 1, ctl) || !warp_wait(p_full, ph, ctl)) { ok = false; break; }
+          tc_fence_after();
+          if (elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < kTileRows / 16; ++kk)                      // dV += P^T dO
+              mma_ts(tdV, tP + kk * 8, kdO_mn + so * kStageDesc + kk * kRowStep, idesc_acc,
+                     (t > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(dv_done);
+            mma_commit(q_empty(sq));                 // S^T and dV are done with both stages
+            mma_commit(o_empty(so));
+          }
+          __syncwarp();
+        } else {
+          if (!warp_wait(ds_full, ph, ctl)) { ok = false; break; }
+          tc_fence_after();
+          if constexpr (kFusedDq) {
+            const uint32_t dsb = (g & 1) * (L::kdSBytes >> 4);               // dS tile g % 2
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < kTileRows / 16; ++kk)                    // dK += dS^T Q
+                mma_ss(tdK, kdS_k + dsb + (kk >> 2) * 1024 + (kk & 3) * 2,
+                       kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(q_empty(sq));               // dP^T and dK are done with the Q stage
+            }
+            __syncwarp();
+            if (!warp_wait(dq_empty, ph ^ 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < kTileRows / 16; ++kk)                    // dQ = dS K
+                mma_ss(tdQ, kdS_mn + dsb + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
+              mma_commit(dq_full);
+            }
+            __syncwarp();
+          } else {
+            if (elect_one()) {
+#pragma unroll
+              for (int kk = 0; kk < kTileRows / 16; ++kk)                    // dK += dS^T Q
+                mma_ts(tdK, tdS + kk * 8, kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc,
+                       (t > 0 || kk > 0) ? 1u : 0u);
+              mma_commit(q_empty(sq));               // dP^T and dK are done with the Q stage
+              mma_commit(dk_done);
+            }
+            __syncwarp();
+          }
+        }
+        sq = sq1;
+        so = so1;
       }
-      sq = sq1;
-      so = so1;
+      if (!ok) break;
+      if (elect_one()) mma_commit(acc_done);
+      __syncwarp();
+      ++units;
     }
-    mma_commit_elect(acc_done);
-    mbar_drain(acc_done, 0, ctl);
+    if (units > 0) mbar_drain(acc_done, (units - 1) & 1, ctl);
   } else if (kFusedDq && warp == 2) {
     // ---------------- dQ reducer ----------------
     // Both head-dim halves of a staged tile are issued before one wait for their reads.
-    for (int k = 0; k < T; ++k) {
-      if (!warp_wait(dqs_full, k & 1, ctl)) break;
-      if (lane == 0) {
-        const int h = kvh * group + k / per_head, m = n + k % per_head;
-        const uint32_t src = smem_u32(sdQs_ptr);
-        tma_reduce_add_4d(&mdq, src, 0, h, m * kTileRows, b);
-        tma_reduce_add_4d(&mdq, src + L::kDqHalfBytes, HD / 2, h, m * kTileRows, b);
-        bulk_commit_group();
-        bulk_wait_read_all();          // the staging buffer may be rewritten
-        mbar_arrive(dqs_empty);
+    bool ok = true;
+#pragma unroll 1
+    for (int k = 0, g = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      set_unit(u);
+#pragma unroll 1
+      for (int t = 0; t < T; ++t, ++g) {
+        if (!warp_wait(dqs_full, g & 1, ctl)) { ok = false; break; }
+        if (lane == 0) {
+          const int h = kvh * group + t / per_head, m = n + t % per_head;
+          const uint32_t src = smem_u32(sdQs_ptr);
+          tma_reduce_add_4d(&mdq, src, 0, h, m * kTileRows, b);
+          tma_reduce_add_4d(&mdq, src + L::kDqHalfBytes, HD / 2, h, m * kTileRows, b);
+          bulk_commit_group();
+          bulk_wait_read_all();        // the staging buffer may be rewritten
+          mbar_arrive(dqs_empty);
+        }
+        __syncwarp();
       }
-      __syncwarp();
     }
     if (lane == 0) bulk_wait_all();    // every reduce-add has landed before the CTA exits
     __syncwarp();
@@ -501,57 +571,64 @@ __global__ void __maxnreg__(168)
     const int j = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int m = n + t % per_head;
-      const bool diag = (m == n);
-      if (!warp_wait(s_full, t & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      // The whole row of S^T(t) comes into registers with one TMEM read and the buffer is
-      // released at once, so S^T(t+1) is computed while these exponentials run.
-      uint32_t r[128];
+#pragma unroll 1
+    for (int k = 0, g = 0, units = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      set_unit(u);
+#pragma unroll 1
+      for (int t = 0; t < T; ++t, ++g) {
+        const int m = n + t % per_head;
+        const bool diag = (m == n);
+        if (!warp_wait(s_full, g & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        // The whole row of S^T(t) comes into registers with one TMEM read and the buffer is
+        // released at once, so S^T(t+1) is computed while these exponentials run.
+        uint32_t r[128];
 #pragma unroll
-      for (int c = 0; c < 128; c += 32) tmem_ld_x32(tS + lane_off + c, r + c);
-      tmem_wait_ld();
-      reg_fence<128>(r);
-      tc_fence_before();
-      mbar_arrive(s_free);
+        for (int c = 0; c < 128; c += 32) tmem_ld_x32(tS + lane_off + c, r + c);
+        tmem_wait_ld();
+        reg_fence<128>(r);
+        tc_fence_before();
+        mbar_arrive(s_free);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const uint32_t *cur = r + 32 * c + 4 * q4;
-          float x0, x1, x2, x3;
-          fmul2(x0, x1, __uint_as_float(cur[0]), __uint_as_float(cur[1]), scale_log2, scale_log2);
-          fmul2(x2, x3, __uint_as_float(cur[2]), __uint_as_float(cur[3]), scale_log2, scale_log2);
-          float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-          if (diag) {
-            const int i = 32 * c + 4 * q4;
-            if (i + 0 < j) p0 = 0.f;
-            if (i + 1 < j) p1 = 0.f;
-            if (i + 2 < j) p2 = 0.f;
-            if (i + 3 < j) p3 = 0.f;
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const uint32_t *cur = r + 32 * c + 4 * q4;
+            float x0, x1, x2, x3;
+            fmul2(x0, x1, __uint_as_float(cur[0]), __uint_as_float(cur[1]), scale_log2, scale_log2);
+            fmul2(x2, x3, __uint_as_float(cur[2]), __uint_as_float(cur[3]), scale_log2, scale_log2);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+            if (diag) {
+              const int i = 32 * c + 4 * q4;
+              if (i + 0 < j) p0 = 0.f;
+              if (i + 1 < j) p1 = 0.f;
+              if (i + 2 < j) p2 = 0.f;
+              if (i + 3 < j) p3 = 0.f;
+            }
+            pk[2 * q4] = pack_bf16x2(p0, p1);
+            pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
           }
-          pk[2 * q4] = pack_bf16x2(p0, p1);
-          pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
-        }
-        if (c == 0 && t > 0) {
-          // P^T(t-1) must have been read by the dS warps and by dV(t-1).
-          if (!warp_wait(p_free, (t - 1) & 1, ctl) || !warp_wait(dv_done, (t - 1) & 1, ctl)) {
-            ok = false;
-            break;
+          if (c == 0) {
+            // P^T of the previous iteration must have been read by the dS warps and by dV.
+            if (!warp_wait(p_free, (g - 1) & 1, ctl) || !warp_wait(dv_done, (g - 1) & 1, ctl)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
           }
-          tc_fence_after();
+          tmem_st_x16(tP + lane_off + 16 * c, pk);
         }
-        tmem_st_x16(tP + lane_off + 16 * c, pk);
+        if (!ok) break;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
       }
       if (!ok) break;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    // Epilogue: dV rows (bf16).
-    if (ok && warp_wait(acc_done, 0, ctl)) {
+      // Epilogue: dV rows (bf16), then the dV columns are free for the next unit.
+      if (!warp_wait(acc_done, units & 1, ctl)) break;
       tc_fence_after();
       const int jg = n * kTileRows + j;
       const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
@@ -571,6 +648,9 @@ __global__ void __maxnreg__(168)
                                 pack_bf16x2(__uint_as_float(v[8 * e + 6]), __uint_as_float(v[8 * e + 7])));
         }
       }
+      tc_fence_before();
+      mbar_arrive(acc_free);
+      ++units;
     }
   } else if (warp >= 8) {
     // ---------------- dS^T (and the fused dQ drain): one thread per key row j ----------------
@@ -607,80 +687,91 @@ __global__ void __maxnreg__(168)
       return true;
     };
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      if (!warp_wait(p_full, t & 1, ctl) || !warp_wait(dp_full, t & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      // 4 chunks of 32 query columns: P^T bf16 (16 TMEM columns) and dP^T (32 columns).
-      uint32_t pa[16], da[32], pb[16], db[32];
-      tmem_ld_x16(tP + lane_off, pa);
-      tmem_ld_x32(tdP + lane_off, da);
-      tmem_wait_ld();
-      reg_fence<16>(pa);
-      reg_fence<32>(da);
+#pragma unroll 1
+    for (int k = 0, g = 0, units = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      set_unit(u);
+#pragma unroll 1
+      for (int t = 0; t < T; ++t, ++g) {
+        if (!warp_wait(p_full, g & 1, ctl) || !warp_wait(dp_full, g & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        // 4 chunks of 32 query columns: P^T bf16 (16 TMEM columns) and dP^T (32 columns).
+        uint32_t pa[16], da[32], pb[16], db[32];
+        tmem_ld_x16(tP + lane_off, pa);
+        tmem_ld_x32(tdP + lane_off, da);
+        tmem_wait_ld();
+        reg_fence<16>(pa);
+        reg_fence<32>(da);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t *pc = (c & 1) ? pb : pa, *dc = (c & 1) ? db : da;
-        uint32_t *pn = (c & 1) ? pa : pb, *dn = (c & 1) ? da : db;
-        if (c < 3) {
-          tmem_ld_x16(tP + lane_off + 16 * (c + 1), pn);
-          tmem_ld_x32(tdP + lane_off + 32 * (c + 1), dn);
-        }
-        // The dS^T buffer about to be written has been read. Fused dQ: tile t % 2 was last
-        // read by dK(t-2) and dQ(t-2), which completed before the drain of dQ(t-2) in the
-        // previous iteration. Otherwise dK(t-1) read dS^T(t-1) from TMEM.
-        if (!kFusedDq && c == 0 && t > 0) {
-          if (!warp_wait(dk_done, (t - 1) & 1, ctl)) {
-            tmem_wait_ld();    // the loads of chunk 1 are still in flight
-            ok = false;
-            break;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t *pc = (c & 1) ? pb : pa, *dc = (c & 1) ? db : da;
+          uint32_t *pn = (c & 1) ? pa : pb, *dn = (c & 1) ? da : db;
+          if (c < 3) {
+            tmem_ld_x16(tP + lane_off + 16 * (c + 1), pn);
+            tmem_ld_x32(tdP + lane_off + 32 * (c + 1), dn);
           }
-          tc_fence_after();
-        }
-        uint32_t dsk[16];
+          // The dS^T buffer about to be written has been read. Fused dQ: tile g % 2 was last
+          // read by dK and dQ of iteration g-2, which completed before the drain of that dQ
+          // (in iteration g-1, or in the epilogue of the previous unit). Otherwise the
+          // previous dK read dS^T from TMEM.
+          if (!kFusedDq && c == 0) {
+            if (!warp_wait(dk_done, (g - 1) & 1, ctl)) {
+              tmem_wait_ld();    // the loads of chunk 1 are still in flight
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          uint32_t dsk[16];
 #pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
-          const uint32_t p01 = pc[2 * q4], p23 = pc[2 * q4 + 1];
-          float t0, t1, t2, t3;
-          fmul2(t0, t1, __uint_as_float(dc[4 * q4]), __uint_as_float(dc[4 * q4 + 1]), bf16lo_to_f32(p01),
-                bf16hi_to_f32(p01));
-          fmul2(t2, t3, __uint_as_float(dc[4 * q4 + 2]), __uint_as_float(dc[4 * q4 + 3]), bf16lo_to_f32(p23),
-                bf16hi_to_f32(p23));
-          dsk[2 * q4] = pack_bf16x2(t0, t1);
-          dsk[2 * q4 + 1] = pack_bf16x2(t2, t3);
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const uint32_t p01 = pc[2 * q4], p23 = pc[2 * q4 + 1];
+            float t0, t1, t2, t3;
+            fmul2(t0, t1, __uint_as_float(dc[4 * q4]), __uint_as_float(dc[4 * q4 + 1]), bf16lo_to_f32(p01),
+                  bf16hi_to_f32(p01));
+            fmul2(t2, t3, __uint_as_float(dc[4 * q4 + 2]), __uint_as_float(dc[4 * q4 + 3]), bf16lo_to_f32(p23),
+                  bf16hi_to_f32(p23));
+            dsk[2 * q4] = pack_bf16x2(t0, t1);
+            dsk[2 * q4 + 1] = pack_bf16x2(t2, t3);
+          }
+          if constexpr (kFusedDq) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4 *>(sdS_ptr + (g & 1) * L::kdSBytes + ds_offset(j, 32 * c + 8 * e)) =
+                  make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
+          } else {
+            tmem_st_x16(tdS + lane_off + 16 * c, dsk);
+          }
+          if (c < 3) {
+            tmem_wait_ld();
+            reg_fence<16>(pn);
+            reg_fence<32>(dn);
+          }
+          if (c == 2) {          // P^T(t) and dP^T(t) are all in registers
+            tc_fence_before();
+            mbar_arrive(p_free);
+            mbar_arrive(dp_free);
+          }
         }
+        if (!ok) break;
         if constexpr (kFusedDq) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            *reinterpret_cast<uint4 *>(sdS_ptr + (t & 1) * L::kdSBytes + ds_offset(j, 32 * c + 8 * e)) =
-                make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
+          fence_proxy_async_smem();
+          mbar_arrive(ds_full);
+          if (t > 0 && !drain_dq(g - 1)) { ok = false; break; }
         } else {
-          tmem_st_x16(tdS + lane_off + 16 * c, dsk);
-        }
-        if (c < 3) {
-          tmem_wait_ld();
-          reg_fence<16>(pn);
-          reg_fence<32>(dn);
-        }
-        if (c == 2) {          // P^T(t) and dP^T(t) are all in registers
+          tmem_wait_st();
           tc_fence_before();
-          mbar_arrive(p_free);
-          mbar_arrive(dp_free);
+          mbar_arrive(ds_full);
         }
       }
       if (!ok) break;
+      // Epilogue: the unit's last dQ (fused), then the dK rows (bf16, times the softmax
+      // scale); the dK columns are then free for the next unit.
       if constexpr (kFusedDq) {
-        fence_proxy_async_smem();
-        mbar_arrive(ds_full);
-        if (t > 0 && !drain_dq(t - 1)) { ok = false; break; }
-      } else {
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(ds_full);
+        if (!drain_dq(g - 1)) break;
       }
-    }
-    // Epilogue: the last dQ (fused), then the dK rows (bf16, times the softmax scale).
-    if constexpr (kFusedDq) ok = ok && drain_dq(T - 1);
-    if (ok && warp_wait(acc_done, 0, ctl)) {
+      if (!warp_wait(acc_done, units & 1, ctl)) break;
       tc_fence_after();
       const int jg = n * kTileRows + j;
       const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
@@ -701,6 +792,9 @@ __global__ void __maxnreg__(168)
                                 pack_bf16x2(f[8 * e + 4], f[8 * e + 5]), pack_bf16x2(f[8 * e + 6], f[8 * e + 7]));
         }
       }
+      tc_fence_before();
+      mbar_arrive(acc_free);
+      ++units;
     }
   }
 
@@ -721,8 +815,12 @@ cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const C
   cudaError_t err = cudaFuncSetAttribute(attn_bwd_main_kernel<HD, kFusedDq>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
   if (err != cudaSuccess) return err;
-  const int num_n = (S + kTileRows - 1) / kTileRows;
-  const unsigned grid = static_cast<unsigned>(B) * nkv * num_n;
+  // Persistent CTAs: one per SM, or one per unit when there are fewer units.
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  const long long units = static_cast<long long>(B) * nkv * ((S + kTileRows - 1) / kTileRows);
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   attn_bwd_main_kernel<HD, kFusedDq><<<grid, kBwdThreads, L::kDynBytes, stream>>>(
       mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns);
   return cudaGetLastError();

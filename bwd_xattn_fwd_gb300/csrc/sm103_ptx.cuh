@@ -292,6 +292,16 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// One elected lane of a converged warp. A product's MMAs and its commits are issued
+// inside one region this guards: a converged-warp form per instruction (below) takes
+// about four times the code per MMA, which the backward's many issue sites cannot afford
+// in the instruction cache.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+  return e != 0;
+}
+
 // Converged-warp forms: every lane of the warp executes the call with the same
 // (warp-uniform) operands and one elected lane issues the instruction. Issuing from a
 // converged warp keeps the operands in the uniform datapath; issuing from a divergent
