@@ -72,7 +72,8 @@ __global__ void __maxnreg__(168)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Warp-uniform by construction; the broadcast lets the compiler see it.
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
 
   // Tile pair of this CTA, longest first.
   const int num_m = (S + kTileRows - 1) / kTileRows;
@@ -132,7 +133,7 @@ __global__ void __maxnreg__(168)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
   auto tS = [&](int x) { return tmem + 128u * x; };
   auto tO = [&](int x) { return tmem + 256u + 64u * x; };
   auto tP = [&](int x) { return tmem + 384u + 64u * x; };
@@ -174,22 +175,34 @@ __global__ void __maxnreg__(168)
     const uint64_t dK = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
     const uint64_t dV = smem_desc(sV, 8192, 8 * L::kRowBytes, L::kSwizzle);
     const uint32_t tSx = tS(x), tOx = tO(x), tPx = tP(x);
+    // Each product's MMAs and commits are issued by one elected lane; the warp then
+    // reconverges.
     auto issue_qk = [&](int s) {
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        mma_ss_elect(tSx, dQ + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          mma_ss(tSx, dQ + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
+        mma_commit(s_full(x));
+      }
+      __syncwarp();
     };
-    auto issue_pv = [&](int s, bool first) {
+    // Release of stage s: each issuer that uses key tile n commits once, or twice when it
+    // is the tile's only user.
+    auto issue_pv = [&](int s, bool first, bool sole_user) {
+      if (elect_one()) {
 #pragma unroll
-      for (int kk = 0; kk < kTileRows / 16; ++kk)
-        mma_ts_elect(tOx, tPx + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv,
-                     (!first || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_ts(tOx, tPx + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        mma_commit(o_done(x));
+        mma_commit(empty(s));                      // this issuer is done with K_n and V_n
+        if (sole_user) mma_commit(empty(s));
+      }
+      __syncwarp();
     };
     bool ok = active && warp_wait(q_full, 0, ctl) && warp_wait(full(0), 0, ctl);
     if (ok) {
       tc_fence_after();
       issue_qk(0);
-      mma_commit_elect(s_full(x));
     }
     // Per key tile n: S_X(n+1) as soon as the softmax has loaded the last of S_X(n)
     // (s_free, signalled half-way through its exponentials), then PV_X(n) once P_X(n) is
@@ -204,19 +217,16 @@ __global__ void __maxnreg__(168)
         if (!warp_wait(s_free(x), n & 1, ctl) || !warp_wait(full(s1), ph1, ctl)) { ok = false; break; }
         tc_fence_after();
         issue_qk(s1);
-        mma_commit_elect(s_full(x));
       }
       if (!warp_wait(p_full(x), n & 1, ctl)) { ok = false; break; }
       tc_fence_after();
-      issue_pv(s, n == 0);
-      mma_commit_elect(o_done(x));
       const bool shared_tile = x == 0 ? hasB : n <= mA;
-      mma_commit_elect(empty(s));                  // this issuer is done with K_n and V_n
-      if (!shared_tile) mma_commit_elect(empty(s));
+      issue_pv(s, n == 0, !shared_tile);
       if (++s == kFwdStages) s = 0;
       if (++s1 == kFwdStages) { s1 = 0; ph1 ^= 1; }
     }
-    mma_commit_elect(mma_final);
+    if (elect_one()) mma_commit(mma_final);
+    __syncwarp();
     mbar_drain(mma_final, 0, ctl);
   } else if (warp >= 4) {
     // ---------------- softmax + epilogue: one thread per query row of tile X ----------------
