@@ -5,9 +5,11 @@
 // log-sum-exp is kept for the backward. Grouped KV heads (row T15): query head h reads
 // kv head h / group.
 //
-// GB300 mapping: one CTA per pair of 128-row query tiles A = 2j and B = 2j+1 of one
-// (batch, head) -- 256 query rows that share every K/V tile they read -- 12 warps:
-//   warp 0     : TMA producer. Q_A and Q_B once; K/V tiles through a 3-stage ring.
+// GB300 mapping: a unit of work is one pair of 128-row query tiles A = 2j and B = 2j+1
+// of one (batch, head) -- 256 query rows that share every K/V tile they read. Persistent
+// CTAs, one per SM, take the units in turn (longest first). 12 warps:
+//   warp 0     : TMA producer. Q_A and Q_B once per unit; K/V tiles through a 3-stage
+//                ring that runs on across units.
 //   warp 1     : TMEM owner and MMA issuer (converged warp, one elected lane issues):
 //                  S_X(n) = Q_X K_n^T  (A, B from shared memory) -> TMEM
 //                  O_X   += P_X(n) V_n (A = P from TMEM)          -> TMEM accumulator
@@ -21,7 +23,7 @@
 // (log2 domain), P in bf16 to TMEM, O rescaled only when the running max grows by more
 // than 2^8 (the stale max is exact because the final normalisation uses the same max).
 // Epilogue: O / l in bf16, LSE = (m + log2 l) ln 2.
-// Causal tile skipping: tile m visits key tiles 0..m. CTAs are issued longest first.
+// Causal tile skipping: tile m visits key tiles 0..m.
 // TMEM columns: S_A [0,128) S_B [128,256) fp32 | O_A [256,256+HD) O_B [320,320+HD) fp32 |
 //               P_A [384,448) P_B [448,512) bf16 pairs.
 #include <type_traits>
@@ -45,8 +47,8 @@ struct FwdLayout {
   static constexpr uint32_t kV = kK + kFwdStages * kTileBytes;
   static constexpr uint32_t kBars = kV + kFwdStages * kTileBytes;
   // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done[2], mma_final,
-  //           s_free[2]
-  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 1 + 2;
+  //           s_free[2], o_free[2]
+  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 1 + 2 + 2;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   // Ask for enough shared memory that one CTA occupies an SM: each CTA holds all 512
@@ -75,17 +77,28 @@ __global__ void __maxnreg__(168)
   // Warp-uniform by construction; the broadcast lets the compiler see it.
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
 
-  // Tile pair of this CTA, longest first.
+  // Work units (tile pair jp of one (batch, head)) are numbered longest first. The CTAs
+  // are persistent: CTA c of G takes unit k G + c in even rounds k and k G + G - 1 - c in
+  // odd ones. Every role walks the same units; the barriers' phases count over all of
+  // them (waits for the phase before the first -- parity 1 of a fresh barrier -- return
+  // at once, so the first unit needs no special case).
   const int num_m = (S + kTileRows - 1) / kTileRows;
   const int num_pairs = (num_m + 1) / 2;
   const int BH = B * nh;
-  const int jp = num_pairs - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int b = bh / nh, h = bh % nh;
-  const int kvh = h / (nh / nkv);
-  const int mA = 2 * jp, mB = 2 * jp + 1;
-  const bool hasB = mB < num_m;
-  const int n_last = hasB ? mB : mA;       // last key tile of the pair
+  const int num_units = num_pairs * BH;
+  const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
+  auto unit_at = [G, cta](int k) { return k * G + ((k & 1) ? G - 1 - cta : cta); };
+// Fields of unit u, as constants of the role loop that processes it.
+#define XATTN_FWD_UNIT(u)                                       \
+  const int jp = num_pairs - 1 - (u) / BH;                      \
+  const int b = ((u) % BH) / nh, h = (u) % nh;                  \
+  const int kvh = h / (nh / nkv);                               \
+  const int mA = 2 * jp, mB = 2 * jp + 1;                       \
+  const bool hasB = mB < num_m;                                 \
+  const int n_last = hasB ? mB : mA; /* last key tile */        \
+  (void)b;                                                      \
+  (void)kvh;                                                    \
+  (void)n_last
 
   const uint32_t sQ = smem_u32(smem + L::kQ);
   const uint32_t sK = smem_u32(smem + L::kK);
@@ -98,8 +111,9 @@ __global__ void __maxnreg__(168)
   auto s_full = [&](int x) { return bar(1 + 2 * kFwdStages + x); };
   auto p_full = [&](int x) { return bar(3 + 2 * kFwdStages + x); };
   auto o_done = [&](int x) { return bar(5 + 2 * kFwdStages + x); };
-  const uint32_t mma_final = bar(7 + 2 * kFwdStages);
+  const uint32_t mma_final = bar(7 + 2 * kFwdStages);                // a unit's products done
   auto s_free = [&](int x) { return bar(8 + 2 * kFwdStages + x); };
+  auto o_free = [&](int x) { return bar(10 + 2 * kFwdStages + x); };   // O_X read by the epilogue
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -117,6 +131,7 @@ __global__ void __maxnreg__(168)
       mbar_init(p_full(x), 128);
       mbar_init(o_done(x), 1);
       mbar_init(s_free(x), 128);
+      mbar_init(o_free(x), 128);
     }
     mbar_init(mma_final, 2);
     fence_mbar_init();
@@ -140,20 +155,39 @@ __global__ void __maxnreg__(168)
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
-    mbar_expect_tx_elect(q_full, (hasB ? 2 : 1) * L::kTileBytes);
-    tma_load_4d_elect(sQ, &mq, q_full, 0, h, mA * kTileRows, b);
-    if (hasB) tma_load_4d_elect(sQ + L::kTileBytes, &mq, q_full, 0, h, mB * kTileRows, b);
-    int issued = 0;
-    for (int n = 0, s = 0, ph = 0; n <= n_last; ++n) {
-      if (!warp_wait(empty(s), ph ^ 1, ctl)) break;
+    // The K/V ring runs on across units (ring index R counts tiles over all of them). A
+    // unit's first kFwdStages tiles only need stages released by earlier units, so they
+    // are issued before waiting for the previous unit's products (mma_final): only then
+    // are Q_A and Q_B overwritten.
+    int units = 0, R = 0, issued = 0;
+    auto load_kv = [&](int n, int kvh, int b) -> bool {
+      const int s = R % kFwdStages;
+      if (!warp_wait(empty(s), ((R / kFwdStages) & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(full(s), 2 * L::kTileBytes);
       tma_load_4d_elect(sK + s * L::kTileBytes, &mk, full(s), 0, kvh, n * kTileRows, b);
       tma_load_4d_elect(sV + s * L::kTileBytes, &mv, full(s), 0, kvh, n * kTileRows, b);
-      issued = n + 1;
-      if (++s == kFwdStages) { s = 0; ph ^= 1; }
+      issued = ++R;
+      return true;
+    };
+    bool ok = true;
+#pragma unroll 1
+    for (int k = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      XATTN_FWD_UNIT(u);
+      const int pre = n_last + 1 < kFwdStages ? n_last + 1 : kFwdStages;
+#pragma unroll 1
+      for (int n = 0; ok && n < pre; ++n) ok = load_kv(n, kvh, b);
+      if (!ok || !warp_wait(mma_final, (units - 1) & 1, ctl)) break;
+      mbar_expect_tx_elect(q_full, (hasB ? 2 : 1) * L::kTileBytes);
+      tma_load_4d_elect(sQ, &mq, q_full, 0, h, mA * kTileRows, b);
+      if (hasB) tma_load_4d_elect(sQ + L::kTileBytes, &mq, q_full, 0, h, mB * kTileRows, b);
+      ++units;
+#pragma unroll 1
+      for (int n = pre; ok && n <= n_last; ++n) ok = load_kv(n, kvh, b);
     }
     // Let every copy in flight land before the CTA can exit.
-    mbar_drain(q_full, 0, ctl);
+    if (units > 0) mbar_drain(q_full, (units - 1) & 1, ctl);
     for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
       mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
   } else if (warp == 1 || warp == 3) {
@@ -163,8 +197,6 @@ __global__ void __maxnreg__(168)
     // SM sub-partitions. The tensor pipe takes their MMAs in arrival order; the K/V
     // stages are released by a commit from each (empty counts 2).
     const int x = warp == 1 ? 0 : 1;
-    const int mX = x == 0 ? mA : mB;
-    const bool active = x == 0 || hasB;
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;        // tile stride, descriptor units
@@ -199,139 +231,166 @@ __global__ void __maxnreg__(168)
       }
       __syncwarp();
     };
-    bool ok = active && warp_wait(q_full, 0, ctl) && warp_wait(full(0), 0, ctl);
-    if (ok) {
-      tc_fence_after();
-      issue_qk(0);
-    }
-    // Per key tile n: S_X(n+1) as soon as the softmax has loaded the last of S_X(n)
-    // (s_free, signalled half-way through its exponentials), then PV_X(n) once P_X(n) is
-    // in TMEM (p_full). The next scores are thus computed while the softmax is still
-    // producing P_X(n).
+    // Per key tile n: S_X(n+1) as soon as the softmax has loaded S_X(n) (s_free), then
+    // PV_X(n) once P_X(n) is in TMEM (p_full). The next scores are thus computed while the
+    // softmax is still producing P_X(n).
     // Release of stage s: each issuer that uses key tile n commits once, or twice when it
     // is the tile's only user (tile mB when there is a tile B; every tile when there is
     // not). An issuer never arrives for a tile it does not use, so its arrivals cannot
     // land in an earlier phase of the stage that the other issuer has not released yet.
-    for (int n = 0, s = 0, s1 = 1 % kFwdStages, ph1 = (1 / kFwdStages) & 1; ok && n <= mX; ++n) {
-      if (n + 1 <= mX) {
-        if (!warp_wait(s_free(x), n & 1, ctl) || !warp_wait(full(s1), ph1, ctl)) { ok = false; break; }
+    // R: ring index of the unit's key tile 0; gx: this tile's key steps over all units.
+    bool ok = true;
+    int units = 0, unitsx = 0;
+    auto ring_stage = [](int r) { return r % kFwdStages; };
+    auto ring_phase = [](int r) { return static_cast<uint32_t>((r / kFwdStages) & 1); };
+#pragma unroll 1
+    for (int k = 0, R = 0, gx = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      XATTN_FWD_UNIT(u);
+      const int mX = x == 0 ? mA : mB;
+      if (x == 0 || hasB) {
+        // The unit's first scores: Q landed, key tile 0 landed, and S_X of the previous
+        // unit read; its first PV overwrites O_X, which the previous epilogue has read.
+        ok = warp_wait(q_full, units & 1, ctl) && warp_wait(full(ring_stage(R)), ring_phase(R), ctl) &&
+             warp_wait(s_free(x), (gx - 1) & 1, ctl);
+        if (!ok) break;
         tc_fence_after();
-        issue_qk(s1);
+        issue_qk(ring_stage(R));
+        if (!warp_wait(o_free(x), (unitsx - 1) & 1, ctl)) { ok = false; break; }
+#pragma unroll 1
+        for (int n = 0; n <= mX; ++n, ++gx) {
+          if (n + 1 <= mX) {
+            if (!warp_wait(s_free(x), gx & 1, ctl) ||
+                !warp_wait(full(ring_stage(R + n + 1)), ring_phase(R + n + 1), ctl)) { ok = false; break; }
+            tc_fence_after();
+            issue_qk(ring_stage(R + n + 1));
+          }
+          if (!warp_wait(p_full(x), gx & 1, ctl)) { ok = false; break; }
+          tc_fence_after();
+          const bool shared_tile = x == 0 ? hasB : n <= mA;
+          issue_pv(ring_stage(R + n), n == 0, !shared_tile);
+        }
+        if (!ok) break;
+        ++unitsx;
       }
-      if (!warp_wait(p_full(x), n & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      const bool shared_tile = x == 0 ? hasB : n <= mA;
-      issue_pv(s, n == 0, !shared_tile);
-      if (++s == kFwdStages) s = 0;
-      if (++s1 == kFwdStages) { s1 = 0; ph1 ^= 1; }
+      if (elect_one()) mma_commit(mma_final);      // covers every MMA of this unit
+      __syncwarp();
+      R += n_last + 1;
+      ++units;
     }
-    if (elect_one()) mma_commit(mma_final);
-    __syncwarp();
-    mbar_drain(mma_final, 0, ctl);
+    if (units > 0) mbar_drain(mma_final, (units - 1) & 1, ctl);
   } else if (warp >= 4) {
     // ---------------- softmax + epilogue: one thread per query row of tile X ----------------
     const int x = (warp - 4) >> 2;          // 0 = tile A, 1 = tile B
-    const int mX = x == 0 ? mA : mB;
-    const bool active = x == 0 || hasB;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t tSx = tS(x) + lane_off, tOx = tO(x) + lane_off, tPx = tP(x) + lane_off;
-    float mrow = -INFINITY, lrow = 0.f;
-    bool ok = active;
-    for (int n = 0; ok && n <= mX; ++n) {
-      if (!warp_wait(s_full(x), n & 1, ctl)) { ok = false; break; }
-      tc_fence_after();
-      const bool diag = (n == mX);
-      // The whole row of S_X(n) comes into registers with one TMEM read, and the buffer
-      // is released at once: S_X(n+1) is computed while this softmax runs.
-      uint32_t r[128];
-#pragma unroll
-      for (int c = 0; c < 128; c += 32) tmem_ld_x32(tSx + c, r + c);
-      tmem_wait_ld();
-      reg_fence<128>(r);
-      tc_fence_before();
-      mbar_arrive(s_free(x));
-      // The row maximum of the scaled scores: the scaled maximum of the raw scores
-      // (scale >= 0) or their scaled minimum (scale < 0); masked columns do not count.
-      constexpr float kFill = kNegScale ? INFINITY : -INFINITY;
-      float mx4[4] = {kFill, kFill, kFill, kFill};
-      auto maxpass = [&](auto masked) {
-#pragma unroll
-        for (int c = 0; c < 128; c += 2) {
-          float v0 = __uint_as_float(r[c]), v1 = __uint_as_float(r[c + 1]);
-          if (decltype(masked)::value) {
-            if (c > row) v0 = kFill;
-            if (c + 1 > row) v1 = kFill;
-          }
-          float &a = mx4[(c >> 1) & 3];
-          a = kNegScale ? fmin3(a, v0, v1) : fmax3(a, v0, v1);
-        }
-      };
-      if (diag) maxpass(std::true_type{});
-      else maxpass(std::false_type{});
-      const float mx = (kNegScale ? fmin3(mx4[0], mx4[1], fminf(mx4[2], mx4[3]))
-                                  : fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]))) * scale_log2;
-      // Conditional rescaling: keep the stale max unless some row of the warp grew by
-      // more than 2^8; the decision is per warp because TMEM loads/stores are collective.
-      const float mnew = fmaxf(mrow, mx);
-      const bool rescale = __any_sync(0xffffffffu, mnew > mrow + 8.0f);
-      const float m_use = rescale ? mnew : mrow;
-      const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
-      const float neg_m = -m_use;
-      // P_X(n) overwrites P_X(n-1), and O_X may be rescaled: PV_X(n-1) must be done.
-      // Every phase of o_done is waited for in order, so the parity wait is unambiguous.
-      if (n > 0) {
-        if (!warp_wait(o_done(x), (n - 1) & 1, ctl)) { ok = false; break; }
+    bool ok = true;
+#pragma unroll 1
+    for (int k = 0, gx = 0; ok; ++k) {
+      const int u = unit_at(k);
+      if (u >= num_units) break;
+      XATTN_FWD_UNIT(u);
+      const int mX = x == 0 ? mA : mB;
+      if (x == 1 && !hasB) continue;
+      float mrow = -INFINITY, lrow = 0.f;
+#pragma unroll 1
+      for (int n = 0; n <= mX; ++n, ++gx) {
+        if (!warp_wait(s_full(x), gx & 1, ctl)) { ok = false; break; }
         tc_fence_after();
-      }
-      // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
-      // included), the exponentials, row sums and bf16 P, 32 columns at a time. The
-      // diagonal tile has its own copy of the body, so the common one is branch-free.
-      float ps[4] = {0.f, 0.f, 0.f, 0.f};
-      auto body = [&](auto masked) {
+        const bool diag = (n == mX);
+        // The whole row of S_X(n) comes into registers with one TMEM read, and the buffer
+        // is released at once: S_X(n+1) is computed while this softmax runs.
+        uint32_t r[128];
 #pragma unroll
-        for (int c32 = 0; c32 < 128; c32 += 32) {
-          uint32_t pk[16];
+        for (int c = 0; c < 128; c += 32) tmem_ld_x32(tSx + c, r + c);
+        tmem_wait_ld();
+        reg_fence<128>(r);
+        tc_fence_before();
+        mbar_arrive(s_free(x));
+        // The row maximum of the scaled scores: the scaled maximum of the raw scores
+        // (scale >= 0) or their scaled minimum (scale < 0); masked columns do not count.
+        constexpr float kFill = kNegScale ? INFINITY : -INFINITY;
+        float mx4[4] = {kFill, kFill, kFill, kFill};
+        auto maxpass = [&](auto masked) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = c32 + 2 * e;
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), scale_log2, scale_log2,
-                  neg_m, neg_m);
+          for (int c = 0; c < 128; c += 2) {
+            float v0 = __uint_as_float(r[c]), v1 = __uint_as_float(r[c + 1]);
             if (decltype(masked)::value) {
-              if (c > row) x0 = -INFINITY;
-              if (c + 1 > row) x1 = -INFINITY;
+              if (c > row) v0 = kFill;
+              if (c + 1 > row) v1 = kFill;
             }
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            const int a = (e & 1) * 2;
-            fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
-            pk[e] = pack_bf16x2(p0, p1);
+            float &a = mx4[(c >> 1) & 3];
+            a = kNegScale ? fmin3(a, v0, v1) : fmax3(a, v0, v1);
           }
-          tmem_st_x16(tPx + c32 / 2, pk);
-        }
-      };
-      if (diag) body(std::true_type{});
-      else body(std::false_type{});
-      if (rescale && n > 0) {
+        };
+        if (diag) maxpass(std::true_type{});
+        else maxpass(std::false_type{});
+        const float mx = (kNegScale ? fmin3(mx4[0], mx4[1], fminf(mx4[2], mx4[3]))
+                                    : fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]))) * scale_log2;
+        // Conditional rescaling: keep the stale max unless some row of the warp grew by
+        // more than 2^8; the decision is per warp because TMEM loads/stores are collective.
+        const float mnew = fmaxf(mrow, mx);
+        const bool rescale = __any_sync(0xffffffffu, mnew > mrow + 8.0f);
+        const float m_use = rescale ? mnew : mrow;
+        const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
+        const float neg_m = -m_use;
+        // P_X(n) overwrites the previous P_X, and O_X may be rescaled: the previous PV_X
+        // must be done (for n == 0 the previous unit's epilogue has already waited for it).
+        // Every phase of o_done is waited for in order, so the parity wait is unambiguous.
+        if (!warp_wait(o_done(x), (gx - 1) & 1, ctl)) { ok = false; break; }
+        tc_fence_after();
+        // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
+        // included), the exponentials, row sums and bf16 P, 32 columns at a time. The
+        // diagonal tile has its own copy of the body, so the common one is branch-free.
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        auto body = [&](auto masked) {
 #pragma unroll
-        for (int c = 0; c < HD; c += 32) {
-          uint32_t ov[32];
-          tmem_ld_x32(tOx + c, ov);
-          tmem_wait_ld();
-          reg_fence<32>(ov);
+          for (int c32 = 0; c32 < 128; c32 += 32) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st_x32(tOx + c, ov);
+            for (int e = 0; e < 16; ++e) {
+              const int c = c32 + 2 * e;
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), scale_log2, scale_log2,
+                    neg_m, neg_m);
+              if (decltype(masked)::value) {
+                if (c > row) x0 = -INFINITY;
+                if (c + 1 > row) x1 = -INFINITY;
+              }
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              const int a = (e & 1) * 2;
+              fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
+              pk[e] = pack_bf16x2(p0, p1);
+            }
+            tmem_st_x16(tPx + c32 / 2, pk);
+          }
+        };
+        if (diag) body(std::true_type{});
+        else body(std::false_type{});
+        if (rescale && n > 0) {
+#pragma unroll
+          for (int c = 0; c < HD; c += 32) {
+            uint32_t ov[32];
+            tmem_ld_x32(tOx + c, ov);
+            tmem_wait_ld();
+            reg_fence<32>(ov);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st_x32(tOx + c, ov);
+          }
         }
+        lrow = lrow * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
+        mrow = m_use;
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full(x));
       }
-      lrow = lrow * alpha + ((ps[0] + ps[1]) + (ps[2] + ps[3]));
-      mrow = m_use;
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full(x));
-    }
-    if (ok && warp_wait(o_done(x), mX & 1, ctl)) {
+      if (!ok) break;
+      // Epilogue: O / l in bf16 and the LSE; then O_X is free for the next unit.
+      if (!warp_wait(o_done(x), (gx - 1) & 1, ctl)) break;
       tc_fence_after();
       const int i = mX * kTileRows + row;
       const float inv = 1.f / lrow;
@@ -354,6 +413,8 @@ __global__ void __maxnreg__(168)
         }
       }
       if (i < S) lse[(static_cast<size_t>(b) * S + i) * nh + h] = (mrow + __log2f(lrow)) * kLn2;
+      tc_fence_before();
+      mbar_arrive(o_free(x));
     }
   }
 
@@ -364,6 +425,7 @@ __global__ void __maxnreg__(168)
     tmem_dealloc(tmem, 512);
   }
 }
+#undef XATTN_FWD_UNIT
 
 template <int HD, bool kNegScale>
 cudaError_t launch_fwd_sign(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
@@ -373,8 +435,13 @@ cudaError_t launch_fwd_sign(const CUtensorMap &mq, const CUtensorMap &mk, const 
   cudaError_t err = cudaFuncSetAttribute(attn_fwd_kernel<HD, kNegScale>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
   if (err != cudaSuccess) return err;
+  // Persistent CTAs: one per SM, or one per unit when there are fewer units.
+  int dev = 0, sms = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
   const int num_m = (S + kTileRows - 1) / kTileRows;
-  const unsigned grid = static_cast<unsigned>(B) * nh * ((num_m + 1) / 2);
+  const long long units = static_cast<long long>(B) * nh * ((num_m + 1) / 2);
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   attn_fwd_kernel<HD, kNegScale><<<grid, kFwdThreads, L::kDynBytes, stream>>>(
       mq, mk, mv, o, lse, B, S, nh, nkv, scale * kLog2e, status, timeout_ns);
   return cudaGetLastError();
