@@ -337,39 +337,44 @@ __global__ void __maxnreg__(168)
         const float m_use = rescale ? mnew : mrow;
         const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
         const float neg_m = -m_use;
-        // P_X(n) overwrites the previous P_X, and O_X may be rescaled: the previous PV_X
-        // must be done (for n == 0 the previous unit's epilogue has already waited for it).
-        // Every phase of o_done is waited for in order, so the parity wait is unambiguous.
-        if (!warp_wait(o_done(x), (gx - 1) & 1, ctl)) { ok = false; break; }
-        tc_fence_after();
         // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
-        // included), the exponentials, row sums and bf16 P, 32 columns at a time. The
-        // diagonal tile has its own copy of the body, so the common one is branch-free.
+        // included), the exponentials, row sums and bf16 P, packed in place into r[0, 64).
+        // The diagonal tile has its own copy of the body, so the common one is branch-free.
+        // The first three quarters of P are computed before waiting for the previous PV_X
+        // (which still reads P_X), so that product's latency overlaps the exponentials;
+        // storing them before the last quarter keeps the register peak at one S row.
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        auto body = [&](auto masked) {
+        auto chunk = [&](auto masked, int c32) {
 #pragma unroll
-          for (int c32 = 0; c32 < 128; c32 += 32) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int c = c32 + 2 * e;
-              float x0, x1;
-              ffma2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), scale_log2, scale_log2,
-                    neg_m, neg_m);
-              if (decltype(masked)::value) {
-                if (c > row) x0 = -INFINITY;
-                if (c + 1 > row) x1 = -INFINITY;
-              }
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              const int a = (e & 1) * 2;
-              fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
-              pk[e] = pack_bf16x2(p0, p1);
+          for (int e = 0; e < 16; ++e) {
+            const int c = c32 + 2 * e;
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), scale_log2, scale_log2,
+                  neg_m, neg_m);
+            if (decltype(masked)::value) {
+              if (c > row) x0 = -INFINITY;
+              if (c + 1 > row) x1 = -INFINITY;
             }
-            tmem_st_x16(tPx + c32 / 2, pk);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            const int a = (e & 1) * 2;
+            fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
+            r[c32 / 2 + e] = pack_bf16x2(p0, p1);
           }
         };
-        if (diag) body(std::true_type{});
-        else body(std::false_type{});
+        auto body = [&](auto masked) -> bool {
+          chunk(masked, 0);
+          chunk(masked, 32);
+          chunk(masked, 64);
+          if (!warp_wait(o_done(x), (gx - 1) & 1, ctl)) return false;
+          tc_fence_after();
+          tmem_st_x32(tPx, r);
+          tmem_st_x16(tPx + 32, r + 32);
+          chunk(masked, 96);
+          tmem_st_x16(tPx + 48, r + 48);
+          return true;
+        };
+        const bool okb = diag ? body(std::true_type{}) : body(std::false_type{});
+        if (!okb) { ok = false; break; }
         if (rescale && n > 0) {
 #pragma unroll
           for (int c = 0; c < HD; c += 32) {
