@@ -123,6 +123,8 @@ __global__ void __maxnreg__(168)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_launch();
+  grid_dep_wait();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tdP = tmem + 128, tdS = tmem + 256, tdQ = tmem + 320;
 
@@ -312,9 +314,8 @@ cudaError_t launch_dq_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUt
   if (err != cudaSuccess) return err;
   const int num_m = (S + kTileRows - 1) / kTileRows;
   const unsigned grid = static_cast<unsigned>(B) * nh * num_m;
-  attn_bwd_dq_kernel<HD><<<grid, kDqThreads, L::kDynBytes, stream>>>(mq, mk, mv, mdo, lse, D, dq, B, S, nh,
-                                                                      nkv, scale, status, timeout_ns);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_dq_kernel<HD>, grid, kDqThreads, L::kDynBytes, stream, mq, mk, mv, mdo, lse, D, dq,
+                    B, S, nh, nkv, scale, status, timeout_ns);
 }
 
 }  // namespace

@@ -83,6 +83,8 @@ __global__ void __launch_bounds__(256) bwd_preprocess_kernel(
     const float *__restrict__ lse, uint4 *__restrict__ aux, float *__restrict__ D,
     float *__restrict__ dqacc, int B, int S, int nh, float lse_mult) {
   constexpr int kLanesPerRow = HD / 8;
+  grid_dep_launch();
+  grid_dep_wait();
   const int S_pad = padded_rows(S);
   const long long n_rows = static_cast<long long>(B) * S * nh;
   const long long n_pad = static_cast<long long>(B) * nh * (S_pad - S);
@@ -346,6 +348,8 @@ __global__ void __maxnreg__(168)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_launch();
+  grid_dep_wait();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
   const uint32_t tS = tmem, tdP = tmem + 128, tP = tmem + 256;
   const uint32_t tdV = tmem + 320, tdK = tmem + 384;
@@ -821,9 +825,8 @@ cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const C
   if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
   const long long units = static_cast<long long>(B) * nkv * ((S + kTileRows - 1) / kTileRows);
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  attn_bwd_main_kernel<HD, kFusedDq><<<grid, kBwdThreads, L::kDynBytes, stream>>>(
-      mq, mk, mv, mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns);
-  return cudaGetLastError();
+  return launch_pdl(attn_bwd_main_kernel<HD, kFusedDq>, grid, kBwdThreads, L::kDynBytes, stream, mq, mk, mv,
+                    mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns);
 }
 
 // 3. dq convert (fused dQ): 8 elements per thread (two 16-byte loads, one 16-byte
@@ -831,6 +834,8 @@ cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const C
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float *__restrict__ acc,
                                                          __nv_bfloat16 *__restrict__ dq,
                                                          size_t n8, float scale) {
+  grid_dep_launch();
+  grid_dep_wait();
   const size_t t = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= n8) return;
   const float4 a = reinterpret_cast<const float4 *>(acc)[2 * t];
@@ -856,12 +861,12 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *d
   const long long threads = (n_rows + n_pad) * lanes;
   const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
   if (hd == 64)
-    bwd_preprocess_kernel<64><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.D, dqacc, B, S, nh, lse_mult);
-  else if (hd == 32)
-    bwd_preprocess_kernel<32><<<grid, 256, 0, stream>>>(o, dO, lse, aux, ws.D, dqacc, B, S, nh, lse_mult);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+    return launch_pdl(bwd_preprocess_kernel<64>, grid, 256, 0, stream, o, dO, lse, aux, ws.D, dqacc, B, S, nh,
+                      lse_mult);
+  if (hd == 32)
+    return launch_pdl(bwd_preprocess_kernel<32>, grid, 256, 0, stream, o, dO, lse, aux, ws.D, dqacc, B, S, nh,
+                      lse_mult);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
@@ -887,8 +892,7 @@ cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, size_t n_el
   const size_t n8 = n_elems / 8;
   const unsigned grid = static_cast<unsigned>((n8 + 255) / 256);
   if (grid == 0) return cudaSuccess;
-  dq_convert_kernel<<<grid, 256, 0, stream>>>(dqacc, dq, n8, scale);
-  return cudaGetLastError();
+  return launch_pdl(dq_convert_kernel, grid, 256, 0, stream, dqacc, dq, n8, scale);
 }
 
 }  // namespace xattn

@@ -148,6 +148,8 @@ __global__ void __maxnreg__(168)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  grid_dep_launch();
+  grid_dep_wait();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
   auto tS = [&](int x) { return tmem + 128u * x; };
   auto tO = [&](int x) { return tmem + 256u + 64u * x; };
@@ -335,7 +337,11 @@ __global__ void __maxnreg__(168)
         const float mnew = fmaxf(mrow, mx);
         const bool rescale = __any_sync(0xffffffffu, mnew > mrow + 8.0f);
         const float m_use = rescale ? mnew : mrow;
-        const float alpha = rescale ? ex2_approx(mrow - mnew) : 1.f;
+        // rescale is warp-uniform, so this is a uniform branch: the common path issues no
+        // special-function op here (one would queue behind the other warpgroup's
+        // exponentials on the shared unit).
+        float alpha = 1.f;
+        if (rescale) alpha = ex2_approx(mrow - mnew);
         const float neg_m = -m_use;
         // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
         // included), the exponentials, row sums and bf16 P, packed in place into r[0, 64).
@@ -447,9 +453,8 @@ cudaError_t launch_fwd_sign(const CUtensorMap &mq, const CUtensorMap &mk, const 
   const int num_m = (S + kTileRows - 1) / kTileRows;
   const long long units = static_cast<long long>(B) * nh * ((num_m + 1) / 2);
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  attn_fwd_kernel<HD, kNegScale><<<grid, kFwdThreads, L::kDynBytes, stream>>>(
-      mq, mk, mv, o, lse, B, S, nh, nkv, scale * kLog2e, status, timeout_ns);
-  return cudaGetLastError();
+  return launch_pdl(attn_fwd_kernel<HD, kNegScale>, grid, kFwdThreads, L::kDynBytes, stream, mq, mk, mv, o,
+                    lse, B, S, nh, nkv, scale * kLog2e, status, timeout_ns);
 }
 
 template <int HD>

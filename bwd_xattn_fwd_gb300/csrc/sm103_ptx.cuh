@@ -430,6 +430,21 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ----------------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel of its stream is still running:
+// grid_dep_wait() blocks until that kernel has completed and its memory is visible (a
+// no-op for an ordinary launch), so every kernel calls it before its first global
+// memory access; what comes before it (barrier set-up, TMEM allocation, tensor-map
+// prefetch) overlaps the previous kernel's tail. grid_dep_launch() allows the next
+// kernel of the stream to begin launching once every CTA of this grid has called it.
+// ----------------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 #undef XATTN_R8
 #undef XATTN_W8
 

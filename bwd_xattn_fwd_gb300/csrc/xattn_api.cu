@@ -39,6 +39,15 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
+}  // namespace
+
+bool pdl_enabled() {
+  static const bool v = std::getenv("XATTN_NO_PDL") == nullptr;
+  return v;
+}
+
+namespace {
+
 xattn_status device_info(DeviceInfo **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return XATTN_ERR_CUDA;

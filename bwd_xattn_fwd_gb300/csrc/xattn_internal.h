@@ -13,6 +13,28 @@ constexpr int kTileRows = 128;                  // rows of Q / K / V per tile
 constexpr float kLog2e = 1.4426950408889634f;   // 1 / ln 2
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Launches kernel<<<grid, threads, smem, stream>>>(args...) with programmatic stream
+// serialization, so that its set-up overlaps the tail of the previous kernel in the
+// stream (each kernel waits for its predecessor with griddepcontrol.wait before touching
+// global memory). XATTN_NO_PDL in the environment turns this off (ordinary launches).
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned threads, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Rows of the per-(batch, head) workspace vectors, padded to whole tiles.
 __host__ __device__ inline int padded_rows(int S) { return (S + kTileRows - 1) / kTileRows * kTileRows; }
 
