@@ -65,7 +65,7 @@ class OracleLib:
     def __init__(self, mutation: int = 0):
         self.mutation = mutation
         self._lib = ctypes.CDLL(build(mutation))
-        for name in ("xo_fwd", "xo_bwd"):
+        for name in ("xo_fwd", "xo_bwd", "xo_decode"):
             getattr(self._lib, name).restype = None
         self._lib.xo_mutation.restype = ctypes.c_int
         assert self._lib.xo_mutation() == mutation
@@ -98,6 +98,23 @@ class OracleLib:
         self._lib.xo_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), B, S, nh, nkv, hd,
                          ctypes.c_double(scale), _ptr(dq), _ptr(dk), _ptr(dv))
         return dq, dk, dv
+
+
+    def decode(self, q, k, v, scale):
+        """One query per sequence against its T cached keys/values.
+
+        q [B, nh, hd], k, v [B, T, nkv, hd] -> (o [B, nh, hd], lse [B, nh]) in float64.
+        """
+        q, k, v = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v))
+        B, nh, hd = q.shape
+        Bk, T, nkv, hdk = k.shape
+        if (Bk, hdk) != (B, hd) or v.shape != k.shape or T <= 0 or nkv <= 0 or nh % nkv != 0:
+            raise ValueError(f"bad shapes q{q.shape} k{k.shape} v{v.shape}")
+        o = np.empty_like(q)
+        lse = np.empty((B, nh), dtype=np.float64)
+        self._lib.xo_decode(_ptr(q), _ptr(k), _ptr(v), B, T, nh, nkv, hd, ctypes.c_double(scale),
+                            _ptr(o), _ptr(lse))
+        return o, lse
 
 
 _default = None

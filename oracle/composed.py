@@ -67,3 +67,22 @@ def backward(q, k, v, dO, scale):
     dk = _sum_groups(np.swapaxes(dk_rep, 1, 2), nkv)
     dv = _sum_groups(np.swapaxes(dv_rep, 1, 2), nkv)
     return dq, dk, dv
+
+
+def decode(q, k, v, scale):
+    """One new query per sequence against its cached K/V (xtrain "演进总览", milestone
+    M2a: single query x cached K/V through a strided GEMM and a plain softmax).
+
+    q [B, nh, hd], k, v [B, T, nkv, hd] -> (o [B, nh, hd], lse [B, nh]). No mask: the
+    query is the newest position, so every cached key is visible.
+    """
+    nh, nkv = q.shape[1], k.shape[2]
+    g = nh // nkv
+    kh = np.swapaxes(_repeat_kv(k, g), 1, 2)          # [B, nh, T, hd]
+    vh = np.swapaxes(_repeat_kv(v, g), 1, 2)
+    s = scale * np.einsum("bhd,bhtd->bht", q, kh)
+    m = s.max(axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    z = e.sum(axis=-1, keepdims=True)
+    o = np.einsum("bht,bhtd->bhd", e / z, vh)
+    return o, (m + np.log(z))[..., 0]

@@ -32,6 +32,16 @@
  * LSE uses the row maximum as a shift only to avoid overflow of exp; that does not
  * change the value. All tensors are row-major [B, S, heads, hd] (lse: [B, S, nh]).
  *
+ * Decode (xtrain "演进总览", post-training milestones M2a-M2c: one new query per
+ * sequence against that sequence's cached keys and values, equal to the last row of
+ * full causal attention, batch-agnostic over the sequences), xo_decode:
+ *
+ *   s_j = scale * sum_d q[b,h,d] * k[b,j,kvh,d]      for every cached j < T
+ *   LSE = log( sum_j exp(s_j) ) ,  O = sum_j exp(s_j - LSE) v[b,j,kvh,:]
+ *
+ * with q, o [B, nh, hd], k, v [B, T, nkv, hd], lse [B, nh]. The query sits at the
+ * newest position, so all T cached keys, its own included, are visible.
+ *
  * ORACLE_MUTATION (compile-time, tests only): a nonzero value plants one known
  * mistake, so the test suite can show that its pins catch it. The default build
  * has ORACLE_MUTATION == 0 and contains none of them.
@@ -230,4 +240,41 @@ void xo_bwd(const double *q, const double *k, const double *v, const double *dO,
 }
 
 /* Build identification for the test suite (which mutation, if any, was compiled in). */
+/*
+ * Decode: q [B,nh,hd], k/v [B,T,nkv,hd] -> o [B,nh,hd], lse [B,nh].
+ */
+void xo_decode(const double *q, const double *k, const double *v, int B, int T, int nh, int nkv,
+               int hd, double scale, double *o, double *lse) {
+#if ORACLE_MUTATION == 10
+    const int n_keys = T - 1;     /* planted: the newest cached key left out */
+#else
+    const int n_keys = T;
+#endif
+    long total = (long)B * nh;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long t = 0; t < total; ++t) {
+        int h = (int)(t % nh);
+        int b = (int)(t / nh);
+        int kvh = kv_head_of(h, nh, nkv);
+        const double *qh = &q[((size_t)b * nh + h) * hd];
+        double mx = -INFINITY;
+        for (int j = 0; j < n_keys; ++j) {
+            double s = scale * dot(qh, &k[IDX4(b, j, kvh, 0, T, nkv, hd)], hd);
+            if (s > mx) mx = s;
+        }
+        double sum = 0.0;
+        for (int j = 0; j < n_keys; ++j)
+            sum += exp(scale * dot(qh, &k[IDX4(b, j, kvh, 0, T, nkv, hd)], hd) - mx);
+        double L = mx + log(sum);
+        lse[(size_t)b * nh + h] = L;
+        double *oh = &o[((size_t)b * nh + h) * hd];
+        for (int d = 0; d < hd; ++d) oh[d] = 0.0;
+        for (int j = 0; j < n_keys; ++j) {
+            double p = exp(scale * dot(qh, &k[IDX4(b, j, kvh, 0, T, nkv, hd)], hd) - L);
+            const double *vj = &v[IDX4(b, j, kvh, 0, T, nkv, hd)];
+            for (int d = 0; d < hd; ++d) oh[d] += p * vj[d];
+        }
+    }
+}
+
 int xo_mutation(void) { return ORACLE_MUTATION; }

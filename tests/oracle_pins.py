@@ -7,7 +7,9 @@ reused by ``test_oracle_mutations.py``, which shows that each planted mistake in
 oracle fails at least one pin.
 
 The function being pinned is causal softmax attention with grouped KV heads and its
-gradient (xtrain "演进总览" / docs/evolution.md, phase table rows T14 and T15).
+gradient (xtrain "演进总览" / docs/evolution.md, phase table rows T14 and T15), and the
+decode form of the same attention: one new query per sequence against its cached keys
+and values (same page, post-training milestones M2a-M2c).
 """
 from __future__ import annotations
 
@@ -200,6 +202,51 @@ def pin_key_shift(orc):
     assert np.abs(lse2 - lse - scale * (q * c).sum(-1)).max() < 1e-12
 
 
+def _decode_problem(B=2, T=13, nh=4, nkv=2, hd=5, seed=11):
+    rng = np.random.default_rng(seed)
+    return _rand((B, nh, hd), rng), _rand((B, T, nkv, hd), rng), _rand((B, T, nkv, hd), rng)
+
+
+def pin_decode_last_row(orc):
+    """Decode equals the last row of full causal attention (milestone M2a's own gate):
+    with the query placed at position T-1 of a full sequence, the causal forward's last
+    row and LSE are the decode's output."""
+    q, k, v = _decode_problem()
+    B, T, nh, hd = 2, 13, 4, 5
+    rng = np.random.default_rng(12)
+    q_full = _rand((B, T, nh, hd), rng)
+    q_full[:, T - 1] = q
+    scale = 0.8
+    o_full, lse_full = orc.fwd(q_full, k, v, scale)
+    o, lse = orc.decode(q, k, v, scale)
+    assert _rel(o, o_full[:, T - 1]) < 1e-12
+    assert np.abs(lse - lse_full[:, T - 1]).max() < 1e-12
+
+
+def pin_decode_closed_forms(orc):
+    """T = 1: O = v_0 and LSE = scale q.k_0. q = 0: O is the mean of the cached V rows of
+    the query's kv head (contiguous groups) and LSE = ln T."""
+    q, k, v = _decode_problem(T=1, seed=13)
+    scale = 0.45
+    o, lse = orc.decode(q, k, v, scale)
+    kv_of = np.arange(4) // 2
+    assert _rel(o, v[:, 0, kv_of]) < 1e-14
+    assert np.abs(lse - scale * np.einsum("bhd,bhd->bh", q, k[:, 0, kv_of])).max() < 1e-13
+    q, k, v = _decode_problem(T=10, seed=14)
+    o, lse = orc.decode(np.zeros_like(q), k, v, scale)
+    assert _rel(o, v.mean(axis=1)[:, kv_of]) < 1e-13
+    assert np.abs(lse - math.log(10)).max() < 1e-13
+
+
+def pin_decode_composed(orc):
+    """Decode against the composed formulation (repeated K/V, materialised scores)."""
+    q, k, v = _decode_problem(B=3, T=21, nh=8, nkv=2, hd=6, seed=15)
+    o, lse = orc.decode(q, k, v, 1.3)
+    o2, lse2 = composed.decode(q, k, v, 1.3)
+    assert _rel(o, o2) < 1e-12 and np.abs(lse - lse2).max() < 1e-12
+
+
 PINS = [pin_golden_two_positions, pin_zero_queries, pin_single_position, pin_constant_values,
         pin_finite_differences, pin_composed, pin_torch_sdpa, pin_gqa_equals_repeated_mha,
-        pin_invariants, pin_key_shift]
+        pin_invariants, pin_key_shift, pin_decode_last_row, pin_decode_closed_forms,
+        pin_decode_composed]

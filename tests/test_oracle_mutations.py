@@ -14,6 +14,7 @@ MUTATIONS = {
     6: "LSE with a base-2 log",
     7: "dQ gathers the key at the query's row",
     9: "scale applied twice to the scores",
+    10: "decode leaves out the newest cached key",
 }
 
 
