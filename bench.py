@@ -7,6 +7,10 @@ flushed by a 256 MiB device write before every step, outside the timed events.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload gqa] [--impl ours|reference]
 
+With --workload decode it times one decode step instead (xattn_decode: one new query
+per sequence against 4096 cached positions, 64 sequences) and reports GB/s of cache
+reads against the measured HBM copy bandwidth.
+
 Prints ONE JSON line (rank 0). `value` is fwd+bwd TFLOP/s of algorithmic work
 (4 hd flops per causal pair forward, 10 hd backward) summed over all ranks and divided
 by the slowest rank's time. `--impl reference` times the CPU oracle on the host cores
@@ -44,7 +48,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="gqa", choices=[n for n in W.ORDER if n != "tiny"])
+    ap.add_argument("--workload", default="gqa",
+                    choices=[n for n in W.ORDER if n != "tiny"] + list(W.DECODE_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -439,8 +444,158 @@ def run_ours(args, w: W.Workload):
         pg.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------------------
+# decode mode: one decode step (one new query per sequence against its cached K/V)
+# ---------------------------------------------------------------------------------------
+DECODE_METRIC = "decode attention GB/s of KV-cache reads (bf16), % of GB300 HBM copy bandwidth"
+
+
+def decode_oracle_sample(w, x_cpu, budget_s: float, max_seqs=None):
+    """Times the oracle's decode (fp64, all host cores) on whole sequences, in order."""
+    cores = os.cpu_count() or 1
+    os.environ["OMP_NUM_THREADS"] = str(cores)
+    import oracle
+    orc = oracle.default()
+    n = w.B if max_seqs is None else min(max_seqs, w.B)
+    done, elapsed = 0, 0.0
+    for b in range(n):
+        q, k, v = (W.as_f64(x_cpu[name][b:b + 1]) for name in ("q", "k", "v"))
+        t0 = time.perf_counter()
+        orc.decode(q, k, v, w.scale)
+        elapsed += time.perf_counter() - t0
+        done += 1
+        if elapsed >= budget_s:
+            break
+    frac = done / w.B
+    return {"bytes": w.io_bytes * frac, "seqs": done, "seconds": elapsed, "cores": cores,
+            "sample": f"{done} of {w.B} sequences of '{w.name}' (T={w.T}, {w.nh} query heads), fp64, "
+                      f"OpenMP over heads"}
+
+
+def run_decode_reference(args, w):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    x = W.make_decode_inputs(w, seed=0)
+    for _ in range(args.warmup):
+        decode_oracle_sample(w, x, 0.0, max_seqs=1)
+    per = [decode_oracle_sample(w, x, 0.0, max_seqs=1) for _ in range(args.steps)]
+    secs = sum(p["seconds"] for p in per)
+    value = sum(p["bytes"] for p in per) / secs / 1e9
+    line = {"impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "T": w.T, "nh": w.nh, "nkv": w.nkv, "hd": w.hd,
+                       "step": "one sequence's decode"},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": per[0]["cores"], "kind": "oracle",
+                             "sample": per[0]["sample"] + " per step"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_decode(args, w):
+    import torch
+    rank, local, world, pg = dist_setup(args.gpus)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    from bwd_xattn_fwd_gb300 import xattn
+    x_cpu = W.make_decode_inputs(w, seed=rank)
+    x = {n: t.to(dev) for n, t in x_cpu.items()}
+    B, T, nh, nkv, hd, scale = w.B, w.T, w.nh, w.nkv, w.hd, w.scale
+    o = torch.empty_like(x["q"])
+    lse = torch.empty((B, nh), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        xattn.xattn_decode(x["q"], x["k"], x["v"], B, T, nh, nkv, hd, scale, o, lse, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if xattn.xattn_check_device_status(stream) != 0:
+        raise RuntimeError("device status during warm-up")
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    barrier(pg)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(pg)
+    if xattn.xattn_check_device_status(stream) != 0:
+        raise RuntimeError("device status in the timed region")
+    total_ms = max_over_ranks(pg, sum(e[0].elapsed_time(e[1]) for e in evs), dev)
+    ms = total_ms / args.steps
+    value = w.io_bytes * world * args.steps / (total_ms * 1e-3) / 1e9
+    pk = peaks()
+    roofline = {"kernel": "decode_partial_kernel + decode_combine_kernel", "bound": "hbm",
+                "achieved": value / world, "peak": pk["gbs"], "unit": "GB/s",
+                "frac": value / world / pk["gbs"], "traffic": None,
+                "algorithmic_per_launch": w.io_bytes, "peak_source": pk["source"] + " (copy)"}
+
+    e2e = None
+    if not args.no_e2e:
+        h_q = x_cpu["q"].pin_memory()
+        h_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        h_l = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        d_q = torch.empty_like(x["q"])
+
+        def e2e_step():
+            d_q.copy_(h_q, non_blocking=True)
+            xattn.xattn_decode(d_q, x["k"], x["v"], B, T, nh, nkv, hd, scale, o, lse, stream)
+            h_o.copy_(o, non_blocking=True)
+            h_l.copy_(lse, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        t = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+        e2e = {"value": w.io_bytes * world * args.steps / (t * 1e-3) / 1e9, "unit": "GB/s",
+               "tok_per_s": B * world * args.steps / (t * 1e-3),
+               "h2d_bytes_per_step": h_q.numel() * h_q.element_size(),
+               "d2h_bytes_per_step": h_o.numel() * h_o.element_size() + h_l.numel() * h_l.element_size(),
+               "note": "the K/V caches stay resident on the device (as in a decode loop); the new "
+                       "token's query comes in and the output goes out each step"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = decode_oracle_sample(w, x_cpu, budget_s=10.0)
+        cpu = {"value": r["bytes"] / r["seconds"] / 1e9, "unit": "GB/s", "cores": r["cores"],
+               "kind": "oracle", "sample": r["sample"], "seconds": r["seconds"]}
+    if rank == 0:
+        line = {"metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": w.name, "B": B, "T": T, "nh": nh, "nkv": nkv, "hd": hd,
+                           "parallelism": f"{world} rank(s), each its own sequences; no collective",
+                           "l2": "flushed before every step (256 MiB device write, outside the timed "
+                                 "events); the caches (%.0f MB) exceed the L2 as well" % (w.cache_bytes / 1e6)},
+                "tok_per_s": B * world / (ms * 1e-3), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def main():
     args = parse()
+    if args.workload in W.DECODE_WORKLOADS:
+        w = W.DECODE_WORKLOADS[args.workload]
+        if args.impl == "reference":
+            run_decode_reference(args, w)
+        else:
+            run_decode(args, w)
+        return
     w = W.WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

@@ -20,10 +20,10 @@ constexpr float kLn2 = 0.6931471805599453f;
 bool pdl_enabled();
 
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned threads, size_t smem,
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, unsigned threads, size_t smem,
                        cudaStream_t stream, Args &&...args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -84,6 +84,16 @@ cudaError_t launch_bwd_dq_bf16(const CUtensorMap &mq, const CUtensorMap &mk, con
                                const CUtensorMap &mdo, const float *lse, const BwdWorkspace &ws,
                                __nv_bfloat16 *dq, int B, int S, int nh, int nkv, int hd, float scale,
                                int *status, uint64_t timeout_ns, cudaStream_t stream);
+
+// Decode (one query per sequence against its T cached keys/values), bf16, hd in
+// {32, 64, 128}, group = nh / nkv <= kMaxDecodeGroup. The workspace holds each 256-key
+// chunk's (max, sum, partial O) per query head: decode_workspace_bytes() bytes.
+constexpr int kDecodeChunk = 256;
+constexpr int kMaxDecodeGroup = 16;
+size_t decode_workspace_bytes(int B, int T, int nh, int hd);
+cudaError_t launch_decode_bf16(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+                               __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, int hd,
+                               float scale, void *workspace, cudaStream_t stream);
 
 // fp32 CUDA-core path (hd <= 128).
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,

@@ -111,6 +111,61 @@ def make_inputs(w: Workload, seed: int = 0):
             (("q", q), ("k", k), ("v", v), ("dO", dO))}
 
 
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One decode step: B sequences, each one new query (all nh heads) against its T
+    cached key/value positions (xtrain "演进总览", milestones M2a-M2c)."""
+    name: str
+    B: int
+    T: int
+    nh: int
+    nkv: int
+    hd: int
+    qkv_scale: float = 0.5
+    description: str = ""
+
+    @property
+    def group(self) -> int:
+        return self.nh // self.nkv
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.hd)
+
+    @property
+    def cache_bytes(self) -> int:
+        """bf16 K and V caches, read once per step."""
+        return 2 * self.B * self.T * self.nkv * self.hd * 2
+
+    @property
+    def io_bytes(self) -> int:
+        """Algorithmic bytes per step: the caches, q and o (bf16), lse (fp32)."""
+        return self.cache_bytes + 2 * self.B * self.nh * self.hd * 2 + self.B * self.nh * 4
+
+    def with_(self, **kw) -> "DecodeWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+DECODE_WORKLOADS = {
+    # The long workload's heads (nh=16, nkv=4, hd=64) over 64 sequences with 4096 cached
+    # positions each: 268 MB of cache per step, more than the L2 holds.
+    "decode": DecodeWorkload("decode", B=64, T=4096, nh=16, nkv=4, hd=64,
+                             description="decode step, 64 sequences x 4096 cached positions, GQA group 4"),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload, seed: int = 0):
+    """Returns dict(q [B,nh,hd], k [B,T,nkv,hd], v [B,T,nkv,hd]) of bf16 CPU tensors:
+    generator seeded as for make_inputs, draw order q, k, v, each torch.randn in
+    float32 times qkv_scale, then cast to bf16."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    q = torch.randn((w.B, w.nh, w.hd), generator=g, dtype=torch.float32)
+    k = torch.randn((w.B, w.T, w.nkv, w.hd), generator=g, dtype=torch.float32)
+    v = torch.randn((w.B, w.T, w.nkv, w.hd), generator=g, dtype=torch.float32)
+    return {name: (t * w.qkv_scale).to(torch.bfloat16).contiguous() for name, t in
+            (("q", q), ("k", k), ("v", v))}
+
+
 def as_f64(t: torch.Tensor):
     """Exact float64 numpy copy of a CPU tensor (bf16 and fp32 embed exactly)."""
     return t.detach().to("cpu", torch.float64).numpy()

@@ -66,6 +66,7 @@ _SIGS = {
     "xattn_bwd_deterministic": [_vp] * 5 + [_vp] + [_i] * 5 + [_f] + [_vp] * 4,
     "xattn_fwd_f32": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp],
     "xattn_bwd_f32": [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp],
+    "xattn_decode": [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp],
     "xattn_check_device_status": [_vp],
 }
 for _name, _args in _SIGS.items():
@@ -168,6 +169,11 @@ def xattn_bwd_f32(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, str
           nh, nkv, hd, scale, _addr(dq), _addr(dk), _addr(dv), _stream(stream))
 
 
+def xattn_decode(q, k_cache, v_cache, B, T, nh, nkv, hd, scale, o, lse, stream=None):
+    _call("xattn_decode", _addr(q), _addr(k_cache), _addr(v_cache), B, T, nh, nkv, hd, scale, _addr(o),
+          _addr(lse), _stream(stream))
+
+
 def xattn_status_string(status: int) -> str:
     return status_string(status)
 
@@ -216,3 +222,16 @@ def attention_bwd(q, k, v, o, dO, lse, scale=None, stream=None, deterministic=Fa
     else:
         raise TypeError(f"unsupported dtype {q.dtype}")
     return dq, dk, dv
+
+
+def attention_decode(q, k_cache, v_cache, scale=None, stream=None):
+    """(o [B,nh,hd], lse [B,nh]) for one new query per sequence: q [B,nh,hd] against the
+    cached k/v [B,T,nkv,hd] (bf16, contiguous CUDA tensors)."""
+    import torch
+    B, nh, hd = (int(x) for x in q.shape)
+    T, nkv = int(k_cache.shape[1]), int(k_cache.shape[2])
+    scale = float(hd ** -0.5 if scale is None else scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, nh), dtype=torch.float32, device=q.device)
+    xattn_decode(q, k_cache, v_cache, B, T, nh, nkv, hd, scale, o, lse, stream)
+    return o, lse

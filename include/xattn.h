@@ -167,6 +167,29 @@ xattn_status xattn_bwd_f32(const float *q, const float *k, const float *v, const
                            void *stream);
 
 /* Static text for a status code (never NULL). */
+/*
+ * Decode attention, bf16 (xtrain docs/evolution.md, post-training milestones M2a-M2c):
+ * one new query per sequence against that sequence's cached keys and values -- equal to
+ * the last row of full causal attention over the T cached positions, which include the
+ * query's own (so every cached key is visible; there is no mask). Batch-agnostic: the B
+ * sequences are independent and share T.
+ *   q      [B, nh, hd]      bf16, the new token's query heads
+ *   k, v   [B, T, nkv, hd]  bf16, the caches, row-major like the [B, S, heads, hd]
+ *                           tensors of xattn_fwd (position T-1 is the new token)
+ *   o      [B, nh, hd]      bf16 out;  lse [B, nh] float out (natural log of the sum of
+ *                           exp of the scaled scores, as xattn_fwd's lse)
+ * Query head h reads kv head h / (nh / nkv). hd in {32, 64, 128}; nh / nkv <= 16
+ * (else XATTN_ERR_GROUP); 1 <= T <= 65535 * 256; any finite scale. q, k, v, o 16-byte
+ * aligned, lse 4-byte aligned.
+ * Arithmetic: fp32 products and softmax statistics on bf16 inputs; o rounded to nearest
+ * even. Scratch (B * nh * ceil(T / 256) * (hd + 2) floats: per 256-key chunk the
+ * maximum, sum and unnormalised output of each query head) is taken with
+ * cudaMallocAsync on `stream` and released with cudaFreeAsync; nothing else is
+ * allocated. The result is bit-for-bit reproducible (fixed reduction order).
+ */
+xattn_status xattn_decode(const void *q, const void *k_cache, const void *v_cache, int B, int T,
+                          int nh, int nkv, int hd, float scale, void *o, float *lse, void *stream);
+
 const char *xattn_status_string(xattn_status status);
 
 /*

@@ -124,3 +124,27 @@ def test_no_device_is_a_cuda_error(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fwd(lib) == 6
+
+
+def _decode(lib, q=16, k=32, v=48, B=2, T=5, nh=4, nkv=2, hd=64, scale=0.125, o=64, lse=80):
+    f = lib.xattn_decode
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 3
+    return f(q, k, v, B, T, nh, nkv, hd, scale, o, lse, None)
+
+
+def test_decode_argument_checks(lib):
+    assert _decode(lib, k=None) == 1                    # NULL pointer
+    assert _decode(lib, lse=None) == 1
+    assert _decode(lib, T=0) == 2                       # bad shape
+    assert _decode(lib, B=-2) == 2
+    assert _decode(lib, nh=6, nkv=4) == 3               # nh % nkv != 0
+    assert _decode(lib, nh=34, nkv=2) == 3              # group above 16
+    assert _decode(lib, hd=48) == 4                     # head dims 32, 64, 128 only
+    assert _decode(lib, hd=256) == 4
+    assert _decode(lib, v=56) == 5                      # not 16-byte aligned
+    assert _decode(lib, lse=82) == 5                    # lse not 4-byte aligned
+    assert _decode(lib, scale=float("nan")) == 9
+    import torch
+    if not torch.cuda.is_available():
+        assert _decode(lib, hd=128, nh=32, nkv=2) == 6  # accepted; no GPU here
