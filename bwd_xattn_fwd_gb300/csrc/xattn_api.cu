@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "xattn.h"
+#include "sm103_ptx.cuh"
 #include "xattn_internal.h"
 
 namespace xattn {
@@ -47,6 +48,23 @@ bool pdl_enabled() {
 }
 
 namespace {
+
+// Self-test of the bounded waits: one CTA waits on an mbarrier that nothing ever arrives
+// on (phase 0 of a barrier expecting one arrival), with the same wait the kernels use.
+// The wait runs out after limit_ns and records XATTN_ERR_DEVICE_TIMEOUT in the status
+// word; nothing else happens on the device.
+__global__ void wait_selftest_kernel(int *status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, status, limit_ns};
+  (void)mbar_wait(smem_u32(&bar), 0, ctl);
+}
 
 xattn_status device_info(DeviceInfo **out) {
   int dev = 0;
@@ -395,6 +413,14 @@ const char *xattn_status_string(xattn_status s) {
       return "these sizes need more scratch than xattn_bwd_noalloc's fixed array holds";
   }
   return "unknown xattn status";
+}
+
+xattn_status xattn_selftest_wait_timeout(unsigned long long limit_ns, void *stream) {
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull) return XATTN_ERR_BAD_SHAPE;
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(device_info(&dev));
+  wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status, limit_ns);
+  return cuda_status(cudaGetLastError());
 }
 
 xattn_status xattn_check_device_status(void *stream) {

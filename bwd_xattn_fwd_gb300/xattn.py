@@ -174,6 +174,15 @@ def xattn_decode(q, k_cache, v_cache, B, T, nh, nkv, hd, scale, o, lse, stream=N
           _addr(lse), _stream(stream))
 
 
+def xattn_selftest_wait_timeout(limit_ns, stream=None):
+    fn = _lib.xattn_selftest_wait_timeout
+    fn.argtypes = [ctypes.c_ulonglong, _vp]
+    fn.restype = ctypes.c_int
+    st = fn(int(limit_ns), _stream(stream))
+    if st != 0:
+        raise XattnError(st, "xattn_selftest_wait_timeout")
+
+
 def xattn_status_string(status: int) -> str:
     return status_string(status)
 

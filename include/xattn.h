@@ -199,6 +199,18 @@ const char *xattn_status_string(xattn_status status);
  */
 xattn_status xattn_check_device_status(void *stream);
 
+/*
+ * Self-test of failure detection (no counterpart on the pages, which have none for
+ * attention). Every wait of this library's kernels is bounded: past the limit the kernel
+ * records XATTN_ERR_DEVICE_TIMEOUT in a device status word, stops and frees what it
+ * holds, and the context stays usable. This call launches one small kernel whose only
+ * work is such a wait on a barrier that nothing completes, with the given limit (1 us to
+ * 10 s, else XATTN_ERR_BAD_SHAPE), so a test can see the timeout reported by
+ * xattn_check_device_status without any kernel of the attention path failing.
+ * Asynchronous on `stream`; returns XATTN_OK once launched.
+ */
+xattn_status xattn_selftest_wait_timeout(unsigned long long limit_ns, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

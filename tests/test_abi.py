@@ -148,3 +148,11 @@ def test_decode_argument_checks(lib):
     import torch
     if not torch.cuda.is_available():
         assert _decode(lib, hd=128, nh=32, nkv=2) == 6  # accepted; no GPU here
+
+
+def test_selftest_limit_checks(lib):
+    f = lib.xattn_selftest_wait_timeout
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+    assert f(0, None) == 2
+    assert f(20 * 10**9, None) == 2
