@@ -183,3 +183,27 @@ def test_stage_calls_match_bwd():
     assert torch.equal(dk, dk2) and torch.equal(dv, dv2)
     assert (dq.float() - dq2.float()).abs().max() <= TOL_BF16 * dq.float().abs().max()
     assert xattn.xattn_check_device_status() == 0
+
+
+def test_right_padded_ragged_batch():
+    """Ragged sequences right-padded to one length (xtrain "演进总览", milestone M2d: under
+    causal masking the real rows never see the padding, so a padded batch needs no
+    per-sequence lengths). The pad rows' inputs are garbage and their output gradient is
+    zero (the loss masks them); every real row of O, LSE, dQ and every real key's dK, dV
+    must then match the oracle run on that sequence alone."""
+    lengths, S = [300, 129, 57], 300
+    w = W.Workload("pad", len(lengths), S, 8, 2, 64, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=11)
+    g = torch.Generator().manual_seed(12)
+    for b, L in enumerate(lengths):
+        for n in ("q", "k", "v"):
+            junk = torch.randn(x[n][b, L:].shape, generator=g) * 3.0
+            x[n][b, L:] = junk.to(x[n].dtype)
+        x["dO"][b, L:] = 0
+    out = run_gpu(w, x)
+    for b, L in enumerate(lengths):
+        wb = w.with_(B=1, S=L)
+        xb = {n: x[n][b:b + 1, :L].contiguous() for n in x}
+        ref = oracle_full(wb, xb)
+        got = {n: out[n][b:b + 1, :L] for n in out}
+        compare(got, ref, "bf16", f"sequence {b} (length {L})")
