@@ -8,8 +8,9 @@
 // GB300 mapping: a unit of work is one pair of 128-row query tiles A = 2j and B = 2j+1
 // of one (batch, head) -- 256 query rows that share every K/V tile they read. Persistent
 // CTAs, one per SM, take the units in turn (longest first). 12 warps:
-//   warp 0     : TMA producer. Q_A and Q_B once per unit; K/V tiles through a 3-stage
-//                ring that runs on across units.
+//   warp 0     : TMA producer. Q_A and Q_B once per unit, into one of two buffers, so a
+//                unit's query tiles land while the previous unit still runs; K/V tiles
+//                through a 3-stage ring that runs on across units.
 //   warp 1     : TMEM owner and MMA issuer (converged warp, one elected lane issues):
 //                  S_X(n) = Q_X K_n^T  (A, B from shared memory) -> TMEM
 //                  O_X   += P_X(n) V_n (A = P from TMEM)          -> TMEM accumulator
@@ -42,13 +43,13 @@ struct FwdLayout {
   static constexpr uint32_t kRowBytes = HD * 2;
   static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
   static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
-  static constexpr uint32_t kQ = 0;                                  // Q_A, Q_B
-  static constexpr uint32_t kK = kQ + 2 * kTileBytes;
+  static constexpr uint32_t kQ = 0;                                  // 2 x (Q_A, Q_B)
+  static constexpr uint32_t kK = kQ + 4 * kTileBytes;
   static constexpr uint32_t kV = kK + kFwdStages * kTileBytes;
   static constexpr uint32_t kBars = kV + kFwdStages * kTileBytes;
-  // barriers: q_full, full[S], empty[S], s_full[2], p_full[2], o_done[2], mma_final,
-  //           s_free[2], o_free[2]
-  static constexpr int kNumBars = 1 + 2 * kFwdStages + 2 + 2 + 2 + 1 + 2 + 2;
+  // barriers: full[S], empty[S], s_full[2], p_full[2], o_done[2], s_free[2], o_free[2],
+  //           q_full[2], mma_final[2] (one each per Q buffer)
+  static constexpr int kNumBars = 2 * kFwdStages + 2 + 2 + 2 + 2 + 2 + 2 + 2;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   // Ask for enough shared memory that one CTA occupies an SM: each CTA holds all 512
@@ -105,22 +106,23 @@ __global__ void __maxnreg__(168)
   const uint32_t sV = smem_u32(smem + L::kV);
   const uint32_t bar0 = smem_u32(smem + L::kBars);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const uint32_t q_full = bar(0);
-  auto full = [&](int s) { return bar(1 + s); };
-  auto empty = [&](int s) { return bar(1 + kFwdStages + s); };
-  auto s_full = [&](int x) { return bar(1 + 2 * kFwdStages + x); };
-  auto p_full = [&](int x) { return bar(3 + 2 * kFwdStages + x); };
-  auto o_done = [&](int x) { return bar(5 + 2 * kFwdStages + x); };
-  const uint32_t mma_final = bar(7 + 2 * kFwdStages);                // a unit's products done
-  auto s_free = [&](int x) { return bar(8 + 2 * kFwdStages + x); };
-  auto o_free = [&](int x) { return bar(10 + 2 * kFwdStages + x); };   // O_X read by the epilogue
+  auto full = [&](int s) { return bar(s); };
+  auto empty = [&](int s) { return bar(kFwdStages + s); };
+  auto s_full = [&](int x) { return bar(2 * kFwdStages + x); };
+  auto p_full = [&](int x) { return bar(2 + 2 * kFwdStages + x); };
+  auto o_done = [&](int x) { return bar(4 + 2 * kFwdStages + x); };
+  auto s_free = [&](int x) { return bar(6 + 2 * kFwdStages + x); };
+  auto o_free = [&](int x) { return bar(8 + 2 * kFwdStages + x); };   // O_X read by the epilogue
+  // Q buffer qb (units alternate between the two): its tiles landed / the unit's products
+  // that read them are done. Each completes once per use of its buffer, every two units.
+  auto q_full = [&](int qb) { return bar(10 + 2 * kFwdStages + qb); };
+  auto mma_final = [&](int qb) { return bar(12 + 2 * kFwdStages + qb); };
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(q_full, 1);
     // Each K/V stage is released by both MMA issuers (warp 1 for tile A, warp 3 for B).
     for (int s = 0; s < kFwdStages; ++s) {
       mbar_init(full(s), 1);
@@ -133,7 +135,10 @@ __global__ void __maxnreg__(168)
       mbar_init(s_free(x), 128);
       mbar_init(o_free(x), 128);
     }
-    mbar_init(mma_final, 2);
+    for (int qb = 0; qb < 2; ++qb) {
+      mbar_init(q_full(qb), 1);
+      mbar_init(mma_final(qb), 2);
+    }
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -158,9 +163,9 @@ __global__ void __maxnreg__(168)
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
     // The K/V ring runs on across units (ring index R counts tiles over all of them). A
-    // unit's first kFwdStages tiles only need stages released by earlier units, so they
-    // are issued before waiting for the previous unit's products (mma_final): only then
-    // are Q_A and Q_B overwritten.
+    // unit's Q tiles go to buffer units % 2 once the products of the unit two before it
+    // (the buffer's previous user) are done -- normally long before -- so they land while
+    // the previous unit still runs; then the unit's K/V tiles as stages come free.
     int units = 0, R = 0, issued = 0;
     auto load_kv = [&](int n, int kvh, int b) -> bool {
       const int s = R % kFwdStages;
@@ -177,19 +182,19 @@ __global__ void __maxnreg__(168)
       const int u = unit_at(k);
       if (u >= num_units) break;
       XATTN_FWD_UNIT(u);
-      const int pre = n_last + 1 < kFwdStages ? n_last + 1 : kFwdStages;
-#pragma unroll 1
-      for (int n = 0; ok && n < pre; ++n) ok = load_kv(n, kvh, b);
-      if (!ok || !warp_wait(mma_final, (units - 1) & 1, ctl)) break;
-      mbar_expect_tx_elect(q_full, (hasB ? 2 : 1) * L::kTileBytes);
-      tma_load_4d_elect(sQ, &mq, q_full, 0, h, mA * kTileRows, b);
-      if (hasB) tma_load_4d_elect(sQ + L::kTileBytes, &mq, q_full, 0, h, mB * kTileRows, b);
+      const int qb = units & 1;
+      const uint32_t sQb = sQ + qb * 2 * L::kTileBytes;
+      // Phase units/2 - 1 of mma_final[qb]: the products of unit units - 2.
+      if (!warp_wait(mma_final(qb), ((units >> 1) & 1) ^ 1, ctl)) break;
+      mbar_expect_tx_elect(q_full(qb), (hasB ? 2 : 1) * L::kTileBytes);
+      tma_load_4d_elect(sQb, &mq, q_full(qb), 0, h, mA * kTileRows, b);
+      if (hasB) tma_load_4d_elect(sQb + L::kTileBytes, &mq, q_full(qb), 0, h, mB * kTileRows, b);
       ++units;
 #pragma unroll 1
-      for (int n = pre; ok && n <= n_last; ++n) ok = load_kv(n, kvh, b);
+      for (int n = 0; ok && n <= n_last; ++n) ok = load_kv(n, kvh, b);
     }
     // Let every copy in flight land before the CTA can exit.
-    if (units > 0) mbar_drain(q_full, (units - 1) & 1, ctl);
+    for (int j = (units > 2 ? units - 2 : 0); j < units; ++j) mbar_drain(q_full(j & 1), (j >> 1) & 1, ctl);
     for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
       mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
   } else if (warp == 1 || warp == 3) {
@@ -211,11 +216,12 @@ __global__ void __maxnreg__(168)
     const uint32_t tSx = tS(x), tOx = tO(x), tPx = tP(x);
     // Each product's MMAs and commits are issued by one elected lane; the warp then
     // reconverges.
-    auto issue_qk = [&](int s) {
+    auto issue_qk = [&](int s, int qb) {
+      const uint64_t dQb = dQ + qb * 2 * kStageDesc;
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss(tSx, dQ + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
+          mma_ss(tSx, dQb + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
         mma_commit(s_full(x));
       }
       __syncwarp();
@@ -251,14 +257,18 @@ __global__ void __maxnreg__(168)
       if (u >= num_units) break;
       XATTN_FWD_UNIT(u);
       const int mX = x == 0 ? mA : mB;
+      const int qb = units & 1;
+      // This unit's Q tiles have landed (phase units/2 of q_full[qb]). Waited for by both
+      // issuers in every unit, even without tile B, so each sees every phase in order and
+      // its mma_final arrival below can never count towards an earlier use of the buffer.
+      if (!warp_wait(q_full(qb), (units >> 1) & 1, ctl)) break;
       if (x == 0 || hasB) {
-        // The unit's first scores: Q landed, key tile 0 landed, and S_X of the previous
-        // unit read; its first PV overwrites O_X, which the previous epilogue has read.
-        ok = warp_wait(q_full, units & 1, ctl) && warp_wait(full(ring_stage(R)), ring_phase(R), ctl) &&
-             warp_wait(s_free(x), (gx - 1) & 1, ctl);
+        // The unit's first scores: key tile 0 landed, and S_X of the previous unit read;
+        // its first PV overwrites O_X, which the previous epilogue has read.
+        ok = warp_wait(full(ring_stage(R)), ring_phase(R), ctl) && warp_wait(s_free(x), (gx - 1) & 1, ctl);
         if (!ok) break;
         tc_fence_after();
-        issue_qk(ring_stage(R));
+        issue_qk(ring_stage(R), qb);
         if (!warp_wait(o_free(x), (unitsx - 1) & 1, ctl)) { ok = false; break; }
 #pragma unroll 1
         for (int n = 0; n <= mX; ++n, ++gx) {
@@ -266,7 +276,7 @@ __global__ void __maxnreg__(168)
             if (!warp_wait(s_free(x), gx & 1, ctl) ||
                 !warp_wait(full(ring_stage(R + n + 1)), ring_phase(R + n + 1), ctl)) { ok = false; break; }
             tc_fence_after();
-            issue_qk(ring_stage(R + n + 1));
+            issue_qk(ring_stage(R + n + 1), qb);
           }
           if (!warp_wait(p_full(x), gx & 1, ctl)) { ok = false; break; }
           tc_fence_after();
@@ -276,12 +286,12 @@ __global__ void __maxnreg__(168)
         if (!ok) break;
         ++unitsx;
       }
-      if (elect_one()) mma_commit(mma_final);      // covers every MMA of this unit
+      if (elect_one()) mma_commit(mma_final(qb));  // covers every MMA of this unit
       __syncwarp();
       R += n_last + 1;
       ++units;
     }
-    if (units > 0) mbar_drain(mma_final, (units - 1) & 1, ctl);
+    if (units > 0) mbar_drain(mma_final((units - 1) & 1), ((units - 1) >> 1) & 1, ctl);
   } else if (warp >= 4) {
     // ---------------- softmax + epilogue: one thread per query row of tile X ----------------
     const int x = (warp - 4) >> 2;          // 0 = tile A, 1 = tile B
