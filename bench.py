@@ -374,44 +374,73 @@ def run_ours(args, w: W.Workload):
                 "frac": d["frac"], "traffic": ncu_traffic(dominant, w.name),
                 "algorithmic_per_launch": work, "peak_source": pk["source"] + " (burst)"}
 
-    # End to end through the public API with host buffers: H2D of the step's inputs,
-    # xattn_fwd + xattn_bwd (which takes its own scratch), D2H of every output.
+    # End to end through the public API with host buffers: every step copies its inputs
+    # in from pinned host memory (H2D), runs xattn_fwd + xattn_bwd (which takes its own
+    # scratch) and copies every output back (D2H). The steps are pipelined over three
+    # streams with two sets of device buffers, as a training loop would overlap them: the
+    # H2D copies of step i+1 and the D2H copies of step i-1 run while step i computes.
     e2e = None
     if not args.no_e2e:
         h_in = {n: t.pin_memory() for n, t in x_cpu.items()}
-        d_in = {n: torch.empty_like(t, device=dev) for n, t in x_cpu.items()}
-        h_out = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                 for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
-        d_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+        d_in = [{n: torch.empty_like(t, device=dev) for n, t in x_cpu.items()} for _ in range(2)]
+        outs = (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))
+        d_out = [{n: torch.empty_like(t) for n, t in outs} for _ in range(2)]
+        h_out = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs}
+                 for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-        d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+        d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+        s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(dev) for _ in range(3))
+        h2d_done = [torch.cuda.Event() for _ in range(2)]
+        cmp_done = [torch.cuda.Event() for _ in range(2)]
+        d2h_done = [torch.cuda.Event() for _ in range(2)]
+        bwd = xattn.xattn_bwd_deterministic if args.deterministic else xattn.xattn_bwd
 
-        def e2e_step():
-            for n in h_in:
-                d_in[n].copy_(h_in[n], non_blocking=True)
-            xattn.xattn_fwd(d_in["q"], d_in["k"], d_in["v"], B, S, nh, nkv, hd, scale, o, lse, stream)
-            bwd = xattn.xattn_bwd_deterministic if args.deterministic else xattn.xattn_bwd
-            bwd(d_in["q"], d_in["k"], d_in["v"], o, d_in["dO"], lse, B, S, nh, nkv, hd, scale, dq, dk,
-                dv, stream)
-            for n in h_out:
-                h_out[n].copy_(d_out[n], non_blocking=True)
+        def e2e_step(i):
+            j = i % 2
+            di, do_, ho = d_in[j], d_out[j], h_out[j]
+            if i >= 2:
+                s_h2d.wait_event(cmp_done[j])          # step i-2 has consumed d_in[j]
+            with torch.cuda.stream(s_h2d):
+                for n in h_in:
+                    di[n].copy_(h_in[n], non_blocking=True)
+            h2d_done[j].record(s_h2d)
+            s_cmp.wait_event(h2d_done[j])
+            if i >= 2:
+                s_cmp.wait_event(d2h_done[j])          # step i-2's outputs have left d_out[j]
+            xattn.xattn_fwd(di["q"], di["k"], di["v"], B, S, nh, nkv, hd, scale, do_["o"], do_["lse"],
+                            s_cmp)
+            bwd(di["q"], di["k"], di["v"], do_["o"], di["dO"], do_["lse"], B, S, nh, nkv, hd, scale,
+                do_["dq"], do_["dk"], do_["dv"], s_cmp)
+            cmp_done[j].record(s_cmp)
+            s_d2h.wait_event(cmp_done[j])
+            with torch.cuda.stream(s_d2h):
+                for n in ho:
+                    ho[n].copy_(do_[n], non_blocking=True)
+            d2h_done[j].record(s_d2h)
 
-        for _ in range(max(3, args.warmup)):
-            e2e_step()
+        for i in range(max(3, args.warmup)):
+            e2e_step(i)
         torch.cuda.synchronize(dev)
         barrier(pg)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
+        e0.record(s_h2d)
+        for i in range(args.steps):
+            e2e_step(i)
+        s_d2h.wait_stream(s_cmp)
+        e1.record(s_d2h)
         torch.cuda.synchronize(dev)
         t_e2e = max_over_ranks(pg, e0.elapsed_time(e1), dev)
-        if xattn.xattn_check_device_status(stream) != 0:
+        if xattn.xattn_check_device_status(s_cmp) != 0:
             raise RuntimeError("device status in the e2e run")
+        # The last step's results are the same as the device-resident run's.
+        last = (args.steps - 1) % 2
+        if not (torch.equal(h_out[last]["o"], o.cpu()) and torch.equal(h_out[last]["dk"], dk.cpu())):
+            raise RuntimeError("e2e outputs differ from the device-resident run")
         e2e = {"value": flops_step * world * args.steps / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                "tok_per_s": w.tokens * world * args.steps / (t_e2e * 1e-3),
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "note": "steps pipelined over three streams (H2D of the next step and D2H of the "
+                       "previous one overlap this step's kernels), two sets of device buffers"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
