@@ -40,6 +40,7 @@ KERNEL_SOURCES = {
     "attn_bwd_main_kernel": ["attn_bwd_sm103.cu", "sm103_ptx.cuh"],
     "bwd_preprocess_kernel": ["attn_bwd_sm103.cu"],
     "dq_convert_kernel": ["attn_bwd_sm103.cu"],
+    "decode_partial_kernel + decode_combine_kernel": ["attn_decode.cu", "sm103_ptx.cuh"],
 }
 
 
@@ -564,7 +565,8 @@ def run_decode(args, w):
     pk = peaks()
     roofline = {"kernel": "decode_partial_kernel + decode_combine_kernel", "bound": "hbm",
                 "achieved": value / world, "peak": pk["gbs"], "unit": "GB/s",
-                "frac": value / world / pk["gbs"], "traffic": None,
+                "frac": value / world / pk["gbs"],
+                "traffic": ncu_traffic("decode_partial_kernel + decode_combine_kernel", w.name),
                 "algorithmic_per_launch": w.io_bytes, "peak_source": pk["source"] + " (copy)"}
 
     e2e = None

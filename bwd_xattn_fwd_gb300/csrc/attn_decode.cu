@@ -16,8 +16,12 @@
 //      cp.async pieces, all in flight at once; V lands during the score pass) and serve
 //      all `group` query heads of the kv head: one key per thread for the scores, a
 //      chunk-local softmax (max and sum in fp32, log2 domain), then two head-dim elements
-//      per thread for the unnormalised partial outputs. Each chunk writes (max, sum,
-//      partial O) per query head to the scratch buffer.
+//      per thread over a contiguous run of keys for the unnormalised partial outputs.
+//      Each chunk writes (max, sum, partial O) per query head to the scratch buffer.
+//      The arithmetic, not HBM, is what the CTAs spend most issue slots on, so both
+//      passes use the packed two-lane fp32 FMA (__ffma2_rn): the scores pair adjacent
+//      head-dim elements, P V pairs adjacent keys (two partial sums per output, added at
+//      the end); each lane is an ordinary fp32 fma.
 //   2. decode_combine_kernel: one warp per (batch, query head) merges the chunks
 //      (rescaling each by 2^(m_c - M)), writes O in bf16 and LSE = (M + log2 L) ln 2.
 #include "sm103_ptx.cuh"
@@ -124,38 +128,34 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_partial_kernel(
 
   // ---- scores: thread t takes key j = chunk * kDecodeChunk + t, all heads of the group ----
   float s[MAXG];
+  {
+    float2 s2[MAXG];
 #pragma unroll
-  for (int r = 0; r < MAXG; ++r) s[r] = 0.f;
-  if (valid) {
-    const uint4 *krow = reinterpret_cast<const uint4 *>(kt + t * kRow);
+    for (int r = 0; r < MAXG; ++r) s2[r] = make_float2(0.f, 0.f);
+    if (valid) {
+      const uint4 *krow = reinterpret_cast<const uint4 *>(kt + t * kRow);
 #pragma unroll
-    for (int c = 0; c < HD / 8; ++c) {
-      const uint4 kv8 = krow[c];
-      const uint32_t w[4] = {kv8.x, kv8.y, kv8.z, kv8.w};
-      float kf[8];
+      for (int c = 0; c < HD / 8; ++c) {
+        const uint4 kv8 = krow[c];
+        const float2 k01 = make_float2(bf16lo_to_f32(kv8.x), bf16hi_to_f32(kv8.x));
+        const float2 k23 = make_float2(bf16lo_to_f32(kv8.y), bf16hi_to_f32(kv8.y));
+        const float2 k45 = make_float2(bf16lo_to_f32(kv8.z), bf16hi_to_f32(kv8.z));
+        const float2 k67 = make_float2(bf16lo_to_f32(kv8.w), bf16hi_to_f32(kv8.w));
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        kf[2 * e] = bf16lo_to_f32(w[e]);
-        kf[2 * e + 1] = bf16hi_to_f32(w[e]);
-      }
-#pragma unroll
-      for (int r = 0; r < MAXG; ++r) {
-        if (r < group) {
-          const float4 qa = *reinterpret_cast<const float4 *>(qs + r * HD + 8 * c);
-          const float4 qb = *reinterpret_cast<const float4 *>(qs + r * HD + 8 * c + 4);
-          float a = s[r];
-          a = fmaf(qa.x, kf[0], a);
-          a = fmaf(qa.y, kf[1], a);
-          a = fmaf(qa.z, kf[2], a);
-          a = fmaf(qa.w, kf[3], a);
-          a = fmaf(qb.x, kf[4], a);
-          a = fmaf(qb.y, kf[5], a);
-          a = fmaf(qb.z, kf[6], a);
-          a = fmaf(qb.w, kf[7], a);
-          s[r] = a;
+        for (int r = 0; r < MAXG; ++r) {
+          if (r < group) {
+            const float4 qa = *reinterpret_cast<const float4 *>(qs + r * HD + 8 * c);
+            const float4 qb = *reinterpret_cast<const float4 *>(qs + r * HD + 8 * c + 4);
+            s2[r] = __ffma2_rn(make_float2(qa.x, qa.y), k01, s2[r]);
+            s2[r] = __ffma2_rn(make_float2(qa.z, qa.w), k23, s2[r]);
+            s2[r] = __ffma2_rn(make_float2(qb.x, qb.y), k45, s2[r]);
+            s2[r] = __ffma2_rn(make_float2(qb.z, qb.w), k67, s2[r]);
+          }
         }
       }
     }
+#pragma unroll
+    for (int r = 0; r < MAXG; ++r) s[r] = s2[r].x + s2[r].y;
   }
 
   // ---- chunk softmax per head: max, exponentials, sum (log2 domain) ----
@@ -193,7 +193,9 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_partial_kernel(
   }
   __syncthreads();
 
-  // ---- P V: thread (subset ks, pair dp) sums keys ks, ks + kSubsets, ... of the chunk ----
+  // ---- P V: thread (subset ks, pair dp) sums the keys [ks * kPer, (ks + 1) * kPer) of
+  // the chunk for head-dim elements 2 dp and 2 dp + 1; the exponentials of four keys
+  // come in one 16-byte broadcast read ----
   const int dp = t % kPairs, ks = t / kPairs;
   float o0[MAXG], o1[MAXG];
 #pragma unroll
@@ -201,14 +203,49 @@ __global__ void __launch_bounds__(kDecodeThreads) decode_partial_kernel(
   cp_async_wait<0>();
   __syncthreads();                                     // every thread's V pieces have landed
   const uint32_t *vcol = reinterpret_cast<const uint32_t *>(vs) + dp;
-#pragma unroll 4
-  for (int jj = ks; jj < n_valid; jj += kSubsets) {
-    const uint32_t vv = vcol[jj * (kRow / 2)];
+  constexpr int kPer = kDecodeChunk / kSubsets;        // contiguous keys per subset
+  const int k0 = ks * kPer;
+  const int kn = max(0, min(kPer, n_valid - k0));
+  const float *pk = ps + k0;
+  int jj = 0;
+  {
+    float2 ae[MAXG], ao[MAXG];                         // even / odd head-dim element, key pairs
+#pragma unroll
+    for (int r = 0; r < MAXG; ++r) ae[r] = ao[r] = make_float2(0.f, 0.f);
+#pragma unroll(MAXG > 8 ? 1 : 2)
+    for (; jj + 4 <= kn; jj += 4) {
+      uint32_t vv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) vv[u] = vcol[(k0 + jj + u) * (kRow / 2)];
+      const float2 e01 = make_float2(bf16lo_to_f32(vv[0]), bf16lo_to_f32(vv[1]));
+      const float2 e23 = make_float2(bf16lo_to_f32(vv[2]), bf16lo_to_f32(vv[3]));
+      const float2 o01 = make_float2(bf16hi_to_f32(vv[0]), bf16hi_to_f32(vv[1]));
+      const float2 o23 = make_float2(bf16hi_to_f32(vv[2]), bf16hi_to_f32(vv[3]));
+#pragma unroll
+      for (int r = 0; r < MAXG; ++r) {
+        if (r < group) {
+          const float4 p4 = *reinterpret_cast<const float4 *>(pk + r * kDecodeChunk + jj);
+          const float2 p01 = make_float2(p4.x, p4.y), p23 = make_float2(p4.z, p4.w);
+          ae[r] = __ffma2_rn(p01, e01, ae[r]);
+          ae[r] = __ffma2_rn(p23, e23, ae[r]);
+          ao[r] = __ffma2_rn(p01, o01, ao[r]);
+          ao[r] = __ffma2_rn(p23, o23, ao[r]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < MAXG; ++r) {
+      o0[r] = ae[r].x + ae[r].y;
+      o1[r] = ao[r].x + ao[r].y;
+    }
+  }
+  for (; jj < kn; ++jj) {
+    const uint32_t vv = vcol[(k0 + jj) * (kRow / 2)];
     const float v0 = bf16lo_to_f32(vv), v1 = bf16hi_to_f32(vv);
 #pragma unroll
     for (int r = 0; r < MAXG; ++r) {
       if (r < group) {
-        const float p = ps[r * kDecodeChunk + jj];
+        const float p = pk[r * kDecodeChunk + jj];
         o0[r] = fmaf(p, v0, o0[r]);
         o1[r] = fmaf(p, v1, o1[r]);
       }
