@@ -26,7 +26,8 @@
 // Epilogue: O / l in bf16, LSE = (m + log2 l) ln 2.
 // Causal tile skipping: tile m visits key tiles 0..m.
 // TMEM columns: S_A [0,128) S_B [128,256) fp32 | O_A [256,256+HD) O_B [320,320+HD) fp32 |
-//               P_A [384,448) P_B [448,512) bf16 pairs.
+//               P_A [384,448) P_B [448,512) bf16 pairs; at hd = 128: O_A [256,384),
+//               O_B [384,512), and P_X in the first 64 columns of S_X.
 #include <type_traits>
 
 #include "sm103_ptx.cuh"
@@ -36,25 +37,40 @@ namespace xattn {
 namespace {
 
 constexpr int kFwdThreads = 384;  // 12 warps
-constexpr int kFwdStages = 3;
 
+// hd = 128 differs from hd = 32 / 64 in three ways, all fixed here at compile time:
+//  * a 256-byte row does not fit one 128-byte swizzle atom, so every tile is stored (and
+//    loaded by TMA) as two 64-column sub-tiles, each laid out like an hd = 64 tile;
+//  * shared memory holds one Q buffer and two K/V stages (three Q+K/V stages of 32 KB
+//    tiles would not fit);
+//  * O_A and O_B take 128 TMEM columns each, so P_X is written over the columns of S_X
+//    (kAliasP) and S_X(n+1) is issued after PV_X(n), whose read of P_X(n) the tensor
+//    pipe completes first (one thread's MMAs execute in issue order).
 template <int HD>
 struct FwdLayout {
+  static constexpr int kStages = HD == 128 ? 2 : 3;                 // K/V ring
+  static constexpr int kQBufs = HD == 128 ? 1 : 2;                  // Q buffers (Q_A, Q_B each)
+  static constexpr bool kAliasP = HD == 128;
   static constexpr uint32_t kRowBytes = HD * 2;
   static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
-  static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
-  static constexpr uint32_t kQ = 0;                                  // 2 x (Q_A, Q_B)
-  static constexpr uint32_t kK = kQ + 4 * kTileBytes;
-  static constexpr uint32_t kV = kK + kFwdStages * kTileBytes;
-  static constexpr uint32_t kBars = kV + kFwdStages * kTileBytes;
+  static constexpr uint32_t kAtomBytes = kRowBytes < 128 ? kRowBytes : 128;  // sub-tile row
+  static constexpr int kSubTiles = static_cast<int>(kRowBytes / kAtomBytes);
+  static constexpr uint32_t kSubBytes = kTileRows * kAtomBytes;
+  static constexpr uint32_t kSwizzle = (HD == 32) ? kSwizzle64 : kSwizzle128;
+  static constexpr uint32_t kQ = 0;                                  // kQBufs x (Q_A, Q_B)
+  static constexpr uint32_t kK = kQ + 2 * kQBufs * kTileBytes;
+  static constexpr uint32_t kV = kK + kStages * kTileBytes;
+  static constexpr uint32_t kBars = kV + kStages * kTileBytes;
   // barriers: full[S], empty[S], s_full[2], p_full[2], o_done[2], s_free[2], o_free[2],
   //           q_full[2], mma_final[2] (one each per Q buffer)
-  static constexpr int kNumBars = 2 * kFwdStages + 2 + 2 + 2 + 2 + 2 + 2 + 2;
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + 2 + 2 + 2 + 2;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   // Ask for enough shared memory that one CTA occupies an SM: each CTA holds all 512
   // TMEM columns, so a second resident CTA would only spin in tcgen05.alloc.
   static constexpr uint32_t kDynBytes = (kUsed + 1024 > 120 * 1024) ? kUsed + 1024 : 120 * 1024;
+  static_assert(kDynBytes <= 227 * 1024, "exceeds the opt-in shared memory of one CTA");
+  static_assert(kSubBytes % 1024 == 0 && kTileBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 };
 
 // Warp-uniform bounded wait: every lane waits, then all agree.
@@ -72,6 +88,8 @@ __global__ void __maxnreg__(168)
                     float *__restrict__ lse, int B, int S, int nh, int nkv, float scale_log2,
                     int *status, unsigned long long timeout_ns) {
   using L = FwdLayout<HD>;
+  constexpr int kFwdStages = L::kStages;
+  constexpr int kQBufs = L::kQBufs;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -157,8 +175,14 @@ __global__ void __maxnreg__(168)
   grid_dep_wait();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
   auto tS = [&](int x) { return tmem + 128u * x; };
-  auto tO = [&](int x) { return tmem + 256u + 64u * x; };
-  auto tP = [&](int x) { return tmem + 384u + 64u * x; };
+  auto tO = [&](int x) { return tmem + 256u + (L::kAliasP ? 128u : 64u) * x; };
+  auto tP = [&](int x) { return L::kAliasP ? tS(x) : tmem + 384u + 64u * x; };
+  // One 128-row tile of a [B, S, heads, hd] tensor: one TMA box per 64-column sub-tile.
+  auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int head, int row0, int bb) {
+#pragma unroll
+    for (int c = 0; c < L::kSubTiles; ++c)
+      tma_load_4d_elect(dst + c * L::kSubBytes, map, bar, c * static_cast<int>(L::kAtomBytes / 2), head, row0, bb);
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
@@ -171,8 +195,8 @@ __global__ void __maxnreg__(168)
       const int s = R % kFwdStages;
       if (!warp_wait(empty(s), ((R / kFwdStages) & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(full(s), 2 * L::kTileBytes);
-      tma_load_4d_elect(sK + s * L::kTileBytes, &mk, full(s), 0, kvh, n * kTileRows, b);
-      tma_load_4d_elect(sV + s * L::kTileBytes, &mv, full(s), 0, kvh, n * kTileRows, b);
+      load_tile(sK + s * L::kTileBytes, &mk, full(s), kvh, n * kTileRows, b);
+      load_tile(sV + s * L::kTileBytes, &mv, full(s), kvh, n * kTileRows, b);
       issued = ++R;
       return true;
     };
@@ -182,19 +206,20 @@ __global__ void __maxnreg__(168)
       const int u = unit_at(k);
       if (u >= num_units) break;
       XATTN_FWD_UNIT(u);
-      const int qb = units & 1;
+      const int qb = units % kQBufs;
       const uint32_t sQb = sQ + qb * 2 * L::kTileBytes;
-      // Phase units/2 - 1 of mma_final[qb]: the products of unit units - 2.
-      if (!warp_wait(mma_final(qb), ((units >> 1) & 1) ^ 1, ctl)) break;
+      // Phase units/kQBufs - 1 of mma_final[qb]: the products of unit units - kQBufs.
+      if (!warp_wait(mma_final(qb), ((units / kQBufs) & 1) ^ 1, ctl)) break;
       mbar_expect_tx_elect(q_full(qb), (hasB ? 2 : 1) * L::kTileBytes);
-      tma_load_4d_elect(sQb, &mq, q_full(qb), 0, h, mA * kTileRows, b);
-      if (hasB) tma_load_4d_elect(sQb + L::kTileBytes, &mq, q_full(qb), 0, h, mB * kTileRows, b);
+      load_tile(sQb, &mq, q_full(qb), h, mA * kTileRows, b);
+      if (hasB) load_tile(sQb + L::kTileBytes, &mq, q_full(qb), h, mB * kTileRows, b);
       ++units;
 #pragma unroll 1
       for (int n = 0; ok && n <= n_last; ++n) ok = load_kv(n, kvh, b);
     }
     // Let every copy in flight land before the CTA can exit.
-    for (int j = (units > 2 ? units - 2 : 0); j < units; ++j) mbar_drain(q_full(j & 1), (j >> 1) & 1, ctl);
+    for (int j = (units > kQBufs ? units - kQBufs : 0); j < units; ++j)
+      mbar_drain(q_full(j % kQBufs), (j / kQBufs) & 1, ctl);
     for (int n = (issued > kFwdStages ? issued - kFwdStages : 0); n < issued; ++n)
       mbar_drain(full(n % kFwdStages), (n / kFwdStages) & 1, ctl);
   } else if (warp == 1 || warp == 3) {
@@ -205,14 +230,17 @@ __global__ void __maxnreg__(168)
     // stages are released by a commit from each (empty counts 2).
     const int x = warp == 1 ? 0 : 1;
     constexpr uint32_t idesc_qk = idesc_bf16_f32(128, 128, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD, false, true);
+    // PV is one N = 64 product per 64-column sub-tile of V (and of O) at hd = 128.
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(128, HD / L::kSubTiles, false, true);
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;        // tile stride, descriptor units
-    constexpr uint32_t kVStep = (16 * L::kRowBytes) >> 4;      // 16 key rows of V
+    constexpr uint32_t kSubDesc = L::kSubBytes >> 4;           // sub-tile stride
+    constexpr uint32_t kVStep = (16 * L::kAtomBytes) >> 4;     // 16 key rows of V
     // Descriptors are built once; a K step of 16 elements is +32 bytes (+2) within the
-    // swizzled K-major rows of Q and K, and +16 rows of the MN-major V tile.
-    const uint64_t dQ = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle) + x * kStageDesc;
-    const uint64_t dK = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t dV = smem_desc(sV, 8192, 8 * L::kRowBytes, L::kSwizzle);
+    // swizzled K-major rows of Q and K (the fifth step starts the second sub-tile), and
+    // +16 rows of the MN-major V tile.
+    const uint64_t dQ = smem_desc(sQ, 16, 8 * L::kAtomBytes, L::kSwizzle) + x * kStageDesc;
+    const uint64_t dK = smem_desc(sK, 16, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t dV = smem_desc(sV, 8192, 8 * L::kAtomBytes, L::kSwizzle);
     const uint32_t tSx = tS(x), tOx = tO(x), tPx = tP(x);
     // Each product's MMAs and commits are issued by one elected lane; the warp then
     // reconverges.
@@ -220,8 +248,10 @@ __global__ void __maxnreg__(168)
       const uint64_t dQb = dQ + qb * 2 * kStageDesc;
       if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          mma_ss(tSx, dQb + 2 * kk, dK + s * kStageDesc + 2 * kk, idesc_qk, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint32_t koff = (kk / 4) * kSubDesc + (kk % 4) * 2;
+          mma_ss(tSx, dQb + koff, dK + s * kStageDesc + koff, idesc_qk, kk > 0);
+        }
         mma_commit(s_full(x));
       }
       __syncwarp();
@@ -232,7 +262,10 @@ __global__ void __maxnreg__(168)
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_ts(tOx, tPx + kk * 8, dV + s * kStageDesc + kk * kVStep, idesc_pv, (!first || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int c = 0; c < L::kSubTiles; ++c)
+            mma_ts(tOx + c * (HD / L::kSubTiles), tPx + kk * 8, dV + s * kStageDesc + c * kSubDesc + kk * kVStep,
+                   idesc_pv, (!first || kk > 0) ? 1u : 0u);
         mma_commit(o_done(x));
         mma_commit(empty(s));                      // this issuer is done with K_n and V_n
         if (sole_user) mma_commit(empty(s));
@@ -257,11 +290,11 @@ __global__ void __maxnreg__(168)
       if (u >= num_units) break;
       XATTN_FWD_UNIT(u);
       const int mX = x == 0 ? mA : mB;
-      const int qb = units & 1;
-      // This unit's Q tiles have landed (phase units/2 of q_full[qb]). Waited for by both
+      const int qb = units % kQBufs;
+      // This unit's Q tiles have landed (phase units/kQBufs of q_full[qb]). Waited for by both
       // issuers in every unit, even without tile B, so each sees every phase in order and
       // its mma_final arrival below can never count towards an earlier use of the buffer.
-      if (!warp_wait(q_full(qb), (units >> 1) & 1, ctl)) break;
+      if (!warp_wait(q_full(qb), (units / kQBufs) & 1, ctl)) break;
       if (x == 0 || hasB) {
         // The unit's first scores: key tile 0 landed, and S_X of the previous unit read;
         // its first PV overwrites O_X, which the previous epilogue has read.
@@ -272,16 +305,28 @@ __global__ void __maxnreg__(168)
         if (!warp_wait(o_free(x), (unitsx - 1) & 1, ctl)) { ok = false; break; }
 #pragma unroll 1
         for (int n = 0; n <= mX; ++n, ++gx) {
-          if (n + 1 <= mX) {
-            if (!warp_wait(s_free(x), gx & 1, ctl) ||
-                !warp_wait(full(ring_stage(R + n + 1)), ring_phase(R + n + 1), ctl)) { ok = false; break; }
-            tc_fence_after();
-            issue_qk(ring_stage(R + n + 1), qb);
-          }
-          if (!warp_wait(p_full(x), gx & 1, ctl)) { ok = false; break; }
-          tc_fence_after();
           const bool shared_tile = x == 0 ? hasB : n <= mA;
-          issue_pv(ring_stage(R + n), n == 0, !shared_tile);
+          if constexpr (!L::kAliasP) {
+            if (n + 1 <= mX) {
+              if (!warp_wait(s_free(x), gx & 1, ctl) ||
+                  !warp_wait(full(ring_stage(R + n + 1)), ring_phase(R + n + 1), ctl)) { ok = false; break; }
+              tc_fence_after();
+              issue_qk(ring_stage(R + n + 1), qb);
+            }
+            if (!warp_wait(p_full(x), gx & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(ring_stage(R + n), n == 0, !shared_tile);
+          } else {
+            // P_X(n) sits in S_X's columns: PV_X(n) first, then S_X(n+1) over them.
+            if (!warp_wait(p_full(x), gx & 1, ctl)) { ok = false; break; }
+            tc_fence_after();
+            issue_pv(ring_stage(R + n), n == 0, !shared_tile);
+            if (n + 1 <= mX) {
+              if (!warp_wait(full(ring_stage(R + n + 1)), ring_phase(R + n + 1), ctl)) { ok = false; break; }
+              tc_fence_after();
+              issue_qk(ring_stage(R + n + 1), qb);
+            }
+          }
         }
         if (!ok) break;
         ++unitsx;
@@ -291,7 +336,7 @@ __global__ void __maxnreg__(168)
       R += n_last + 1;
       ++units;
     }
-    if (units > 0) mbar_drain(mma_final((units - 1) & 1), ((units - 1) >> 1) & 1, ctl);
+    if (units > 0) mbar_drain(mma_final((units - 1) % kQBufs), ((units - 1) / kQBufs) & 1, ctl);
   } else if (warp >= 4) {
     // ---------------- softmax + epilogue: one thread per query row of tile X ----------------
     const int x = (warp - 4) >> 2;          // 0 = tile A, 1 = tile B
@@ -485,6 +530,8 @@ cudaError_t launch_fwd_bf16(const CUtensorMap &mq, const CUtensorMap &mk, const 
     return launch_fwd_hd<64>(mq, mk, mv, o, lse, B, S, nh, nkv, scale, status, timeout_ns, stream);
   if (hd == 32)
     return launch_fwd_hd<32>(mq, mk, mv, o, lse, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  if (hd == 128)
+    return launch_fwd_hd<128>(mq, mk, mv, o, lse, B, S, nh, nkv, scale, status, timeout_ns, stream);
   return cudaErrorInvalidValue;
 }
 

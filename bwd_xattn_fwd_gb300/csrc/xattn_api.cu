@@ -94,19 +94,20 @@ xattn_status get_encode() {
   return g_encode ? XATTN_OK : XATTN_ERR_CUDA;
 }
 
-// 4-D map over a contiguous [B, S, H, hd] bf16 tensor; box = one head's 128-row tile.
-// The 128-byte (hd = 64) or 64-byte (hd = 32) swizzle matches the UMMA operand layout.
-// Rows past S read as zeros.
+// 4-D map over a contiguous [B, S, H, hd] bf16 tensor; box = one head's 128-row tile, or
+// at hd = 128 one 64-column half of it (a swizzled box row is at most 128 bytes; the
+// kernels load the two halves as two sub-tiles). The 128-byte (hd = 64, 128) or 64-byte
+// (hd = 32) swizzle matches the UMMA operand layout. Rows past S read as zeros.
 xattn_status make_map(CUtensorMap *map, const void *ptr, int B, int S, int H, int hd) {
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(hd), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
   const cuuint64_t row = static_cast<cuuint64_t>(hd) * 2;
   const cuuint64_t strides[3] = {row, row * H, row * H * S};
-  const cuuint32_t box[4] = {static_cast<cuuint32_t>(hd), 1, static_cast<cuuint32_t>(kTileRows), 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(hd > 64 ? 64 : hd), 1, static_cast<cuuint32_t>(kTileRows), 1};
   const cuuint32_t elem[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims,
                               strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              hd == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                              hd == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? XATTN_OK : XATTN_ERR_CUDA;
 }
@@ -167,6 +168,9 @@ xattn_status check_bwd_scale(float scale) {
 }
 
 xattn_status check_bf16(int hd) { return (hd == 32 || hd == 64) ? XATTN_OK : XATTN_ERR_UNSUPPORTED_HD; }
+xattn_status check_bf16_fwd(int hd) {
+  return (hd == 32 || hd == 64 || hd == 128) ? XATTN_OK : XATTN_ERR_UNSUPPORTED_HD;
+}
 
 // With XATTN_VERBOSE set in the environment, CUDA failures are also reported on stderr.
 xattn_status cuda_status(cudaError_t e) {
@@ -205,7 +209,7 @@ xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S
                        int hd, float scale, void *o, float *lse, void *stream) {
   if (!q || !k || !v || !o || !lse) return XATTN_ERR_NULL_PTR;
   XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
-  XATTN_TRY(check_bf16(hd));
+  XATTN_TRY(check_bf16_fwd(hd));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return XATTN_ERR_MISALIGNED;
   DeviceInfo *dev = nullptr;
   XATTN_TRY(bf16_device(&dev));

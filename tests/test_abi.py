@@ -66,7 +66,7 @@ def test_fwd_argument_checks(lib):
     assert _fwd(lib, S=-1) == 2
     assert _fwd(lib, nh=3, nkv=2) == 3                 # nh % nkv != 0
     assert _fwd(lib, hd=48) == 4                       # unsupported head dim for bf16
-    assert _fwd(lib, hd=128) == 4
+    assert _fwd(lib, hd=256) == 4
     assert _fwd(lib, q=18) == 5                        # not 16-byte aligned
     assert _fwd(lib, scale=float("nan")) == 9
     assert _fwd(lib, scale=float("inf")) == 9
@@ -90,6 +90,18 @@ def test_bwd_scale_checks(lib):
     if not torch.cuda.is_available():
         assert _bwd(lib, 0.0) == 6                     # accepted; fails only for want of a GPU
         assert _bwd(lib, 2.0 ** -64) == 6
+
+
+def test_head_dim_128_forward_only(lib):
+    """bf16 hd = 128 passes the forward's host checks; the backward rejects it."""
+    import torch
+    if not torch.cuda.is_available():
+        assert _fwd(lib, hd=128) == 6                  # accepted; fails only for want of a GPU
+    f = lib.xattn_bwd
+    f.restype = ctypes.c_int
+    f.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_float]
+                  + [ctypes.c_void_p] * 4)
+    assert f(16, 32, 48, 64, 80, 96, 1, 4, 2, 1, 128, 0.1, 112, 128, 144, None) == 4
 
 
 def test_f32_head_dim_limit(lib):
