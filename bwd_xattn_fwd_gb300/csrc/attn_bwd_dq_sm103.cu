@@ -26,24 +26,30 @@ namespace {
 // warps (one per TMEM lane quarter); group g owns key columns [64 g, 64 g + 64) of
 // every tile, one query row per thread.
 constexpr int kDqThreads = 384;
-constexpr int kDqStages = 3;            // K / V stages
 
+// hd = 128: two K / V stages (32 KB tiles), and every tile is two 64-column sub-tiles laid
+// out like hd = 64 tiles (a 256-byte row does not fit one 128-byte swizzle atom).
 template <int HD>
 struct DqLayout {
+  static constexpr int kStages = HD == 128 ? 2 : 3;                 // K / V stages
   static constexpr uint32_t kRowBytes = HD * 2;
   static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
-  static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
+  static constexpr uint32_t kAtomBytes = kRowBytes < 128 ? kRowBytes : 128;  // sub-tile row
+  static constexpr int kSubTiles = static_cast<int>(kRowBytes / kAtomBytes);
+  static constexpr uint32_t kSubBytes = kTileRows * kAtomBytes;
+  static constexpr uint32_t kSwizzle = (HD == 32) ? kSwizzle64 : kSwizzle128;
   static constexpr uint32_t kQ = 0;
   static constexpr uint32_t kdO = kQ + kTileBytes;
-  static constexpr uint32_t kK = kdO + kTileBytes;                   // kDqStages stages
-  static constexpr uint32_t kV = kK + kDqStages * kTileBytes;        // kDqStages stages
+  static constexpr uint32_t kK = kdO + kTileBytes;                   // kStages stages
+  static constexpr uint32_t kV = kK + kStages * kTileBytes;          // kStages stages
   // barriers: q_full, full[S], empty[S], s_full, s_free, dp_full, dp_free, ds_full,
   //           dq_done, acc_done
-  static constexpr int kNumBars = 1 + 2 * kDqStages + 7;
-  static constexpr uint32_t kBars = kV + kDqStages * kTileBytes;
+  static constexpr int kNumBars = 1 + 2 * kStages + 7;
+  static constexpr uint32_t kBars = kV + kStages * kTileBytes;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
   static constexpr uint32_t kDynBytes = kUsed + 1024;
+  static_assert(kDynBytes <= 227 * 1024, "exceeds the opt-in shared memory of one CTA");
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
@@ -51,7 +57,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(0xffffffffu, ok);
 }
 
-// TMEM columns: S [0,128) fp32 | dP [128,256) fp32 | dS bf16 [256,320) | dQ [320,320+HD).
+// TMEM columns: S [0,128) fp32 | dP [128,256) fp32 | dS bf16 [256,320) | dQ [320,320+HD)
+// (at most 448 columns, hd = 128 included).
 // S and dP are each released (s_free, dp_free) as soon as both groups have loaded their
 // columns, so the next tile's products overlap this tile's arithmetic; the dS slot is
 // rewritten only after dQ(n-1) has read it (dq_done).
@@ -63,6 +70,7 @@ __global__ void __maxnreg__(168)
                        __nv_bfloat16 *__restrict__ dq, int B, int S, int nh, int nkv, float scale,
                        int *status, unsigned long long timeout_ns) {
   using L = DqLayout<HD>;
+  constexpr int kDqStages = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -127,18 +135,24 @@ __global__ void __maxnreg__(168)
   grid_dep_wait();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tdP = tmem + 128, tdS = tmem + 256, tdQ = tmem + 320;
+  // One 128-row tile of a [B, S, heads, hd] tensor: one TMA box per 64-column sub-tile.
+  auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int head, int row0, int bb) {
+#pragma unroll
+    for (int c = 0; c < L::kSubTiles; ++c)
+      tma_load_4d_elect(dst + c * L::kSubBytes, map, bar, c * static_cast<int>(L::kAtomBytes / 2), head, row0, bb);
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
     mbar_expect_tx_elect(q_full, 2 * L::kTileBytes);
-    tma_load_4d_elect(sQ, &mq, q_full, 0, h, m * kTileRows, b);
-    tma_load_4d_elect(sdO, &mdo, q_full, 0, h, m * kTileRows, b);
+    load_tile(sQ, &mq, q_full, h, m * kTileRows, b);
+    load_tile(sdO, &mdo, q_full, h, m * kTileRows, b);
     int issued = 0;
     for (int n = 0, s = 0, use = 0; n < T; ++n) {
       if (!warp_wait(empty(s), (use & 1) ^ 1, ctl)) break;
       mbar_expect_tx_elect(full(s), 2 * L::kTileBytes);
-      tma_load_4d_elect(sK + s * L::kTileBytes, &mk, full(s), 0, kvh, n * kTileRows, b);
-      tma_load_4d_elect(sV + s * L::kTileBytes, &mv, full(s), 0, kvh, n * kTileRows, b);
+      load_tile(sK + s * L::kTileBytes, &mk, full(s), kvh, n * kTileRows, b);
+      load_tile(sV + s * L::kTileBytes, &mv, full(s), kvh, n * kTileRows, b);
       issued = n + 1;
       if (++s == kDqStages) { s = 0; ++use; }
     }
@@ -149,19 +163,25 @@ __global__ void __maxnreg__(168)
   } else if (warp == 1) {
     // ---------------- MMA issuer (converged warp, one elected lane issues) ----------------
     constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);  // S, dP
-    constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, false, true);   // dQ (B = K, MN-major)
+    // dQ (B = K, MN-major): one N = 64 product per 64-column sub-tile at hd = 128.
+    constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD / L::kSubTiles, false, true);
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;
-    constexpr uint32_t kRowStep = (16 * L::kRowBytes) >> 4;              // 16 key rows of K
-    // K-major operands advance +32 bytes (+2) per 16-element K step; the MN-major K tile
-    // (dQ's B: K dimension = keys) advances 16 rows.
-    const uint64_t kQ_k = smem_desc(sQ, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kdO_k = smem_desc(sdO, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kK_k = smem_desc(sK, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kV_k = smem_desc(sV, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kRowBytes, L::kSwizzle);
+    constexpr uint32_t kSubDesc = L::kSubBytes >> 4;                     // sub-tile stride
+    constexpr uint32_t kRowStep = (16 * L::kAtomBytes) >> 4;             // 16 key rows of K
+    // K-major operands advance +32 bytes (+2) per 16-element K step (the fifth step
+    // starts the second sub-tile); the MN-major K tile (dQ's B: K dimension = keys)
+    // advances 16 rows.
+    const uint64_t kQ_k = smem_desc(sQ, 16, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kdO_k = smem_desc(sdO, 16, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kK_k = smem_desc(sK, 16, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kV_k = smem_desc(sV, 16, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kAtomBytes, L::kSwizzle);
     auto issue_s = [&](uint32_t d, uint64_t a, uint64_t bdesc) {
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk) mma_ss_elect(d, a + 2 * kk, bdesc + 2 * kk, idesc_s, kk > 0);
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint32_t koff = (kk / 4) * kSubDesc + (kk % 4) * 2;
+        mma_ss_elect(d, a + koff, bdesc + koff, idesc_s, kk > 0);
+      }
     };
     bool ok = warp_wait(q_full, 0, ctl) && warp_wait(full(0), 0, ctl);
     if (ok) {
@@ -190,8 +210,10 @@ __global__ void __maxnreg__(168)
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kTileRows / 16; ++kk)                  // dQ += dS K_n
-        mma_ts_elect(tdQ, tdS + kk * 8, kK_mn + s * kStageDesc + kk * kRowStep, idesc_dq,
-                     (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int c = 0; c < L::kSubTiles; ++c)
+          mma_ts_elect(tdQ + c * (HD / L::kSubTiles), tdS + kk * 8, kK_mn + s * kStageDesc + c * kSubDesc + kk * kRowStep,
+                       idesc_dq, (n > 0 || kk > 0) ? 1u : 0u);
       mma_commit_elect(dq_done);
       mma_commit_elect(empty(s));                                  // K_n, V_n fully consumed
       s = s1;
@@ -328,6 +350,8 @@ cudaError_t launch_bwd_dq_bf16(const CUtensorMap &mq, const CUtensorMap &mk, con
     return launch_dq_hd<64>(mq, mk, mv, mdo, lse, ws.D, dq, B, S, nh, nkv, scale, status, timeout_ns, stream);
   if (hd == 32)
     return launch_dq_hd<32>(mq, mk, mv, mdo, lse, ws.D, dq, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  if (hd == 128)
+    return launch_dq_hd<128>(mq, mk, mv, mdo, lse, ws.D, dq, B, S, nh, nkv, scale, status, timeout_ns, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -155,11 +155,20 @@ struct BwdLayout {
   // Two rings of query-tile operands, each sized by how long a stage is held: Q and the
   // auxiliary rows are read until dK(t), at the very end of an iteration; dO only until
   // dP^T(t) and dV(t).
-  static constexpr int kQStages = kFusedDq ? 3 : 4;                 // Q + auxiliary rows
-  static constexpr int kOStages = kFusedDq ? 2 : 4;                 // dO
+  // hd = 128 (dK / dV only): 32 KB tiles leave room for two stages of each, every tile
+  // is two 64-column sub-tiles laid out like hd = 64 tiles (a 256-byte row does not fit
+  // one 128-byte swizzle atom), and dV, dK take 128 TMEM columns each, so P^T is written
+  // over S^T and dS^T over dP^T (kAlias).
+  static_assert(!(kFusedDq && HD == 128), "hd = 128 runs with the query-stationary dQ kernel");
+  static constexpr bool kAlias = HD == 128;
+  static constexpr int kQStages = HD == 128 ? 2 : kFusedDq ? 3 : 4;  // Q + auxiliary rows
+  static constexpr int kOStages = HD == 128 ? 2 : kFusedDq ? 2 : 4;  // dO
   static constexpr uint32_t kRowBytes = HD * 2;
   static constexpr uint32_t kTileBytes = kTileRows * kRowBytes;
-  static constexpr uint32_t kSwizzle = (HD == 64) ? kSwizzle128 : kSwizzle64;
+  static constexpr uint32_t kAtomBytes = kRowBytes < 128 ? kRowBytes : 128;  // sub-tile row
+  static constexpr int kSubTiles = static_cast<int>(kRowBytes / kAtomBytes);
+  static constexpr uint32_t kSubBytes = kTileRows * kAtomBytes;
+  static constexpr uint32_t kSwizzle = (HD == 32) ? kSwizzle64 : kSwizzle128;
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kK + kTileBytes;
   static constexpr uint32_t kQ = kV + kTileBytes;                    // kQStages stages
@@ -351,9 +360,17 @@ __global__ void __maxnreg__(168)
   grid_dep_launch();
   grid_dep_wait();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
-  const uint32_t tS = tmem, tdP = tmem + 128, tP = tmem + 256;
-  const uint32_t tdV = tmem + 320, tdK = tmem + 384;
-  const uint32_t tdQ = tmem + 448, tdS = tmem + 448;   // fused dQ: dQ; otherwise dS^T
+  // hd = 128: S^T [0,128) with P^T in its first 64 columns | dP^T [128,256) with dS^T
+  // in its first 64 | dV [256,384) | dK [384,512).
+  const uint32_t tS = tmem, tdP = tmem + 128, tP = L::kAlias ? tS : tmem + 256;
+  const uint32_t tdV = tmem + (L::kAlias ? 256 : 320), tdK = tmem + 384;
+  const uint32_t tdQ = tmem + 448, tdS = L::kAlias ? tdP : tmem + 448;   // fused dQ: dQ; otherwise dS^T
+  // One 128-row tile of a [B, S, heads, hd] tensor: one TMA box per 64-column sub-tile.
+  auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int head, int row0, int bb) {
+#pragma unroll
+    for (int c = 0; c < L::kSubTiles; ++c)
+      tma_load_4d_elect(dst + c * L::kSubBytes, map, bar, c * static_cast<int>(L::kAtomBytes / 2), head, row0, bb);
+  };
 
   if (warp == 0) {
     // ---------------- TMA producer (converged warp, one elected lane issues) ----------------
@@ -368,12 +385,12 @@ __global__ void __maxnreg__(168)
       const int h = kvh * group + t / per_head, m = n + t % per_head;
       if (!warp_wait(q_empty(sq), (uq & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(q_full(sq), L::kTileBytes + L::kAuxTileBytes);
-      tma_load_4d_elect(sQ + sq * L::kTileBytes, &mq, q_full(sq), 0, h, m * kTileRows, b);
+      load_tile(sQ + sq * L::kTileBytes, &mq, q_full(sq), h, m * kTileRows, b);
       tma_load_4d_elect(sAuxB + sq * L::kAuxTileBytes, &maux, q_full(sq), 0, m * kTileRows, h, b);
       issued_q = g + 1;
       if (!warp_wait(o_empty(so), (uo & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(o_full(so), L::kTileBytes);
-      tma_load_4d_elect(sdO + so * L::kTileBytes, &mdo, o_full(so), 0, h, m * kTileRows, b);
+      load_tile(sdO + so * L::kTileBytes, &mdo, o_full(so), h, m * kTileRows, b);
       issued_o = g + 1;
       ++g;
       if (++sq == kQS) { sq = 0; ++uq; }
@@ -390,8 +407,8 @@ __global__ void __maxnreg__(168)
       for (int t = 0; ok && t < pre; ++t) ok = load_ring(t);
       if (!ok || !warp_wait(acc_done, (units - 1) & 1, ctl)) break;
       mbar_expect_tx_elect(kv_full, 2 * L::kTileBytes);
-      tma_load_4d_elect(sK, &mk, kv_full, 0, kvh, n * kTileRows, b);
-      tma_load_4d_elect(sV, &mv, kv_full, 0, kvh, n * kTileRows, b);
+      load_tile(sK, &mk, kv_full, kvh, n * kTileRows, b);
+      load_tile(sV, &mv, kv_full, kvh, n * kTileRows, b);
       ++units;
       for (int t = pre; ok && t < T; ++t) ok = load_ring(t);
     }
@@ -411,16 +428,19 @@ __global__ void __maxnreg__(168)
     // commit from each issuer (empty counts 2), and acc_done gets one from each.
     const bool p_side = warp == 1;
     constexpr uint32_t idesc_t = idesc_bf16_f32(128, 128, false, false);  // S^T, dP^T
-    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD, false, true);  // dV, dK (A K-major)
+    // dV, dK (A K-major): one N = 64 product per 64-column sub-tile at hd = 128.
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(128, HD / L::kSubTiles, false, true);
     constexpr uint32_t kStageDesc = L::kTileBytes >> 4;   // stage stride, descriptor units
-    constexpr uint32_t kRowStep = (16 * L::kRowBytes) >> 4;  // 16 rows of an MN-major tile
+    constexpr uint32_t kSubDesc = L::kSubBytes >> 4;      // sub-tile stride
+    constexpr uint32_t kRowStep = (16 * L::kAtomBytes) >> 4;  // 16 rows of an MN-major tile
     // Descriptors are built once. K-major operands advance +32 bytes (+2) per
-    // 16-element K step; MN-major ones advance 16 rows.
-    const uint64_t kA_k = smem_desc(p_side ? sK : sV, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kB_k = smem_desc(p_side ? sQ : sdO, 16, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kQ_mn = smem_desc(sQ, 8192, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kdO_mn = smem_desc(sdO, 8192, 8 * L::kRowBytes, L::kSwizzle);
-    const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kRowBytes, L::kSwizzle);       // fused dQ
+    // 16-element K step (the fifth step starts the second sub-tile); MN-major ones
+    // advance 16 rows.
+    const uint64_t kA_k = smem_desc(p_side ? sK : sV, 16, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kB_k = smem_desc(p_side ? sQ : sdO, 16, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kQ_mn = smem_desc(sQ, 8192, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kdO_mn = smem_desc(sdO, 8192, 8 * L::kAtomBytes, L::kSwizzle);
+    const uint64_t kK_mn = smem_desc(sK, 8192, 8 * L::kAtomBytes, L::kSwizzle);       // fused dQ
     const uint64_t kdS_mn = smem_desc(sdS, 16384, 1024, kSwizzle128);
     const uint64_t kdS_k = smem_desc(sdS, 16, 1024, kSwizzle128);
     constexpr uint32_t idesc_dq = idesc_bf16_f32(128, HD, true, true);  // dQ (A = dS, MN-major)
@@ -444,7 +464,10 @@ __global__ void __maxnreg__(168)
         if (with_qk) {
           const uint64_t b_k = kB_k + (p_side ? sq : so) * kStageDesc;
 #pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) mma_ss(tD, kA_k + 2 * kk, b_k + 2 * kk, idesc_t, kk > 0);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            const uint32_t koff = (kk / 4) * kSubDesc + (kk % 4) * 2;
+            mma_ss(tD, kA_k + koff, b_k + koff, idesc_t, kk > 0);
+          }
         }
         mma_ss(tD, kAuxA, kAuxQ + sq * kAuxStageDesc, idesc_t, with_qk ? 1u : 0u);
         mma_commit(t_full);
@@ -469,6 +492,8 @@ __global__ void __maxnreg__(168)
       // read the previous score tile (the last one of the previous unit).
       ok = warp_wait(kv_full, units & 1, ctl) && wait_operands(g, sq, so) &&
            warp_wait(t_free, (g - 1) & 1, ctl);
+      // With P^T over S^T, S^T overwrites the previous P^T: the dS warps have read it.
+      if (L::kAlias && p_side) ok = ok && warp_wait(p_free, (g - 1) & 1, ctl);
       if (!ok) break;
       tc_fence_after();
       issue_t(sq, so);
@@ -481,20 +506,31 @@ __global__ void __maxnreg__(168)
         const int so1 = (so + 1 == kOS) ? 0 : so + 1;
         const bool more = t + 1 < T;
         const uint32_t ph = g & 1;
-        if (more) {
-          // The next score product as soon as this side's warps have read the current one.
-          if (!wait_operands(g + 1, sq1, so1) || !warp_wait(t_free, ph, ctl)) { ok = false; break; }
+        // The next score product as soon as this side's warps have read the current one
+        // -- or, with P^T / dS^T in the score columns (kAlias), after this iteration's dV
+        // / dK product (the tensor pipe runs one thread's MMAs in issue order, so that
+        // product reads P^T / dS^T before the next scores overwrite them) and, on the P
+        // side, once the dS warps have read P^T.
+        auto issue_next = [&]() -> bool {
+          if (!more) return true;
+          if (!wait_operands(g + 1, sq1, so1) || !warp_wait(t_free, ph, ctl)) return false;
+          if (L::kAlias && p_side && !warp_wait(p_free, ph, ctl)) return false;
           tc_fence_after();
           issue_t(sq1, so1);
-        }
+          return true;
+        };
+        if (!L::kAlias && !issue_next()) { ok = false; break; }
         if (p_side) {
           if (!warp_wait(o_full(so), (g / kOS) & 1, ctl) || !warp_wait(p_full, ph, ctl)) { ok = false; break; }
           tc_fence_after();
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < kTileRows / 16; ++kk)                      // dV += P^T dO
-              mma_ts(tdV, tP + kk * 8, kdO_mn + so * kStageDesc + kk * kRowStep, idesc_acc,
-                     (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+              for (int c = 0; c < L::kSubTiles; ++c)
+                mma_ts(tdV + c * (HD / L::kSubTiles), tP + kk * 8,
+                       kdO_mn + so * kStageDesc + c * kSubDesc + kk * kRowStep, idesc_acc,
+                       (t > 0 || kk > 0) ? 1u : 0u);
             mma_commit(dv_done);
             mma_commit(q_empty(sq));                 // S^T and dV are done with both stages
             mma_commit(o_empty(so));
@@ -526,14 +562,18 @@ __global__ void __maxnreg__(168)
             if (elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < kTileRows / 16; ++kk)                    // dK += dS^T Q
-                mma_ts(tdK, tdS + kk * 8, kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc,
-                       (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int c = 0; c < L::kSubTiles; ++c)
+                  mma_ts(tdK + c * (HD / L::kSubTiles), tdS + kk * 8,
+                         kQ_mn + sq * kStageDesc + c * kSubDesc + kk * kRowStep, idesc_acc,
+                         (t > 0 || kk > 0) ? 1u : 0u);
               mma_commit(q_empty(sq));               // dP^T and dK are done with the Q stage
               mma_commit(dk_done);
             }
             __syncwarp();
           }
         }
+        if (L::kAlias && !issue_next()) { ok = false; break; }
         sq = sq1;
         so = so1;
       }
@@ -866,6 +906,9 @@ cudaError_t launch_bwd_preprocess(const __nv_bfloat16 *o, const __nv_bfloat16 *d
   if (hd == 32)
     return launch_pdl(bwd_preprocess_kernel<32>, grid, 256, 0, stream, o, dO, lse, aux, ws.D, dqacc, B, S, nh,
                       lse_mult);
+  if (hd == 128)
+    return launch_pdl(bwd_preprocess_kernel<128>, grid, 256, 0, stream, o, dO, lse, aux, ws.D, dqacc, B, S, nh,
+                      lse_mult);
   return cudaErrorInvalidValue;
 }
 
@@ -884,6 +927,8 @@ cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
   if (hd == 32)
     return mdq ? launch_main_hd<32, true>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream)
                : launch_main_hd<32, false>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+  if (hd == 128 && !mdq)
+    return launch_main_hd<128, false>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
   return cudaErrorInvalidValue;
 }
 

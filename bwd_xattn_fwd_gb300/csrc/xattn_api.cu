@@ -293,10 +293,13 @@ xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return XATTN_ERR_NULL_PTR;
   XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
   XATTN_TRY(check_bwd_scale(scale));
-  XATTN_TRY(check_bf16(hd));
+  XATTN_TRY(check_bf16_fwd(hd));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return XATTN_ERR_MISALIGNED;
+  // hd = 128: dV, dK and a dQ accumulator do not fit in TMEM together, so dQ comes from
+  // the query-stationary kernel (the deterministic backward).
+  if (hd == 128) return xattn_bwd_deterministic(q, k, v, o, dO, lse, B, S, nh, nkv, hd, scale, dq, dk, dv, stream);
   DeviceInfo *dev = nullptr;
   XATTN_TRY(bf16_device(&dev));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -343,7 +346,7 @@ xattn_status xattn_bwd_deterministic(const void *q, const void *k, const void *v
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return XATTN_ERR_NULL_PTR;
   XATTN_TRY(check_shape(B, S, nh, nkv, hd, scale));
   XATTN_TRY(check_bwd_scale(scale));
-  XATTN_TRY(check_bf16(hd));
+  XATTN_TRY(check_bf16_fwd(hd));
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
       !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
     return XATTN_ERR_MISALIGNED;

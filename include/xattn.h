@@ -51,7 +51,9 @@ typedef enum {
     XATTN_ERR_NULL_PTR = 1,           /* a required pointer is NULL */
     XATTN_ERR_BAD_SHAPE = 2,          /* B, S, nh, nkv or hd <= 0, or a size overflows int32 */
     XATTN_ERR_GROUP = 3,              /* nh is not a multiple of nkv */
-    XATTN_ERR_UNSUPPORTED_HD = 4,     /* bf16: hd not in {32, 64}; fp32: hd > 128 */
+    XATTN_ERR_UNSUPPORTED_HD = 4,     /* bf16: hd not in {32, 64, 128} (the backward's
+                                         stage calls and xattn_bwd_noalloc: {32, 64});
+                                         fp32: hd > 128 */
     XATTN_ERR_MISALIGNED = 5,         /* a bf16 tensor pointer is not 16-byte aligned */
     XATTN_ERR_CUDA = 6,               /* a CUDA runtime or driver call failed */
     XATTN_ERR_NO_DEVICE_SUPPORT = 7,  /* the current device is not compute capability 10.3 */
@@ -65,7 +67,7 @@ typedef enum {
 /*
  * Forward, bf16 (xtrain docs/evolution.md, row T14: online softmax tiled over KV,
  * per-row log-sum-exp kept). q, k, v, o are bf16; lse is float.
- * hd in {32, 64}; any S >= 1. Arithmetic: bf16 products, fp32 accumulation and
+ * hd in {32, 64, 128}; any S >= 1. Arithmetic: bf16 products, fp32 accumulation and
  * softmax statistics (row T12: softmax kept in fp32 under bf16); P is rounded to bf16
  * before the P.V product; o is rounded to nearest even.
  */
@@ -83,6 +85,9 @@ xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S
  * dQ is accumulated across key tiles with fp32 reduce-adds whose order is not fixed,
  * so its last bits may vary from run to run; dK, dV, o and lse are bit-for-bit
  * reproducible. xattn_bwd_deterministic gives a dQ that is reproducible too.
+ * hd in {32, 64, 128}. At hd = 128 dV, dK and a dQ accumulator do not fit in the
+ * tensor memory together, so xattn_bwd runs xattn_bwd_deterministic (every output
+ * reproducible; scratch as described there).
  */
 xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *o,
                        const void *dO, const float *lse, int B, int S, int nh, int nkv,
@@ -93,6 +98,7 @@ xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *
  * memory themselves (or capture the call in a CUDA graph). xattn_bwd is exactly
  * workspace allocation + these three calls + release.
  *
+ * hd in {32, 64} only (hd = 128 has no fused dQ step; use xattn_bwd).
  * workspace: device pointer, 256-byte aligned, at least xattn_bwd_workspace_bytes()
  * bytes. Its contents on entry do not matter; the three steps must run in this order
  * on one stream with the same arguments.
@@ -137,7 +143,7 @@ xattn_status xattn_bwd_deterministic(const void *q, const void *k, const void *v
  * whose device memory is already fully reserved by its own allocator, so the
  * cudaMallocAsync inside xattn_bwd would fail.
  *
- * Same arguments and results as xattn_bwd. The scratch (xattn_bwd_workspace_bytes(B, S,
+ * Same arguments and results as xattn_bwd, for hd in {32, 64}. The scratch (xattn_bwd_workspace_bytes(B, S,
  * nh, hd) bytes) lives in one fixed device array of XATTN_NOALLOC_SCRATCH_BYTES inside
  * the library; every GPU that loads the library holds that array until the process
  * exits. Sizes that need more return XATTN_ERR_SCRATCH_LIMIT before anything is

@@ -92,16 +92,28 @@ def test_bwd_scale_checks(lib):
         assert _bwd(lib, 2.0 ** -64) == 6
 
 
-def test_head_dim_128_forward_only(lib):
-    """bf16 hd = 128 passes the forward's host checks; the backward rejects it."""
+def test_head_dim_128(lib):
+    """bf16 hd = 128 passes the host checks of the forward and of both backwards; the
+    backward's stage calls and the no-allocation backward (fused dQ only) reject it."""
     import torch
+    bwd_types = ([ctypes.c_void_p] * 5 + [ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_float]
+                 + [ctypes.c_void_p] * 4)
+    args = (16, 32, 48, 64, 80, 96, 1, 4, 2, 1, 128, 0.1, 112, 128, 144, None)
+    for name in ("xattn_bwd", "xattn_bwd_deterministic", "xattn_bwd_noalloc"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = bwd_types
+        if name == "xattn_bwd_noalloc":
+            assert f(*args) == 4
+        elif not torch.cuda.is_available():
+            assert f(*args) == 6                       # accepted; fails only for want of a GPU
     if not torch.cuda.is_available():
-        assert _fwd(lib, hd=128) == 6                  # accepted; fails only for want of a GPU
-    f = lib.xattn_bwd
+        assert _fwd(lib, hd=128) == 6
+    f = lib.xattn_bwd_main
     f.restype = ctypes.c_int
-    f.argtypes = ([ctypes.c_void_p] * 5 + [ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_float]
-                  + [ctypes.c_void_p] * 4)
-    assert f(16, 32, 48, 64, 80, 96, 1, 4, 2, 1, 128, 0.1, 112, 128, 144, None) == 4
+    f.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 5 + [ctypes.c_float] + [ctypes.c_void_p] * 2 + \
+        [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert f(16, 32, 48, 64, 1, 4, 2, 1, 128, 0.1, 80, 96, 256, 1 << 20, None) == 4
 
 
 def test_f32_head_dim_limit(lib):

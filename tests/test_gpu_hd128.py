@@ -1,14 +1,17 @@
-"""bf16 forward at head dim 128 against the oracle: each tile is two 64-column swizzled
-sub-tiles, one Q buffer and two K/V stages, and P written over its own scores in TMEM.
-Shapes cover S = 1, partial tiles, one-tile and many-tile sequences with and without a
-second query tile per unit, and groups 1 to 8; scales zero, negative and large."""
+"""bf16 forward and backward at head dim 128 against the oracle. Each tile is two
+64-column swizzled sub-tiles; the forward keeps one Q buffer and two K/V stages and
+writes P over its own scores in TMEM; the backward runs the key-stationary dK / dV
+kernel (P^T over S^T, dS^T over dP^T) and the query-stationary dQ kernel. Shapes cover
+S = 1, partial tiles, one-tile and many-tile sequences with and without a second query
+tile per unit, and groups 1 to 8; scales zero, negative and large."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from bwd_xattn_fwd_gb300 import workloads as W
-from gpu_path import TOL_BF16, TOL_LSE, rel_err
+from gpu_path import (TOL_BF16, TOL_LSE, check_invariants, compare, gpu_unit, oracle_full, oracle_unit,
+                      rel_err, run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -73,3 +76,46 @@ def test_fwd_hd128_matches_fp32_path_rows():
     torch.cuda.synchronize()
     assert rel_err(o, W.as_f64(o32)) <= TOL_BF16
     assert float(np.abs(lse - W.as_f64(lse32)).max()) <= TOL_LSE
+
+
+# ---- backward at hd = 128: the key-stationary dK / dV kernel with P^T over S^T and
+# dS^T over dP^T in TMEM, and the query-stationary dQ kernel; xattn_bwd takes that path
+# (every output reproducible) ----
+BWD_SHAPES = [(1, 1, 2, 1), (2, 77, 4, 2), (1, 300, 4, 1), (2, 513, 6, 3), (1, 1024, 4, 4)]
+
+
+@pytest.mark.parametrize("shape", BWD_SHAPES, ids=lambda s: "B%d_S%d_nh%d_nkv%d" % s)
+def test_bwd_hd128_shapes(shape):
+    B, S, nh, nkv = shape
+    w = W.Workload("hd128", B, S, nh, nkv, 128, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=19)
+    compare(run_gpu(w, x), oracle_full(w, x), "bf16", str(shape))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.3], ids=lambda s: "scale=%g" % s)
+def test_bwd_hd128_scales(scale):
+    w = W.Workload("hd128", 2, 300, 4, 2, 128, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=23)
+    compare(run_gpu(w, x, scale=scale), oracle_full(w, x, scale=scale), "bf16", "scale=%g" % scale)
+
+
+def test_bwd_hd128_long_sampled_units():
+    """A long-sequence GQA problem at hd = 128 (4 x 4096, 16 query heads on 4 kv heads):
+    sampled (batch, kv head) units element by element, and the gradient identities on
+    the whole output."""
+    w = W.Workload("hd128_long", 4, 4096, 16, 4, 128, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=29)
+    out = run_gpu(w, x)
+    for b, kvh in sorted({(0, 0), (w.B - 1, w.nkv - 1)}):
+        compare(gpu_unit(w, out, b, kvh), oracle_unit(w, x, b, kvh), "bf16", f"unit ({b}, {kvh})")
+    check_invariants(w, x, out, tol=TOL_BF16)
+
+
+def test_bwd_hd128_reproducible_and_same_as_deterministic():
+    w = W.Workload("hd128", 2, 700, 8, 2, 128, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=31)
+    a = run_gpu(w, x)
+    b = run_gpu(w, x)
+    c = run_gpu(w, x, deterministic=True)
+    for n in ("o", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(a[n], b[n]) and np.array_equal(a[n], c[n]), n
