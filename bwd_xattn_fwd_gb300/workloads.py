@@ -82,9 +82,12 @@ WORKLOADS = {
     "long": Workload("long", B=4, S=4096, nh=16, nkv=4, hd=64, dtype="bf16",
                      qkv_scale=0.5, do_scale=1.0,
                      description="long-seq dim1024 GQA, group 4"),
+    "long_hd128": Workload("long_hd128", B=4, S=4096, nh=16, nkv=4, hd=128, dtype="bf16",
+                           qkv_scale=0.5, do_scale=1.0,
+                           description="long-seq GQA at head dim 128 (dim2048), group 4"),
 }
 
-ORDER = ["tiny", "dim384", "dim768", "gqa", "long"]
+ORDER = ["tiny", "dim384", "dim768", "gqa", "long", "long_hd128"]
 
 
 def torch_dtype(w: Workload):
