@@ -73,6 +73,27 @@ struct FwdLayout {
   static_assert(kSubBytes % 1024 == 0 && kTileBytes % 1024 == 0, "swizzled tiles need 1024-byte alignment");
 };
 
+
+// 2^x for a pair on the FMA pipe: x = j + f with j = rint(x) and |f| <= 1/2 (x clamped
+// at -126), 2^f from a cubic fitted to it on [-1/2, 1/2] by least squares on Chebyshev
+// nodes (relative error below 8e-5), and j added into the exponent field.
+__device__ __forceinline__ void exp2_fma2(float x0, float x1, float &y0, float &y1) {
+  constexpr float kRound = 12582912.f;   // 1.5 * 2^23: x + kRound is rint(x) in the low bits
+  constexpr float c0 = 0.9999279975891113f, c1 = 0.6932597756385803f;
+  constexpr float c2 = 0.24261167645454407f, c3 = 0.05517822131514549f;
+  x0 = fmaxf(x0, -126.f);
+  x1 = fmaxf(x1, -126.f);
+  float j0, j1, t0, t1, f0, f1, p0, p1;
+  fadd2(j0, j1, x0, x1, kRound, kRound);
+  fadd2(t0, t1, j0, j1, -kRound, -kRound);
+  ffma2(f0, f1, t0, t1, -1.f, -1.f, x0, x1);
+  ffma2(p0, p1, f0, f1, c3, c3, c2, c2);
+  ffma2(p0, p1, p0, p1, f0, f1, c1, c1);
+  ffma2(p0, p1, p0, p1, f0, f1, c0, c0);
+  y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(j0) << 23));
+  y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(j1) << 23));
+}
+
 // Warp-uniform bounded wait: every lane waits, then all agree.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
   const bool ok = mbar_wait(bar, parity, ctl);
@@ -400,6 +421,8 @@ __global__ void __maxnreg__(168)
         const float neg_m = -m_use;
         // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
         // included), the exponentials, row sums and bf16 P, packed in place into r[0, 64).
+        // One pair in eight of an unmasked tile is exponentiated on the FMA pipe
+        // (exp2_fma2) instead of MUFU, which both tiles' softmax warps share.
         // The diagonal tile has its own copy of the body, so the common one is branch-free.
         // The first three quarters of P are computed before waiting for the previous PV_X
         // (which still reads P_X), so that product's latency overlaps the exponentials;
@@ -416,7 +439,13 @@ __global__ void __maxnreg__(168)
               if (c > row) x0 = -INFINITY;
               if (c + 1 > row) x1 = -INFINITY;
             }
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            float p0, p1;
+            if (!decltype(masked)::value && (e & 7) == 7) {
+              exp2_fma2(x0, x1, p0, p1);
+            } else {
+              p0 = ex2_approx(x0);
+              p1 = ex2_approx(x1);
+            }
             const int a = (e & 1) * 2;
             fadd2(ps[a], ps[a + 1], ps[a], ps[a + 1], p0, p1);
             r[c32 / 2 + e] = pack_bf16x2(p0, p1);
