@@ -41,6 +41,7 @@ KERNEL_SOURCES = {
     "bwd_preprocess_kernel": ["attn_bwd_sm103.cu"],
     "dq_convert_kernel": ["attn_bwd_sm103.cu"],
     "decode_partial_kernel + decode_combine_kernel": ["attn_decode.cu", "sm103_ptx.cuh"],
+    "bwd_deterministic": ["attn_bwd_sm103.cu", "attn_bwd_dq_sm103.cu", "sm103_ptx.cuh"],
 }
 
 
