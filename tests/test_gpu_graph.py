@@ -65,8 +65,9 @@ def test_graph_replay_matches_eager(hd, step):
     w = W.Workload("graph", 2, 700, 8, 2, hd, "bf16", qkv_scale=0.5)
     x1, x2 = W.make_inputs(w, seed=41), W.make_inputs(w, seed=42)
     t = _buffers(w, x1)
-    ws = torch.empty(max(1, xattn.xattn_bwd_workspace_bytes(w.B, w.S, w.nh, min(hd, 64))),
-                     dtype=torch.uint8, device="cuda")
+    ws = None                               # xattn_bwd takes its own scratch
+    if step == "stages":
+        ws = torch.empty(xattn.xattn_bwd_workspace_bytes(w.B, w.S, w.nh, hd), dtype=torch.uint8, device="cuda")
     run = _step_stages if step == "stages" else _step_api
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
