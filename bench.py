@@ -78,6 +78,20 @@ def source_sha(kernel: str) -> str:
     return h.hexdigest()[:16]
 
 
+def packed_views(specs, device=None, pin=False):
+    """One flat byte buffer holding tensors of the given (name, shape, dtype), each at a
+    256-byte-aligned offset, so that a step moves its inputs (or outputs) with one copy.
+    Returns (flat buffer, {name: typed view})."""
+    import torch
+    offs, total = {}, 0
+    for n, shape, dt in specs:
+        nbytes = int(torch.Size(shape).numel()) * torch.empty((), dtype=dt).element_size()
+        offs[n] = (total, nbytes, shape, dt)
+        total = (total + nbytes + 255) // 256 * 256
+    flat = torch.empty(total, dtype=torch.uint8, device=device, pin_memory=pin)
+    return flat, {n: flat[o:o + nb].view(dt).view(shape) for n, (o, nb, shape, dt) in offs.items()}
+
+
 def ncu_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu capture, or None if there is none
     for this kernel and workload or the kernel's source changed since."""
@@ -386,14 +400,19 @@ def run_ours(args, w: W.Workload):
     # H2D copies of step i+1 and the D2H copies of step i-1 run while step i computes.
     e2e = None
     if not args.no_e2e:
-        h_in = {n: t.pin_memory() for n, t in x_cpu.items()}
-        d_in = [{n: torch.empty_like(t, device=dev) for n, t in x_cpu.items()} for _ in range(2)]
-        outs = (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))
-        d_out = [{n: torch.empty_like(t) for n, t in outs} for _ in range(2)]
-        h_out = [{n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for n, t in outs}
-                 for _ in range(2)]
-        h2d = sum(t.numel() * t.element_size() for t in h_in.values())
-        d2h = sum(t.numel() * t.element_size() for t in h_out[0].values())
+        # Each step's inputs sit in one pinned buffer and its outputs in one device buffer
+        # (256-byte-aligned views), so a step is one H2D and one D2H copy.
+        in_specs = [(n, tuple(t.shape), t.dtype) for n, t in x_cpu.items()]
+        out_specs = [(n, tuple(t.shape), t.dtype) for n, t in
+                     (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))]
+        h_in_flat, h_in = packed_views(in_specs, pin=True)
+        for n, t in x_cpu.items():
+            h_in[n].copy_(t)
+        d_in = [packed_views(in_specs, device=dev) for _ in range(2)]
+        d_out = [packed_views(out_specs, device=dev) for _ in range(2)]
+        h_out = [packed_views(out_specs, pin=True) for _ in range(2)]
+        h2d = h_in_flat.numel()
+        d2h = h_out[0][0].numel()
         s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(dev) for _ in range(3))
         h2d_done = [torch.cuda.Event() for _ in range(2)]
         cmp_done = [torch.cuda.Event() for _ in range(2)]
@@ -402,12 +421,11 @@ def run_ours(args, w: W.Workload):
 
         def e2e_step(i):
             j = i % 2
-            di, do_, ho = d_in[j], d_out[j], h_out[j]
+            (di_flat, di), (do_flat, do_), (ho_flat, _) = d_in[j], d_out[j], h_out[j]
             if i >= 2:
                 s_h2d.wait_event(cmp_done[j])          # step i-2 has consumed d_in[j]
             with torch.cuda.stream(s_h2d):
-                for n in h_in:
-                    di[n].copy_(h_in[n], non_blocking=True)
+                di_flat.copy_(h_in_flat, non_blocking=True)
             h2d_done[j].record(s_h2d)
             s_cmp.wait_event(h2d_done[j])
             if i >= 2:
@@ -419,8 +437,7 @@ def run_ours(args, w: W.Workload):
             cmp_done[j].record(s_cmp)
             s_d2h.wait_event(cmp_done[j])
             with torch.cuda.stream(s_d2h):
-                for n in ho:
-                    ho[n].copy_(do_[n], non_blocking=True)
+                ho_flat.copy_(do_flat, non_blocking=True)
             d2h_done[j].record(s_d2h)
 
         for i in range(max(3, args.warmup)):
@@ -439,13 +456,15 @@ def run_ours(args, w: W.Workload):
             raise RuntimeError("device status in the e2e run")
         # The last step's results are the same as the device-resident run's.
         last = (args.steps - 1) % 2
-        if not (torch.equal(h_out[last]["o"], o.cpu()) and torch.equal(h_out[last]["dk"], dk.cpu())):
+        ho_last = h_out[last][1]
+        if not (torch.equal(ho_last["o"], o.cpu()) and torch.equal(ho_last["dk"], dk.cpu())):
             raise RuntimeError("e2e outputs differ from the device-resident run")
         e2e = {"value": flops_step * world * args.steps / (t_e2e * 1e-3) / 1e12, "unit": "TFLOP/s",
                "tok_per_s": w.tokens * world * args.steps / (t_e2e * 1e-3),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "note": "steps pipelined over three streams (H2D of the next step and D2H of the "
-                       "previous one overlap this step's kernels), two sets of device buffers"}
+                       "previous one overlap this step's kernels), two sets of device buffers; a "
+                       "step's inputs and outputs each move as one packed copy"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
