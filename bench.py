@@ -615,6 +615,9 @@ def run_decode(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         t = max_over_ranks(pg, e0.elapsed_time(e1), dev)
+        # Decode is bit-reproducible: the host copy of the last step equals the device run's.
+        if not (torch.equal(h_o, o.cpu()) and torch.equal(h_l, lse.cpu())):
+            raise RuntimeError("decode e2e outputs differ from the device-resident run")
         e2e = {"value": w.io_bytes * world * args.steps / (t * 1e-3) / 1e9, "unit": "GB/s",
                "tok_per_s": B * world * args.steps / (t * 1e-3),
                "h2d_bytes_per_step": h_q.numel() * h_q.element_size(),
