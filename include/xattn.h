@@ -37,8 +37,8 @@
  *     two seconds) gives up, records XATTN_ERR_DEVICE_TIMEOUT in a device status word
  *     and finishes; xattn_check_device_status reports it.
  *   - CUDA graphs: the calls may be captured on a stream and replayed, once the device
- *     has seen one ordinary call of the same entry point (the first call on a device
- *     looks up its status word and sets kernel attributes). Entry points that take
+ *     has seen one ordinary call (the first call on a device looks up its device
+ *     status word, which a capture may not do). Entry points that take
  *     scratch with cudaMallocAsync record it in the graph as stream-ordered
  *     allocation nodes.
  */
