@@ -38,7 +38,7 @@
  *     and finishes; xattn_check_device_status reports it.
  *   - CUDA graphs: the calls may be captured on a stream and replayed, once the device
  *     has seen one ordinary call (the first call on a device looks up its device
- *     status word, which a capture may not do). Entry points that take
+ *     status word; make that call outside the capture). Entry points that take
  *     scratch with cudaMallocAsync record it in the graph as stream-ordered
  *     allocation nodes.
  */
