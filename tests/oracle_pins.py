@@ -148,6 +148,26 @@ def pin_torch_sdpa(orc):
         assert _rel(a, back(t)) < 1e-12, _rel(a, back(t))
 
 
+def pin_torch_sdpa_head_dims(orc):
+    """The same agreement at the head dims the kernels take (32, 64, 128), with groups of
+    2 and 4 and a length that is not a multiple of anything in particular."""
+    import torch
+    import torch.nn.functional as F
+    for hd, nh, nkv in ((32, 4, 2), (64, 4, 1), (128, 8, 2)):
+        q, k, v, dO = _problem(B=1, S=19, nh=nh, nkv=nkv, hd=hd, seed=30 + hd)
+        scale = 1 / math.sqrt(hd)
+        tq, tk, tv = (torch.tensor(x.transpose(0, 2, 1, 3).copy(), requires_grad=True)
+                      for x in (q, k, v))
+        out = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=scale, enable_gqa=True)
+        out.backward(torch.tensor(dO.transpose(0, 2, 1, 3).copy()))
+        o, _ = orc.fwd(q, k, v, scale)
+        dq, dk, dv = orc.bwd(q, k, v, dO, scale)
+        back = lambda t: t.detach().numpy().transpose(0, 2, 1, 3)  # noqa: E731
+        assert _rel(o, back(out)) < 1e-12, hd
+        for a, t in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            assert _rel(a, back(t)) < 1e-12, (hd, _rel(a, back(t)))
+
+
 def pin_gqa_equals_repeated_mha(orc):
     """GQA on (K, V) equals MHA on K/V repeated per group, with dK/dV summed over each group."""
     q, k, v, dO = _problem(B=2, S=8, nh=6, nkv=3, hd=4, seed=8)
@@ -247,6 +267,7 @@ def pin_decode_composed(orc):
 
 
 PINS = [pin_golden_two_positions, pin_zero_queries, pin_single_position, pin_constant_values,
-        pin_finite_differences, pin_composed, pin_torch_sdpa, pin_gqa_equals_repeated_mha,
+        pin_finite_differences, pin_composed, pin_torch_sdpa, pin_torch_sdpa_head_dims,
+        pin_gqa_equals_repeated_mha,
         pin_invariants, pin_key_shift, pin_decode_last_row, pin_decode_closed_forms,
         pin_decode_composed]
