@@ -11,15 +11,16 @@
 //   warp 0     : TMA producer. Q_A and Q_B once per unit, into one of two buffers, so a
 //                unit's query tiles land while the previous unit still runs; K/V tiles
 //                through a 3-stage ring that runs on across units.
-//   warp 1     : TMEM owner and MMA issuer (converged warp, one elected lane issues):
+//   warps 1, 3 : MMA issuers, warp 1 for tile A (and TMEM owner), warp 3 for tile B
+//                (converged warps, one elected lane issues):
 //                  S_X(n) = Q_X K_n^T  (A, B from shared memory) -> TMEM
 //                  O_X   += P_X(n) V_n (A = P from TMEM)          -> TMEM accumulator
-//                alternating X = A, B, so the tensor core works on one tile while the
-//                other tile's softmax runs; S_X(n+1) is issued as soon as the softmax has
-//                read S_X(n), before it finishes P_X(n).
+//                so the tensor core works on one tile while the other tile's softmax
+//                runs; S_X(n+1) is issued as soon as the softmax has read S_X(n), before
+//                it finishes P_X(n). Each K/V stage is released by a commit from both.
 //   warps 4-7  : softmax of tile A, one thread per query row (TMEM lane), all 128 key
 //                columns of a tile; warps 8-11 the same for tile B.
-//   warps 2-3  : idle.
+//   warp 2     : idle.
 // Softmax per key tile: causal mask on the diagonal tile, running max and sum in fp32
 // (log2 domain), P in bf16 to TMEM, O rescaled only when the running max grows by more
 // than 2^8 (the stale max is exact because the final normalisation uses the same max).

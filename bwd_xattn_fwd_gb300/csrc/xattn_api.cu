@@ -409,7 +409,7 @@ const char *xattn_status_string(xattn_status s) {
     case XATTN_ERR_NULL_PTR: return "a required pointer is NULL";
     case XATTN_ERR_BAD_SHAPE: return "B, S, nh, nkv and hd must be positive and within size limits";
     case XATTN_ERR_GROUP: return "nh must be a multiple of nkv";
-    case XATTN_ERR_UNSUPPORTED_HD: return "unsupported head dimension (bf16: 32 or 64; fp32: <= 128)";
+    case XATTN_ERR_UNSUPPORTED_HD: return "unsupported head dimension (bf16: 32, 64 or 128; the backward's stage calls and xattn_bwd_noalloc: 32 or 64; fp32: <= 128)";
     case XATTN_ERR_MISALIGNED: return "a bf16 tensor pointer is not 16-byte aligned";
     case XATTN_ERR_CUDA: return "a CUDA runtime or driver call failed";
     case XATTN_ERR_NO_DEVICE_SUPPORT: return "the current device is not compute capability 10.3 (sm_103)";

@@ -8,11 +8,14 @@
 // library would fail. xattn_bwd takes its scratch with cudaMallocAsync; this entry
 // point takes none.
 //
-// The scratch is a file-scope device array of XATTN_NOALLOC_SCRATCH_BYTES (64 MiB). It
-// exists on every GPU that loads this library, from module load until process exit.
+// The scratch is a file-scope device array of XATTN_NOALLOC_SCRATCH_BYTES (64 MiB).
+// CUDA loads a library's device code lazily, so the array is placed on a GPU by the
+// first call of this entry point on that GPU, and stays there until the process exits.
 // Host code cannot use the array's name as a device address (on the host it names a
-// stand-in object), so the first call on each device looks the address up with
-// cudaGetSymbolAddress while that device is current, and every later call reuses it.
+// stand-in object), so that first call looks the address up with cudaGetSymbolAddress
+// while the device is current (which is what loads the module and places the array),
+// and every later call reuses it. A failed lookup (say the device had no 64 MiB left)
+// is not remembered: the next call tries again.
 #include <cmath>
 #include <mutex>
 
@@ -26,24 +29,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[XATTN_NOALLOC_S
 
 constexpr int kMaxNoAllocDevices = 64;
 
-struct ScratchSlot {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  void *ptr = nullptr;
-};
-ScratchSlot g_slots[kMaxNoAllocDevices];
+std::mutex g_slots_mutex;
+void *g_slots[kMaxNoAllocDevices];   // scratch address per device; null until found
 
-// Device address of the scratch array on the current device (looked up once per device).
-xattn_status scratch_address(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxNoAllocDevices)
-    return XATTN_ERR_CUDA;
-  ScratchSlot &slot = g_slots[dev];
-  std::call_once(slot.once, [&slot] {
-    slot.err = cudaGetSymbolAddress(&slot.ptr, g_noalloc_scratch);
-  });
-  if (slot.err != cudaSuccess || slot.ptr == nullptr) return XATTN_ERR_CUDA;
-  *out = slot.ptr;
+// Device address of the scratch array on the current device. Only a successful lookup is
+// kept, so a device where it failed once is tried again on the next call.
+xattn_status scratch_address(int dev, void **out) {
+  if (dev < 0 || dev >= kMaxNoAllocDevices) return XATTN_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_slots_mutex);
+  if (g_slots[dev] == nullptr) {
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();   // do not leave the failure for the caller's next error check
+      return XATTN_ERR_CUDA;
+    }
+    g_slots[dev] = ptr;
+  }
+  *out = g_slots[dev];
   return XATTN_OK;
 }
 
@@ -68,8 +70,14 @@ extern "C" xattn_status xattn_bwd_noalloc(const void *q, const void *k, const vo
   const size_t need = xattn_bwd_workspace_bytes(B, S, nh, hd);
   if (need == 0) return XATTN_ERR_BAD_SHAPE;
   if (need > static_cast<size_t>(XATTN_NOALLOC_SCRATCH_BYTES)) return XATTN_ERR_SCRATCH_LIMIT;
+  // The scratch address is the current device's, so the stream must belong to it.
+  int dev = 0, stream_dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return XATTN_ERR_CUDA;
+  if (cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &stream_dev) != cudaSuccess ||
+      stream_dev != dev)
+    return XATTN_ERR_CUDA;
   void *scratch = nullptr;
-  const xattn_status st = xattn::scratch_address(&scratch);
+  const xattn_status st = xattn::scratch_address(dev, &scratch);
   if (st != XATTN_OK) return st;
   // The three steps rewrite every scratch byte they read (the preprocess writes every
   // auxiliary row, pad rows included, and every D_i, and zeroes the dQ accumulator), so

@@ -28,9 +28,9 @@
  * Conventions shared by every entry point:
  *   - Pointers are DEVICE pointers owned by the caller, unless a comment says
  *     otherwise. Inputs are read only. Outputs are overwritten, never accumulated into.
- *   - stream is a cudaStream_t (NULL = the legacy default stream). Calls enqueue work
- *     and return; none synchronises the device (xtrain docs/06-performance.md,
- *     "Phase T7", design decision 3: no per-op synchronisation).
+ *   - stream is a cudaStream_t (NULL = the legacy default stream) of the current
+ *     device. Calls enqueue work and return; none synchronises the device (xtrain
+ *     docs/06-performance.md, "Phase T7", design decision 3: no per-op synchronisation).
  *   - Argument checks run before any launch. On a check failure nothing is enqueued
  *     and the outputs are untouched. Launch failures return XATTN_ERR_CUDA.
  *   - A kernel that waits on an on-chip barrier longer than a bounded time (about
@@ -150,11 +150,14 @@ xattn_status xattn_bwd_deterministic(const void *q, const void *k, const void *v
  *
  * Same arguments and results as xattn_bwd, for hd in {32, 64}. The scratch (xattn_bwd_workspace_bytes(B, S,
  * nh, hd) bytes) lives in one fixed device array of XATTN_NOALLOC_SCRATCH_BYTES inside
- * the library; every GPU that loads the library holds that array until the process
- * exits. Sizes that need more return XATTN_ERR_SCRATCH_LIMIT before anything is
+ * the library. Sizes that need more return XATTN_ERR_SCRATCH_LIMIT before anything is
  * launched (64 MiB fits, e.g., B=8, S=2048, nh=8, hd=64).
- * The first call on a device looks up the array's device address for that device
- * (cudaGetSymbolAddress); make that first call before any stream capture on the device.
+ * CUDA loads the library's device code lazily: the first call on a device places the
+ * 64 MiB array on that device (looking up its address with cudaGetSymbolAddress), and
+ * the device holds it until the process exits. Make that first call before the host's
+ * own allocator reserves the device's memory, and before any stream capture on the
+ * device. If it fails (XATTN_ERR_CUDA, e.g. no 64 MiB left), the next call tries again.
+ * `stream` must belong to the current device (else XATTN_ERR_CUDA, nothing launched).
  * All calls share the one array and each call overwrites all of the scratch it uses, so
  * nothing carries over between calls, but calls whose work overlaps on the GPU (on
  * different streams, or from different threads) race on it and must be serialised by

@@ -6,8 +6,7 @@ import pytest
 import torch
 
 from bwd_xattn_fwd_gb300 import workloads as W
-from gpu_path import (TOL_BF16, check_invariants, compare, gpu_unit, oracle_full, oracle_unit,
-                      run_gpu, tol_for)
+from gpu_path import (TOL_BF16, compare, compare_every_unit, oracle_full, run_gpu, tol_for)
 
 pytestmark = pytest.mark.gpu
 
@@ -19,9 +18,17 @@ def _cuda():
     from bwd_xattn_fwd_gb300 import xattn  # noqa: F401  (fails loudly if not built)
 
 
-# Units compared element by element at full size: first and last batch, first and last kv head.
-def _units(w):
-    return sorted({(0, 0), (w.B - 1, w.nkv - 1), (w.B // 2, w.nkv // 2)})
+# Oracle outputs of the seeded full-size workloads (seed 0), computed once per session:
+# the default and the deterministic backward are both compared with them.
+_ORACLE_CACHE = {}
+
+
+def _workload_oracle(name):
+    if name not in _ORACLE_CACHE:
+        w = W.WORKLOADS[name]
+        x = W.make_inputs(w)
+        _ORACLE_CACHE[name] = (x, oracle_full(w, x))
+    return _ORACLE_CACHE[name]
 
 
 @pytest.mark.parametrize("name", ["tiny", "dim384"])
@@ -34,15 +41,15 @@ def test_workload_full(name):
 
 
 @pytest.mark.parametrize("name", ["dim768", "gqa", "long"])
-def test_workload_sampled_units(name):
+def test_workload_every_unit(name):
+    """The full-size workloads, in the launch configuration the benchmark times, compared
+    element by element with the oracle on every (batch, kv head) unit: 384 units of
+    dim768, 16 of gqa and 16 of long."""
     w = W.WORKLOADS[name]
-    x = W.make_inputs(w)
+    x, ref = _workload_oracle(name)
     out = run_gpu(w, x)
-    for b, kvh in _units(w):
-        rep = compare(gpu_unit(w, out, b, kvh), oracle_unit(w, x, b, kvh), w.dtype,
-                      f"{name} unit (b={b}, kvh={kvh})")
-        print(name, (b, kvh), rep)
-    check_invariants(w, x, out, tol=TOL_BF16)
+    compare(out, ref, w.dtype, name)
+    print(name, compare_every_unit(w, out, ref, name))
 
 
 EDGE = [
@@ -143,12 +150,13 @@ def test_deterministic_scales(scale):
             "det scale=%g" % scale)
 
 
-def test_deterministic_workload_units():
-    w = W.WORKLOADS["gqa"]
-    x = W.make_inputs(w)
+@pytest.mark.parametrize("name", ["gqa", "dim768"])
+def test_deterministic_workload_every_unit(name):
+    w = W.WORKLOADS[name]
+    x, ref = _workload_oracle(name)
     out = run_gpu(w, x, deterministic=True)
-    for b, kvh in _units(w):
-        compare(gpu_unit(w, out, b, kvh), oracle_unit(w, x, b, kvh), "bf16", f"det gqa unit ({b}, {kvh})")
+    compare(out, ref, "bf16", "det " + name)
+    print(name, compare_every_unit(w, out, ref, "det " + name))
 
 
 def test_deterministic_is_bit_reproducible():

@@ -41,6 +41,10 @@ def test_noalloc_matches_bwd_on_two_calls_in_a_row():
             assert torch.isfinite(got).all(), (w.name, name)
             e = _max_rel(got, ref)
             assert e <= TOL_BF16, f"{w.name} {name}: max|err|/max|ref| = {e:.3e}"
+        # Both entry points run the same kernels, and dK, dV are summed in a fixed order,
+        # so they must agree bit for bit: a stale-scratch fault that shifted them only
+        # slightly would show here. (dQ's fp32 reduce-adds have no fixed order.)
+        assert torch.equal(dk2, dk) and torch.equal(dv2, dv), w.name
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
