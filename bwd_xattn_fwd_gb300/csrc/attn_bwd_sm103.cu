@@ -27,6 +27,8 @@
 //      writes dq = bf16(scale * accumulator); the deterministic backward instead runs
 //      the query-stationary dQ kernel of attn_bwd_dq_sm103.cu (dQ accumulated in TMEM
 //      over the key tiles, written once).
+#include <type_traits>
+
 #include "sm103_ptx.cuh"
 #include "xattn_internal.h"
 
@@ -635,36 +637,45 @@ __global__ void __maxnreg__(168)
         reg_fence<128>(r);
         tc_fence_before();
         mbar_arrive(s_free);
+        // 4 chunks of 32 query columns. Within a chunk the 32 exponents are computed
+        // first, then the 32 exponentials, then the bf16 pairs: independent
+        // special-function operations back to back, which one warp per SM sub-partition
+        // needs to keep that unit busy (measured: the exponential chunks take half the
+        // time of a per-pair interleaved order). On the diagonal tile, query column
+        // i < key row j is masked (P = 0); the common body has no mask.
+        auto chunk = [&](auto masked, auto chunk_index, uint32_t *pk) {
+          constexpr int c = decltype(chunk_index)::value;
+          float xs[32];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+          for (int e = 0; e < 32; e += 2)
+            fmul2(xs[e], xs[e + 1], __uint_as_float(r[32 * c + e]), __uint_as_float(r[32 * c + e + 1]),
+                  scale_log2, scale_log2);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) xs[e] = ex2_approx(xs[e]);
+          if constexpr (decltype(masked)::value) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * c + e < j) xs[e] = 0.f;
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(xs[2 * e], xs[2 * e + 1]);
+        };
+        auto body = [&](auto masked) -> bool {
           uint32_t pk[16];
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const uint32_t *cur = r + 32 * c + 4 * q4;
-            float x0, x1, x2, x3;
-            fmul2(x0, x1, __uint_as_float(cur[0]), __uint_as_float(cur[1]), scale_log2, scale_log2);
-            fmul2(x2, x3, __uint_as_float(cur[2]), __uint_as_float(cur[3]), scale_log2, scale_log2);
-            float p0 = ex2_approx(x0), p1 = ex2_approx(x1), p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-            if (diag) {
-              const int i = 32 * c + 4 * q4;
-              if (i + 0 < j) p0 = 0.f;
-              if (i + 1 < j) p1 = 0.f;
-              if (i + 2 < j) p2 = 0.f;
-              if (i + 3 < j) p3 = 0.f;
-            }
-            pk[2 * q4] = pack_bf16x2(p0, p1);
-            pk[2 * q4 + 1] = pack_bf16x2(p2, p3);
-          }
-          if (c == 0) {
-            // P^T of the previous iteration must have been read by the dS warps and by dV.
-            if (!warp_wait(p_free, (g - 1) & 1, ctl) || !warp_wait(dv_done, (g - 1) & 1, ctl)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-          }
-          tmem_st_x16(tP + lane_off + 16 * c, pk);
-        }
+          chunk(masked, std::integral_constant<int, 0>{}, pk);
+          // P^T of the previous iteration must have been read by the dS warps and by dV.
+          if (!warp_wait(p_free, (g - 1) & 1, ctl) || !warp_wait(dv_done, (g - 1) & 1, ctl)) return false;
+          tc_fence_after();
+          tmem_st_x16(tP + lane_off, pk);
+          chunk(masked, std::integral_constant<int, 1>{}, pk);
+          tmem_st_x16(tP + lane_off + 16, pk);
+          chunk(masked, std::integral_constant<int, 2>{}, pk);
+          tmem_st_x16(tP + lane_off + 32, pk);
+          chunk(masked, std::integral_constant<int, 3>{}, pk);
+          tmem_st_x16(tP + lane_off + 48, pk);
+          return true;
+        };
+        if (!(diag ? body(std::true_type{}) : body(std::false_type{}))) ok = false;
         if (!ok) break;
         tmem_wait_st();
         tc_fence_before();
