@@ -48,7 +48,7 @@ KERNEL_SOURCES = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="gqa",
                     choices=[n for n in W.ORDER if n != "tiny"] + list(W.DECODE_WORKLOADS))
@@ -107,6 +107,89 @@ def ncu_traffic(kernel: str, workload: str):
 # ---------------------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------------------
+class NvmlClockSampler:
+    """Reads the SM clock, power and clock-event reasons through NVML (the driver's
+    libnvidia-ml, read-only queries) every 2 ms from a host thread while the timed loops
+    run, so even a timed region of a few milliseconds gets samples under load. Falls back
+    to ClockSampler (nvidia-smi, 100 ms) where NVML cannot be loaded."""
+    PERIOD_S = 0.002
+    # nvmlClocksEventReasons bits
+    REASONS = ((0x8, "hw_slowdown"), (0x40, "hw_thermal_slowdown"),
+               (0x20, "sw_thermal_slowdown"), (0x4, "sw_power_cap"))
+
+    def __init__(self, device_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        bus = torch_pci_bus_id(device_index)
+        if bus is not None:
+            rc = self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.handle))
+        else:
+            rc = self.lib.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.handle))
+        if rc != 0:
+            raise OSError(f"nvmlDeviceGetHandle failed ({rc})")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self.rows = []
+        self.stop = threading.Event()
+        self.thread = None
+
+    def _sample(self):
+        ct = self.ct
+        sm, mx, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        while not self.stop.is_set():
+            ok = (self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(sm)) == 0 and
+                  self.lib.nvmlDeviceGetMaxClockInfo(self.handle, 1, ct.byref(mx)) == 0)
+            pw = self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw)) == 0
+            rr = self.reasons_fn(self.handle, ct.byref(rs)) == 0
+            if ok:
+                self.rows.append({"sm": float(sm.value), "max": float(mx.value),
+                                  "power": mw.value / 1000.0 if pw else None,
+                                  "reasons": rs.value if rr else 0})
+            time.sleep(self.PERIOD_S)
+
+    def __enter__(self):
+        self.thread = threading.Thread(target=self._sample, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+
+    def summary(self):
+        if not self.rows:
+            return None
+        reasons = [name for bit, name in self.REASONS if any(r["reasons"] & bit for r in self.rows)]
+        powers = [r["power"] for r in self.rows if r["power"] is not None]
+        return {"sm_mhz": statistics.median(r["sm"] for r in self.rows),
+                "sm_mhz_min": min(r["sm"] for r in self.rows),
+                "sm_max_mhz": max(r["max"] for r in self.rows), "reasons": reasons,
+                "samples": len(self.rows), "power_w_max": max(powers) if powers else None,
+                "source": "NVML, every 2 ms during the timed loops"}
+
+
+def torch_pci_bus_id(device_index: int):
+    """PCI bus id of a CUDA device as NVML spells it, or None if torch does not expose it."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(device_index)
+        return "%08X:%02X:%02X.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        return None
+
+
+def clock_sampler(device_index: int):
+    try:
+        return NvmlClockSampler(device_index)
+    except (OSError, AttributeError):
+        return ClockSampler(device_index)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -332,7 +415,7 @@ def run_ours(args, w: W.Workload):
               for _ in range(args.steps)]
     barrier(pg)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
+    with clock_sampler(local) as clk:
         for i in range(args.steps):
             flush.zero_()
             step_events[i][0].record(stream)
@@ -572,7 +655,7 @@ def run_decode(args, w):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier(pg)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
+    with clock_sampler(local) as clk:
         for i in range(args.steps):
             flush.zero_()
             evs[i][0].record(stream)

@@ -252,21 +252,29 @@ __global__ void __maxnreg__(168)
   // Warp-uniform by construction; the broadcast lets the compiler see it.
   const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
 
-  // Work units (key tile n, batch b, kv head kvh) are numbered most work first (n
-  // ascending). The CTAs are persistent: CTA c of G takes unit k G + c in even rounds k
-  // and k G + G - 1 - c in odd ones, which evens out the CTAs' total work. Every role
-  // walks the same units; the barriers' phases count iterations over all of them.
+  // Work units (key tile n, batch b, kv head kvh). The CTAs are persistent: CTA c of G
+  // takes unit k G + c in even rounds k and k G + G - 1 - c in odd ones, which evens out
+  // the CTAs' total work. Every role walks the same units; the barriers' phases count
+  // iterations over all of them.
+  // With query groups (group > 1) the units are numbered most work first (n ascending):
+  // they are long, and the order balances the CTAs. With one query head per kv head the
+  // units are short (at most num_m iterations) and are numbered head by head instead
+  // (n fastest), so the CTAs running at the same time work on the same heads and share
+  // their Q, dO and auxiliary tiles in L2 (measured on 32 x 1024 x 12 heads: 248 -> 202
+  // us; on the grouped workloads the same order is 10 % slower).
   const int num_m = (S + kTileRows - 1) / kTileRows;
   const int BK = B * nkv;
   const int group = nh / nkv;
   const int num_units = num_m * BK;
+  const bool head_major = group == 1;
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
   auto unit_at = [&](int k) { return k * G + ((k & 1) ? G - 1 - cta : cta); };
   int n = 0, b = 0, kvh = 0, per_head = 0, T = 0;
   auto set_unit = [&](int u) {
-    n = u / BK;
-    b = (u % BK) / nkv;
-    kvh = u % nkv;
+    const int bk = head_major ? u / num_m : u % BK;
+    n = head_major ? u % num_m : u / BK;
+    b = bk / nkv;
+    kvh = bk % nkv;
     per_head = num_m - n;                 // query tiles m = n .. num_m-1
     T = group * per_head;                 // iterations (r, m)
   };

@@ -54,3 +54,18 @@ def test_traffic_entries_match_current_sources():
                 assert got == e["dram_bytes_per_launch"] == e["read"] + e["write"]
             else:
                 assert got is None
+
+
+def test_nvml_clock_summary_reports_reasons_and_median():
+    """The 2 ms NVML sampler's summary: median and minimum SM clock over the samples, and
+    every throttle reason seen in any sample (bits of nvmlClocksEventReasons)."""
+    bench = _bench()
+    s = bench.NvmlClockSampler.__new__(bench.NvmlClockSampler)
+    s.rows = [{"sm": 2070.0, "max": 2070.0, "power": 900.0, "reasons": 0},
+              {"sm": 2040.0, "max": 2070.0, "power": 1300.0, "reasons": 0x4},
+              {"sm": 2070.0, "max": 2070.0, "power": None, "reasons": 0x1}]
+    out = s.summary()
+    assert out["sm_mhz"] == 2070.0 and out["sm_mhz_min"] == 2040.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"] and out["samples"] == 3 and out["power_w_max"] == 1300.0
+    s.rows = [{"sm": 1500.0, "max": 2070.0, "power": 500.0, "reasons": 0x8 | 0x40}]
+    assert s.summary()["reasons"] == ["hw_slowdown", "hw_thermal_slowdown"]
