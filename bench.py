@@ -42,6 +42,7 @@ KERNEL_SOURCES = {
     "dq_convert_kernel": ["attn_bwd_sm103.cu"],
     "decode_partial_kernel + decode_combine_kernel": ["attn_decode.cu", "sm103_ptx.cuh"],
     "bwd_deterministic": ["attn_bwd_sm103.cu", "attn_bwd_dq_sm103.cu", "sm103_ptx.cuh"],
+    "bwd_resident_dq": ["attn_bwd_sm103.cu", "sm103_ptx.cuh"],
 }
 
 
@@ -55,6 +56,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step as replays of one CUDA graph of it instead of stream launches")
     ap.add_argument("--deterministic", action="store_true",
                     help="time xattn_bwd_deterministic (bit-reproducible dQ) as the backward")
     return ap.parse_args()
@@ -366,36 +369,39 @@ def run_ours(args, w: W.Workload):
     stream = torch.cuda.current_stream(dev)
 
     names = ["attn_fwd_kernel", "bwd_preprocess_kernel", "attn_bwd_main_kernel", "dq_convert_kernel"]
-    # hd = 128 has no fused-dQ backward (its stage calls take hd 32 and 64 only): the
-    # backward is the deterministic one, as xattn_bwd itself runs it there.
-    det = args.deterministic or hd == 128
+    # The backward xattn_bwd (or, with --deterministic, xattn_bwd_deterministic) runs for
+    # these sizes: the fused-dQ one is timed through its three stage calls (one segment
+    # each); the deterministic one (xattn_bwd's at hd = 128) as one segment: its
+    # preprocess, then dQ resident in tensor memory on small problems or the dK/dV and
+    # query-stationary dQ kernels.
+    mode = xattn.xattn_bwd_dq_mode(S, nh, nkv, hd, args.deterministic)
+    det = mode != xattn.BWD_FUSED_DQ
     if det:
-        # xattn_bwd_deterministic runs its three kernels (preprocess, dK/dV recompute, dQ
-        # recompute) inside one call: it is timed as one segment.
-        names = ["attn_fwd_kernel", "bwd_deterministic"]
+        names = ["attn_fwd_kernel",
+                 "bwd_resident_dq" if mode == xattn.BWD_RESIDENT_DQ else "bwd_deterministic"]
 
-    def step(evs=None):
+    def step(evs=None, st=stream):
         if evs:
-            evs[0].record(stream)
-        xattn.xattn_fwd(x["q"], x["k"], x["v"], B, S, nh, nkv, hd, scale, o, lse, stream)
+            evs[0].record(st)
+        xattn.xattn_fwd(x["q"], x["k"], x["v"], B, S, nh, nkv, hd, scale, o, lse, st)
         if evs:
-            evs[1].record(stream)
+            evs[1].record(st)
         if det:
             xattn.xattn_bwd_deterministic(x["q"], x["k"], x["v"], o, x["dO"], lse, B, S, nh, nkv, hd,
-                                          scale, dq, dk, dv, stream)
+                                          scale, dq, dk, dv, st)
             if evs:
-                evs[2].record(stream)
+                evs[2].record(st)
             return
-        xattn.xattn_bwd_preprocess(o, x["dO"], lse, B, S, nh, hd, scale, ws, ws_bytes, stream)
+        xattn.xattn_bwd_preprocess(o, x["dO"], lse, B, S, nh, hd, scale, ws, ws_bytes, st)
         if evs:
-            evs[2].record(stream)
+            evs[2].record(st)
         xattn.xattn_bwd_main(x["q"], x["k"], x["v"], x["dO"], B, S, nh, nkv, hd, scale, dk, dv,
-                             ws, ws_bytes, stream)
+                             ws, ws_bytes, st)
         if evs:
-            evs[3].record(stream)
-        xattn.xattn_bwd_dq_convert(B, S, nh, hd, scale, dq, ws, ws_bytes, stream)
+            evs[3].record(st)
+        xattn.xattn_bwd_dq_convert(B, S, nh, hd, scale, dq, ws, ws_bytes, st)
         if evs:
-            evs[4].record(stream)
+            evs[4].record(st)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -404,6 +410,30 @@ def run_ours(args, w: W.Workload):
     status = xattn.xattn_check_device_status(stream)
     if status != 0:
         raise RuntimeError(f"device status {status} during warm-up")
+
+    # --graph: the headline replays one CUDA graph of the step (the forward and the
+    # backward's calls, captured once after the eager warm-up), as a training loop may:
+    # the same kernels and programmatic-launch edges without the host launch path. It
+    # measured the same as the eager launches on every workload (the programmatic launches
+    # already overlap each kernel's set-up with its predecessor), so eager is the default.
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(graph, stream=cap):
+            step(st=cap)
+        torch.cuda.synchronize(dev)
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+        torch.cuda.synchronize(dev)
+
+    def timed_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
 
     # Two timed loops over the same steps. The headline takes one pair of events per
     # step, so consecutive kernels of a step follow each other directly in the stream (an
@@ -419,7 +449,7 @@ def run_ours(args, w: W.Workload):
         for i in range(args.steps):
             flush.zero_()
             step_events[i][0].record(stream)
-            step()
+            timed_step()
             step_events[i][1].record(stream)
         torch.cuda.synchronize(dev)
         barrier(pg)
@@ -455,6 +485,7 @@ def run_ours(args, w: W.Workload):
                                   + B * S * nh * 4 + elems * 4),
         "dq_convert_kernel": ("hbm", elems * 4 + elems * 2),
         "bwd_deterministic": ("tensor", w.bwd_flops),
+        "bwd_resident_dq": ("tensor", w.bwd_flops),
     }
     kernels = {}
     for n in names:
@@ -564,7 +595,10 @@ def run_ours(args, w: W.Workload):
             "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "S": w.S, "nh": w.nh, "nkv": w.nkv,
                        "hd": w.hd, "scale": scale,
-                       "backward": "deterministic dQ" if det else "default",
+                       "backward": ("deterministic, dQ resident in tensor memory" if mode == xattn.BWD_RESIDENT_DQ
+                                    else "deterministic dQ" if det else "default"),
+                       "launch": "eager stream launches" if graph is None else
+                                 "CUDA graph of the step, replayed (per-kernel times: eager launches)",
                        "parallelism": f"{world} rank(s), each its own batch of (batch, kv-head) units; no collective",
                        "l2": "flushed before every step (256 MiB device write, outside the timed events)"},
             "tok_per_s": tok_s,
@@ -573,7 +607,7 @@ def run_ours(args, w: W.Workload):
             "roofline": roofline, "kernels": kernels,
             "ms_per_step_with_kernel_events": statistics.mean(ev[0].elapsed_time(ev[len(names)]) for ev in events),
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 4 * args.steps, "clocks": clk.summary(),
+            "gpu_launches": (3 if mode == xattn.BWD_RESIDENT_DQ else 4) * args.steps, "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
     if pg is not None:

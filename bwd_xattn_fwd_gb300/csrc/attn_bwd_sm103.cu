@@ -192,7 +192,7 @@ struct BwdLayout {
   static constexpr uint32_t kAuxTileBytes = kTileRows * kAuxCols * 2;
   static constexpr uint32_t kAuxA = kFusedDq ? kdQs + 2 * kDqHalfBytes : kdS;
   static constexpr uint32_t kAuxB = kAuxA + 1024;                    // kQStages stages
-  static constexpr int kNumBars = 1 + 2 * (kQStages + kOStages) + (kFusedDq ? 14 : 11);
+  static constexpr int kNumBars = 1 + 2 * (kQStages + kOStages) + (kFusedDq ? 17 : 11);
   static constexpr uint32_t kBars = kAuxB + kQStages * kAuxTileBytes;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
@@ -236,14 +236,22 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
 // rewritten: S^T (s_free), dP^T (dp_free), P^T (p_free by the dS warps, dv_done by the
 // dV product), dQ (dq_empty) or dS^T (dk_done).
 // mdq (fused dQ only): fp32 map over the dQ accumulator.
-template <int HD, bool kFusedDq>
+//
+// kResident (with kFusedDq, small problems): a CTA takes every key tile of one (batch, kv
+// head) in turn, and the dQ tiles of the head's query rows stay in TMEM (columns
+// [448, 512): the head's group x num_m dQ tiles must fit, group * num_m * HD <= 64),
+// accumulated over the key tiles in a fixed order and written once, in bf16, after the
+// head's last key tile: no fp32 accumulator in global memory, no reduce-adds, no convert
+// pass, and dQ is reproducible. dq: the bf16 output (resident mode only).
+template <int HD, bool kFusedDq, bool kResident = false>
 __global__ void __maxnreg__(168)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
                          const __grid_constant__ CUtensorMap maux, const __grid_constant__ CUtensorMap mdq,
                          __nv_bfloat16 *__restrict__ dk,
-                         __nv_bfloat16 *__restrict__ dv, int B, int S, int nh, int nkv,
-                         float scale, int *status, unsigned long long timeout_ns) {
+                         __nv_bfloat16 *__restrict__ dv, __nv_bfloat16 *__restrict__ dq, int B, int S, int nh,
+                         int nkv, float scale, int *status, unsigned long long timeout_ns) {
+  static_assert(kFusedDq || !kResident, "the resident dQ is a fused-dQ mode");
   using L = BwdLayout<HD, kFusedDq>;
   constexpr int kQS = L::kQStages, kOS = L::kOStages;
   extern __shared__ uint8_t smem_raw[];
@@ -266,9 +274,13 @@ __global__ void __maxnreg__(168)
   const int BK = B * nkv;
   const int group = nh / nkv;
   const int num_units = num_m * BK;
-  const bool head_major = group == 1;
+  const bool head_major = kResident || group == 1;
   const int G = static_cast<int>(gridDim.x), cta = static_cast<int>(blockIdx.x);
-  auto unit_at = [&](int k) { return k * G + ((k & 1) ? G - 1 - cta : cta); };
+  // Resident dQ: CTA c takes heads c, c + G, ... and each head's key tiles in order.
+  auto unit_at = [&](int k) {
+    if constexpr (kResident) return (cta + G * (k / num_m)) * num_m + k % num_m;
+    return k * G + ((k & 1) ? G - 1 - cta : cta);
+  };
   int n = 0, b = 0, kvh = 0, per_head = 0, T = 0;
   auto set_unit = [&](int u) {
     const int bk = head_major ? u / num_m : u % BK;
@@ -306,6 +318,10 @@ __global__ void __maxnreg__(168)
   const uint32_t dk_done = bar(kB + 10);                              // dK(t) read dS^T(t)
   const uint32_t dq_full = bar(kB + 10), dq_empty = bar(kB + 11);     // fused dQ
   const uint32_t dqs_full = bar(kB + 12), dqs_empty = bar(kB + 13);
+  // Resident dQ: dS tile b's readers (dK and dQ of its iteration) are done (one phase per
+  // use of the tile), and the head's dQ tiles have been read out of TMEM.
+  auto ds_done = [&](int buf) { return bar(kB + 14 + buf); };
+  const uint32_t dqt_free = bar(kB + 16);
   uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
@@ -336,6 +352,9 @@ __global__ void __maxnreg__(168)
       mbar_init(dq_empty, 128);
       mbar_init(dqs_full, 128);
       mbar_init(dqs_empty, 1);
+      mbar_init(ds_done(0), 1);
+      mbar_init(ds_done(1), 1);
+      mbar_init(dqt_free, 128);
     } else {
       mbar_init(dk_done, 1);
     }
@@ -492,7 +511,7 @@ __global__ void __maxnreg__(168)
              (p_side || warp_wait(o_full(so), (u / kOS) & 1, ctl));
     };
     bool ok = true;
-    int units = 0;
+    int units = 0, heads = 0;
 #pragma unroll 1
     for (int k = 0, g = 0, sq = 0, so = 0; ok; ++k) {
       const int u = unit_at(k);
@@ -559,15 +578,31 @@ __global__ void __maxnreg__(168)
               mma_commit(q_empty(sq));               // dP^T and dK are done with the Q stage
             }
             __syncwarp();
-            if (!warp_wait(dq_empty, ph ^ 1, ctl)) { ok = false; break; }
-            tc_fence_after();
-            if (elect_one()) {
+            if constexpr (kResident) {
+              // dQ of query tile (r, m) += dS K_n, in its own TMEM columns; the head's first
+              // key tile (n = 0, which every query tile sees) overwrites. The head's first
+              // product waits for the previous head's dQ read-out.
+              if (n == 0 && t == 0 && !warp_wait(dqt_free, (heads - 1) & 1, ctl)) { ok = false; break; }
+              tc_fence_after();
+              const uint32_t col = static_cast<uint32_t>(((t / per_head) * num_m + n + t % per_head) * HD);
+              if (elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < kTileRows / 16; ++kk)                    // dQ = dS K
-                mma_ss(tdQ, kdS_mn + dsb + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
-              mma_commit(dq_full);
+                for (int kk = 0; kk < kTileRows / 16; ++kk)
+                  mma_ss(tdQ + col, kdS_mn + dsb + kk * 128, kK_mn + kk * kRowStep, idesc_dq, (n > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(ds_done(g & 1));            // dK and dQ are done with dS tile g % 2
+              }
+              __syncwarp();
+            } else {
+              if (!warp_wait(dq_empty, ph ^ 1, ctl)) { ok = false; break; }
+              tc_fence_after();
+              if (elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kTileRows / 16; ++kk)                  // dQ = dS K
+                  mma_ss(tdQ, kdS_mn + dsb + kk * 128, kK_mn + kk * kRowStep, idesc_dq, kk > 0);
+                mma_commit(dq_full);
+              }
+              __syncwarp();
             }
-            __syncwarp();
           } else {
             if (elect_one()) {
 #pragma unroll
@@ -591,9 +626,10 @@ __global__ void __maxnreg__(168)
       if (elect_one()) mma_commit(acc_done);
       __syncwarp();
       ++units;
+      if (n == num_m - 1) ++heads;            // resident dQ: the head's last key tile
     }
     if (units > 0) mbar_drain(acc_done, (units - 1) & 1, ctl);
-  } else if (kFusedDq && warp == 2) {
+  } else if (kFusedDq && !kResident && warp == 2) {
     // ---------------- dQ reducer ----------------
     // Both head-dim halves of a staged tile are issued before one wait for their reads.
     bool ok = true;
@@ -786,6 +822,15 @@ __global__ void __maxnreg__(168)
             }
             tc_fence_after();
           }
+          // Resident dQ (no per-iteration dQ drain): wait for dK and dQ of iteration g-2,
+          // the last readers of dS tile g % 2 (one phase of ds_done per use of the tile).
+          if (kResident && c == 0) {
+            if (!warp_wait(ds_done(g & 1), ((g >> 1) & 1) ^ 1, ctl)) {
+              tmem_wait_ld();
+              ok = false;
+              break;
+            }
+          }
           uint32_t dsk[16];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
@@ -821,7 +866,7 @@ __global__ void __maxnreg__(168)
         if constexpr (kFusedDq) {
           fence_proxy_async_smem();
           mbar_arrive(ds_full);
-          if (t > 0 && !drain_dq(g - 1)) { ok = false; break; }
+          if (!kResident && t > 0 && !drain_dq(g - 1)) { ok = false; break; }
         } else {
           tmem_wait_st();
           tc_fence_before();
@@ -831,7 +876,7 @@ __global__ void __maxnreg__(168)
       if (!ok) break;
       // Epilogue: the unit's last dQ (fused), then the dK rows (bf16, times the softmax
       // scale); the dK columns are then free for the next unit.
-      if constexpr (kFusedDq) {
+      if constexpr (kFusedDq && !kResident) {
         if (!drain_dq(g - 1)) break;
       }
       if (!warp_wait(acc_done, units & 1, ctl)) break;
@@ -858,6 +903,42 @@ __global__ void __maxnreg__(168)
       tc_fence_before();
       mbar_arrive(acc_free);
       ++units;
+      if constexpr (kResident) {
+        if (n == num_m - 1) {
+          // The head's dQ tiles are complete after its last key tile (acc_done covers
+          // every dQ product): dq = bf16(scale * accumulator), query row j of each tile.
+#pragma unroll 1
+          for (int r = 0; r < group; ++r) {
+#pragma unroll 1
+            for (int m = 0; m < num_m; ++m) {
+              const uint32_t col = static_cast<uint32_t>((r * num_m + m) * HD);
+              const int i = m * kTileRows + j;
+              __nv_bfloat16 *qrow =
+                  dq + ((static_cast<size_t>(b) * S + i) * nh + static_cast<size_t>(kvh) * group + r) * HD;
+#pragma unroll
+              for (int c = 0; c < HD; c += 16) {
+                uint32_t v[16];
+                tmem_ld_x16(tdQ + lane_off + col + c, v);
+                tmem_wait_ld();
+                reg_fence<16>(v);
+                if (i < S) {
+                  float f[16];
+#pragma unroll
+                  for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(v[e]) * scale;
+                  uint4 *dst = reinterpret_cast<uint4 *>(qrow + c);
+#pragma unroll
+                  for (int e = 0; e < 2; ++e)
+                    dst[e] = make_uint4(pack_bf16x2(f[8 * e], f[8 * e + 1]), pack_bf16x2(f[8 * e + 2], f[8 * e + 3]),
+                                        pack_bf16x2(f[8 * e + 4], f[8 * e + 5]),
+                                        pack_bf16x2(f[8 * e + 6], f[8 * e + 7]));
+                }
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(dqt_free);
+        }
+      }
     }
   }
 
@@ -869,23 +950,24 @@ __global__ void __maxnreg__(168)
   }
 }
 
-template <int HD, bool kFusedDq>
+template <int HD, bool kFusedDq, bool kResident = false>
 cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const CUtensorMap &mdo, const CUtensorMap &maux, const CUtensorMap &mdq,
-                           __nv_bfloat16 *dk, __nv_bfloat16 *dv, int B, int S, int nh, int nkv,
-                           float scale, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+                           __nv_bfloat16 *dk, __nv_bfloat16 *dv, __nv_bfloat16 *dq, int B, int S, int nh,
+                           int nkv, float scale, int *status, uint64_t timeout_ns, cudaStream_t stream) {
   using L = BwdLayout<HD, kFusedDq>;
-  cudaError_t err = cudaFuncSetAttribute(attn_bwd_main_kernel<HD, kFusedDq>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
+  auto kernel = attn_bwd_main_kernel<HD, kFusedDq, kResident>;
+  cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
   if (err != cudaSuccess) return err;
-  // Persistent CTAs: one per SM, or one per unit when there are fewer units.
+  // Persistent CTAs: one per SM, or one per unit (resident dQ: per head) when there are
+  // fewer.
   int dev = 0, sms = 0;
   if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
   if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
-  const long long units = static_cast<long long>(B) * nkv * ((S + kTileRows - 1) / kTileRows);
+  const long long units = static_cast<long long>(B) * nkv * (kResident ? 1 : (S + kTileRows - 1) / kTileRows);
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  return launch_pdl(attn_bwd_main_kernel<HD, kFusedDq>, grid, kBwdThreads, L::kDynBytes, stream, mq, mk, mv,
-                    mdo, maux, mdq, dk, dv, B, S, nh, nkv, scale, status, timeout_ns);
+  return launch_pdl(kernel, grid, kBwdThreads, L::kDynBytes, stream, mq, mk, mv, mdo, maux, mdq, dk, dv, dq, B, S,
+                    nh, nkv, scale, status, timeout_ns);
 }
 
 // 3. dq convert (fused dQ): 8 elements per thread (two 16-byte loads, one 16-byte
@@ -941,14 +1023,33 @@ cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
   // is then unused (maux stands in for it).
   const CUtensorMap &md = mdq ? *mdq : maux;
   if (hd == 64)
-    return mdq ? launch_main_hd<64, true>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream)
-               : launch_main_hd<64, false>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return mdq ? launch_main_hd<64, true>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale, status, timeout_ns, stream)
+               : launch_main_hd<64, false>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale, status, timeout_ns, stream);
   if (hd == 32)
-    return mdq ? launch_main_hd<32, true>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream)
-               : launch_main_hd<32, false>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return mdq ? launch_main_hd<32, true>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale, status, timeout_ns, stream)
+               : launch_main_hd<32, false>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale, status, timeout_ns, stream);
   if (hd == 128 && !mdq)
-    return launch_main_hd<128, false>(mq, mk, mv, mdo, maux, md, dk, dv, B, S, nh, nkv, scale, status, timeout_ns, stream);
+    return launch_main_hd<128, false>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale, status, timeout_ns, stream);
   return cudaErrorInvalidValue;
+}
+
+bool bwd_resident_dq_ok(int S, int nh, int nkv, int hd) {
+  const int num_m = (S + kTileRows - 1) / kTileRows;
+  return (hd == 32 || hd == 64) && static_cast<long long>(nh / nkv) * num_m * hd <= 64;
+}
+
+cudaError_t launch_bwd_main_resident_bf16(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                                          const CUtensorMap &mdo, const CUtensorMap &maux, __nv_bfloat16 *dk,
+                                          __nv_bfloat16 *dv, __nv_bfloat16 *dq, int B, int S, int nh, int nkv,
+                                          int hd, float scale, int *status, uint64_t timeout_ns,
+                                          cudaStream_t stream) {
+  if (!bwd_resident_dq_ok(S, nh, nkv, hd)) return cudaErrorInvalidValue;
+  // The resident kernel reads no dQ accumulator map; maux stands in for it.
+  if (hd == 64)
+    return launch_main_hd<64, true, true>(mq, mk, mv, mdo, maux, maux, dk, dv, dq, B, S, nh, nkv, scale, status,
+                                          timeout_ns, stream);
+  return launch_main_hd<32, true, true>(mq, mk, mv, mdo, maux, maux, dk, dv, dq, B, S, nh, nkv, scale, status,
+                                        timeout_ns, stream);
 }
 
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, size_t n_elems,

@@ -222,6 +222,13 @@ xattn_status xattn_fwd(const void *q, const void *k, const void *v, int B, int S
                                      static_cast<cudaStream_t>(stream)));
 }
 
+int xattn_bwd_dq_mode(int S, int nh, int nkv, int hd, int deterministic) {
+  if (S <= 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0) return -1;
+  if (hd != 32 && hd != 64 && hd != 128) return -1;
+  if (!deterministic && hd != 128) return XATTN_BWD_FUSED_DQ;
+  return bwd_resident_dq_ok(S, nh, nkv, hd) ? XATTN_BWD_RESIDENT_DQ : XATTN_BWD_QUERY_DQ;
+}
+
 size_t xattn_bwd_workspace_bytes(int B, int S, int nh, int hd) {
   if (B <= 0 || S <= 0 || nh <= 0 || hd <= 0) return 0;
   return bwd_workspace_bytes(B, S, nh, hd, true);
@@ -368,13 +375,20 @@ xattn_status xattn_bwd_deterministic(const void *q, const void *k, const void *v
     r = cuda_status(launch_bwd_preprocess(static_cast<const __nv_bfloat16 *>(o),
                                           static_cast<const __nv_bfloat16 *>(dO), lse, B, S, nh, hd,
                                           scale, ws, false, st));
-  if (r == XATTN_OK)
-    r = cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, maux, nullptr, static_cast<__nv_bfloat16 *>(dk),
-                                         static_cast<__nv_bfloat16 *>(dv), B, S, nh, nkv, hd, scale,
-                                         dev->status, wait_limit_ns(), st));
-  if (r == XATTN_OK)
-    r = cuda_status(launch_bwd_dq_bf16(mq, mk, mv, mdo, lse, ws, static_cast<__nv_bfloat16 *>(dq), B, S,
-                                       nh, nkv, hd, scale, dev->status, wait_limit_ns(), st));
+  if (r == XATTN_OK && bwd_resident_dq_ok(S, nh, nkv, hd)) {
+    // Small problems: one kernel, dQ resident in TMEM over each head's key tiles.
+    r = cuda_status(launch_bwd_main_resident_bf16(mq, mk, mv, mdo, maux, static_cast<__nv_bfloat16 *>(dk),
+                                                  static_cast<__nv_bfloat16 *>(dv), static_cast<__nv_bfloat16 *>(dq),
+                                                  B, S, nh, nkv, hd, scale, dev->status, wait_limit_ns(), st));
+  } else {
+    if (r == XATTN_OK)
+      r = cuda_status(launch_bwd_main_bf16(mq, mk, mv, mdo, maux, nullptr, static_cast<__nv_bfloat16 *>(dk),
+                                           static_cast<__nv_bfloat16 *>(dv), B, S, nh, nkv, hd, scale,
+                                           dev->status, wait_limit_ns(), st));
+    if (r == XATTN_OK)
+      r = cuda_status(launch_bwd_dq_bf16(mq, mk, mv, mdo, lse, ws, static_cast<__nv_bfloat16 *>(dq), B, S,
+                                         nh, nkv, hd, scale, dev->status, wait_limit_ns(), st));
+  }
   const cudaError_t fe = cudaFreeAsync(base, st);
   if (r == XATTN_OK && fe != cudaSuccess) r = XATTN_ERR_CUDA;
   return r;

@@ -75,6 +75,17 @@ cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
                                  int B, int S, int nh, int nkv, int hd, float scale, int *status,
                                  uint64_t timeout_ns, cudaStream_t stream);
 
+// Small problems: the backward with dQ resident in tensor memory (one CTA per (batch, kv
+// head), all its key tiles; dQ accumulated over them in a fixed order and written once in
+// bf16). Needs the workspace of the preprocess without the dQ accumulator. Usable when
+// bwd_resident_dq_ok(S, nh, nkv, hd): hd in {32, 64} and group * ceil(S / 128) * hd <= 64.
+bool bwd_resident_dq_ok(int S, int nh, int nkv, int hd);
+cudaError_t launch_bwd_main_resident_bf16(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                                          const CUtensorMap &mdo, const CUtensorMap &maux, __nv_bfloat16 *dk,
+                                          __nv_bfloat16 *dv, __nv_bfloat16 *dq, int B, int S, int nh, int nkv,
+                                          int hd, float scale, int *status, uint64_t timeout_ns,
+                                          cudaStream_t stream);
+
 cudaError_t launch_dq_convert(const float *dqacc, __nv_bfloat16 *dq, size_t n_elems,
                               float scale, cudaStream_t stream);
 

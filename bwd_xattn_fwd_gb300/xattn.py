@@ -77,6 +77,10 @@ _lib.xattn_status_string.argtypes = [ctypes.c_int]
 _lib.xattn_status_string.restype = ctypes.c_char_p
 _lib.xattn_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i]
 _lib.xattn_bwd_workspace_bytes.restype = ctypes.c_size_t
+_lib.xattn_bwd_dq_mode.argtypes = [_i, _i, _i, _i, _i]
+_lib.xattn_bwd_dq_mode.restype = ctypes.c_int
+
+BWD_FUSED_DQ, BWD_RESIDENT_DQ, BWD_QUERY_DQ = 0, 1, 2
 
 
 def lib_path() -> str:
@@ -141,6 +145,12 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # XATTN_NOALLOC_SCRATCH_BYTES in xatt
 
 def xattn_bwd_workspace_bytes(B, S, nh, hd) -> int:
     return int(_lib.xattn_bwd_workspace_bytes(B, S, nh, hd))
+
+
+def xattn_bwd_dq_mode(S, nh, nkv, hd, deterministic=False) -> int:
+    """Which backward xattn_bwd (or, with deterministic, xattn_bwd_deterministic) runs for
+    these sizes (BWD_FUSED_DQ, BWD_RESIDENT_DQ, BWD_QUERY_DQ), or -1 for sizes it rejects."""
+    return int(_lib.xattn_bwd_dq_mode(S, nh, nkv, hd, int(bool(deterministic))))
 
 
 def xattn_bwd_preprocess(o, dO, lse, B, S, nh, hd, scale, workspace, workspace_bytes, stream=None):

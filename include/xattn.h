@@ -99,6 +99,27 @@ xattn_status xattn_bwd(const void *q, const void *k, const void *v, const void *
                        int hd, float scale, void *dq, void *dk, void *dv, void *stream);
 
 /*
+ * Which backward xattn_bwd (deterministic == 0) or xattn_bwd_deterministic
+ * (deterministic != 0) runs for these sizes; no device work, -1 for sizes they reject:
+ *   XATTN_BWD_FUSED_DQ      xattn_bwd at hd 32 / 64: dK/dV key-stationary; dQ added across
+ *                           key tiles into an fp32 accumulator with reduce-adds, then
+ *                           converted (the three stage calls below); dQ's last bits may vary
+ *                           from run to run.
+ *   XATTN_BWD_RESIDENT_DQ   xattn_bwd_deterministic on small problems (group * ceil(S / 128)
+ *                           * hd <= 64, hd 32 or 64): one CTA per (batch, kv head) takes all
+ *                           its key tiles and keeps the head's dQ tiles in tensor memory,
+ *                           summed in a fixed order and written once (one kernel after the
+ *                           preprocess).
+ *   XATTN_BWD_QUERY_DQ      otherwise deterministic (and xattn_bwd at hd 128): dQ from a
+ *                           query-stationary recompute.
+ * The last two give every output bit-for-bit the same from run to run.
+ */
+#define XATTN_BWD_FUSED_DQ 0
+#define XATTN_BWD_RESIDENT_DQ 1
+#define XATTN_BWD_QUERY_DQ 2
+int xattn_bwd_dq_mode(int S, int nh, int nkv, int hd, int deterministic);
+
+/*
  * The backward's three steps with a caller-owned workspace, for callers that manage
  * memory themselves (or capture the call in a CUDA graph). xattn_bwd is exactly
  * workspace allocation + these three calls + release.

@@ -180,3 +180,20 @@ def test_selftest_limit_checks(lib):
     f.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
     assert f(0, None) == 2
     assert f(20 * 10**9, None) == 2
+
+
+def test_bwd_dq_mode(lib):
+    """The backward that xattn_bwd / xattn_bwd_deterministic pick, by sizes: xattn_bwd runs
+    the fused-dQ backward at hd 32 and 64 and the query-stationary one at hd 128; the
+    deterministic backward keeps dQ in tensor memory when a head's dQ tiles fit its 64
+    free columns, else it runs the query-stationary dQ."""
+    f = lib.xattn_bwd_dq_mode
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 5
+    assert f(256, 12, 12, 32, 0) == 0 and f(2048, 8, 2, 64, 0) == 0 and f(4096, 16, 4, 128, 0) == 2
+    assert f(256, 12, 12, 32, 1) == 1         # one head, two query tiles at hd 32
+    assert f(128, 4, 2, 32, 1) == 1           # group 2, one tile
+    assert f(129, 4, 2, 32, 1) == 2           # group 2, two tiles: 128 columns
+    assert f(128, 2, 2, 64, 1) == 1 and f(129, 2, 2, 64, 1) == 2
+    assert f(2048, 8, 2, 64, 1) == 2 and f(4096, 16, 4, 128, 1) == 2
+    assert f(256, 6, 4, 32, 0) == -1 and f(0, 2, 2, 32, 1) == -1 and f(256, 2, 2, 48, 0) == -1

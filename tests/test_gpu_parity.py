@@ -215,3 +215,54 @@ def test_right_padded_ragged_batch():
         ref = oracle_full(wb, xb)
         got = {n: out[n][b:b + 1, :L] for n in out}
         compare(got, ref, "bf16", f"sequence {b} (length {L})")
+
+
+# ---- small problems: the deterministic backward with dQ resident in TMEM (one CTA per
+# (batch, kv head) over all its key tiles; taken when group * ceil(S / 128) * hd <= 64) ----
+RESIDENT = [
+    # (B, S, nh, nkv, hd): S = 1; one tile at hd 64; two query tiles at hd 32; a query
+    # group of 2 in one tile; partial second tile; more heads than SMs (a CTA takes two)
+    (1, 1, 2, 2, 64),
+    (2, 77, 6, 6, 64),
+    (3, 200, 4, 4, 32),
+    (2, 100, 4, 2, 32),
+    (1, 130, 2, 2, 32),
+    (160, 100, 2, 1, 32),
+]
+
+
+@pytest.mark.parametrize("shape", RESIDENT, ids=lambda s: "B%d_S%d_nh%d_nkv%d_hd%d" % s)
+def test_resident_dq_shapes(shape):
+    from bwd_xattn_fwd_gb300 import xattn
+    B, S, nh, nkv, hd = shape
+    assert xattn.xattn_bwd_dq_mode(S, nh, nkv, hd, True) == xattn.BWD_RESIDENT_DQ
+    w = W.Workload("res", B, S, nh, nkv, hd, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=21)
+    compare(run_gpu(w, x, deterministic=True), oracle_full(w, x), "bf16", "resident " + str(shape))
+
+
+@pytest.mark.parametrize("scale", [0.0, -0.3], ids=lambda s: "scale=%g" % s)
+def test_resident_dq_scales(scale):
+    w = W.Workload("res", 2, 256, 4, 4, 32, "bf16", qkv_scale=0.5)
+    x = W.make_inputs(w, seed=22)
+    compare(run_gpu(w, x, scale=scale, deterministic=True), oracle_full(w, x, scale=scale), "bf16",
+            "resident scale=%g" % scale)
+
+
+def test_resident_dq_workload_and_reproducible():
+    """The dim384 workload (16 x 256 x 12 heads, hd 32) through the deterministic backward,
+    which keeps dQ resident in TMEM there: every (batch, head) unit against the oracle,
+    every output bit-identical run to run, and dK, dV bit-identical to the default
+    backward's (the same key-stationary products in the same order)."""
+    w = W.WORKLOADS["dim384"]
+    x = W.make_inputs(w)
+    a, b = run_gpu(w, x, deterministic=True), run_gpu(w, x, deterministic=True)
+    ref = oracle_full(w, x)
+    compare(a, ref, "bf16", "dim384 resident")
+    compare_every_unit(w, a, ref, "dim384 resident")
+    for name in ("o", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(a[name], b[name]), name
+    c = run_gpu(w, x)
+    for name in ("o", "lse", "dk", "dv"):
+        assert np.array_equal(a[name], c[name]), name
+    assert np.abs(a["dq"] - c["dq"]).max() <= TOL_BF16 * np.abs(c["dq"]).max()
