@@ -175,24 +175,27 @@ struct BwdLayout {
   static constexpr uint32_t kV = kK + kTileBytes;
   static constexpr uint32_t kQ = kV + kTileBytes;                    // kQStages stages
   static constexpr uint32_t kdO = kQ + kQStages * kTileBytes;        // kOStages stages
-  // Fused dQ only: two 128 x 128 bf16 dS tiles (32 KB each; iteration t uses tile t % 2,
-  // so dS(t+1) is written while dK(t) and dQ(t) still read dS(t)) and the dQ staging for
-  // the TMA reduce-add (2 head-dim halves x 128 rows of HD/2 floats, swizzled like the
-  // tensor map's box).
+  // Fused dQ only: three 128 x 128 bf16 dS tiles (32 KB each; iteration t uses tile
+  // t % 3, so dS(t+1) is written while dK(t) and dQ(t) still read dS(t)). Once dK(t) and
+  // dQ(t) are done the tile stages dQ(t) for the TMA reduce-add (fp32, 2 head-dim halves x
+  // 128 rows of HD/2 floats, swizzled like the tensor map's box): the dQ drain never waits
+  // for an earlier reduce-add, and dS(t+3) waits for the reduce-add of dQ(t) to have read
+  // the tile, two iterations later. The resident dQ uses tiles t % 2 only.
   static constexpr uint32_t kdS = kdO + kOStages * kTileBytes;
   static constexpr uint32_t kdSBytes = 32768;
+  static constexpr int kdSTiles = 3;
   static constexpr uint32_t kDqRowBytes = HD / 2 * 4;
   static constexpr uint32_t kDqHalfBytes = kTileRows * kDqRowBytes;
-  static constexpr uint32_t kdQs = kdS + 2 * kdSBytes;
+  static_assert(!kFusedDq || 2 * kDqHalfBytes <= kdSBytes, "a dQ tile is staged in a dS tile");
   // Auxiliary K step of S^T and dP^T: the key-side operand is constant (ones under the
   // LSE columns, or under the D columns, of every row), so it is three 8-row x 16-byte
   // core matrices read without swizzle and with a zero row-group stride: [1 1 1 0 ...],
   // [0 0 0 1 1 1 0 0] and zeros. The query-side rows (128 x 16 bf16, 32-byte swizzle,
   // 4 KB) come with each stage.
   static constexpr uint32_t kAuxTileBytes = kTileRows * kAuxCols * 2;
-  static constexpr uint32_t kAuxA = kFusedDq ? kdQs + 2 * kDqHalfBytes : kdS;
+  static constexpr uint32_t kAuxA = kFusedDq ? kdS + kdSTiles * kdSBytes : kdS;
   static constexpr uint32_t kAuxB = kAuxA + 1024;                    // kQStages stages
-  static constexpr int kNumBars = 1 + 2 * (kQStages + kOStages) + (kFusedDq ? 17 : 11);
+  static constexpr int kNumBars = 1 + 2 * (kQStages + kOStages) + (kFusedDq ? 21 : 11);
   static constexpr uint32_t kBars = kAuxB + kQStages * kAuxTileBytes;
   static constexpr uint32_t kMisc = kBars + 8 * kNumBars;
   static constexpr uint32_t kUsed = kMisc + 32;
@@ -297,7 +300,6 @@ __global__ void __maxnreg__(168)
   const uint32_t sdO = smem_u32(smem + L::kdO);
   uint8_t *sdS_ptr = smem + L::kdS;          // fused dQ only
   const uint32_t sdS = smem_u32(sdS_ptr);
-  uint8_t *sdQs_ptr = smem + L::kdQs;
   const uint32_t sAuxA = smem_u32(smem + L::kAuxA);
   const uint32_t sAuxB = smem_u32(smem + L::kAuxB);
   // scale == 0: S^T is the auxiliary term alone (-LSE log2 e) and is not scaled.
@@ -317,7 +319,11 @@ __global__ void __maxnreg__(168)
   const uint32_t acc_free = bar(kB + 9);     // its epilogue has read dV and dK
   const uint32_t dk_done = bar(kB + 10);                              // dK(t) read dS^T(t)
   const uint32_t dq_full = bar(kB + 10), dq_empty = bar(kB + 11);     // fused dQ
-  const uint32_t dqs_full = bar(kB + 12), dqs_empty = bar(kB + 13);
+  // dQ staged in dS tile t % 3 / that tile read by its reduce-add: one phase of each per
+  // use of the tile. (One dqs_full for all tiles would be ambiguous: the drain no longer
+  // waits for the previous reduce-add, so it can run two phases ahead of the reducer.)
+  auto dqs_full = [&](int tile) { return bar(tile == 0 ? kB + 12 : kB + 18 + tile); };
+  auto dqs_empty = [&](int tile) { return bar(tile == 0 ? kB + 13 : kB + 16 + tile); };
   // Resident dQ: dS tile b's readers (dK and dQ of its iteration) are done (one phase per
   // use of the tile), and the head's dQ tiles have been read out of TMEM.
   auto ds_done = [&](int buf) { return bar(kB + 14 + buf); };
@@ -350,8 +356,10 @@ __global__ void __maxnreg__(168)
     if constexpr (kFusedDq) {
       mbar_init(dq_full, 1);
       mbar_init(dq_empty, 128);
-      mbar_init(dqs_full, 128);
-      mbar_init(dqs_empty, 1);
+      for (int i = 0; i < L::kdSTiles; ++i) {
+        mbar_init(dqs_full(i), 128);
+        mbar_init(dqs_empty(i), 1);
+      }
       mbar_init(ds_done(0), 1);
       mbar_init(ds_done(1), 1);
       mbar_init(dqt_free, 128);
@@ -569,7 +577,7 @@ __global__ void __maxnreg__(168)
           if (!warp_wait(ds_full, ph, ctl)) { ok = false; break; }
           tc_fence_after();
           if constexpr (kFusedDq) {
-            const uint32_t dsb = (g & 1) * (L::kdSBytes >> 4);               // dS tile g % 2
+            const uint32_t dsb = (kResident ? (g & 1) : (g % L::kdSTiles)) * (L::kdSBytes >> 4);  // dS tile
             if (elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < kTileRows / 16; ++kk)                    // dK += dS^T Q
@@ -640,15 +648,15 @@ __global__ void __maxnreg__(168)
       set_unit(u);
 #pragma unroll 1
       for (int t = 0; t < T; ++t, ++g) {
-        if (!warp_wait(dqs_full, g & 1, ctl)) { ok = false; break; }
+        if (!warp_wait(dqs_full(g % L::kdSTiles), (g / L::kdSTiles) & 1, ctl)) { ok = false; break; }
         if (lane == 0) {
           const int h = kvh * group + t / per_head, m = n + t % per_head;
-          const uint32_t src = smem_u32(sdQs_ptr);
+          const uint32_t src = smem_u32(sdS_ptr + (g % L::kdSTiles) * L::kdSBytes);
           tma_reduce_add_4d(&mdq, src, 0, h, m * kTileRows, b);
           tma_reduce_add_4d(&mdq, src + L::kDqHalfBytes, HD / 2, h, m * kTileRows, b);
           bulk_commit_group();
-          bulk_wait_read_all();        // the staging buffer may be rewritten
-          mbar_arrive(dqs_empty);
+          bulk_wait_read_all();        // the tile may take the next dS
+          mbar_arrive(dqs_empty(g % L::kdSTiles));
         }
         __syncwarp();
       }
@@ -756,10 +764,11 @@ __global__ void __maxnreg__(168)
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    // Fused dQ: dQ(k) from TMEM (query row j of its tile) into the staging buffer,
-    // swizzled like the reduce's tensor-map box (two halves of HD/2 floats per row); warp
-    // 2 then adds it to global memory. The phases of dq_full are waited in order, one per
-    // call: dQ(k+1) is only issued after this call has read dQ(k) (dq_empty).
+    // Fused dQ: dQ(k) from TMEM (query row j of its tile) into dS tile k % 3 (dK(k) and
+    // dQ(k), its last readers, are done once dq_full shows dQ(k)), swizzled like the
+    // reduce's tensor-map box (two halves of HD/2 floats per row); warp 2 then adds it to
+    // global memory. The phases of dq_full are waited in order, one per call: dQ(k+1) is
+    // only issued after this call has read dQ(k) (dq_empty).
     auto drain_dq = [&](int k) -> bool {
       if (!warp_wait(dq_full, k & 1, ctl)) return false;
       tc_fence_after();
@@ -770,10 +779,9 @@ __global__ void __maxnreg__(168)
       reg_fence<HD>(v);
       tc_fence_before();
       mbar_arrive(dq_empty);
-      if (!warp_wait(dqs_empty, (k & 1) ^ 1, ctl)) return false;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint8_t *row = sdQs_ptr + half * L::kDqHalfBytes + j * L::kDqRowBytes;
+        uint8_t *row = sdS_ptr + (k % L::kdSTiles) * L::kdSBytes + half * L::kDqHalfBytes + j * L::kDqRowBytes;
 #pragma unroll
         for (int ch = 0; ch < HD / 8; ++ch) {
           const int sw = (HD == 64) ? (ch ^ (j & 7)) : (ch ^ ((j >> 1) & 3));
@@ -782,7 +790,7 @@ __global__ void __maxnreg__(168)
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(dqs_full);
+      mbar_arrive(dqs_full(k % L::kdSTiles));
       return true;
     };
     bool ok = true;
@@ -810,10 +818,8 @@ __global__ void __maxnreg__(168)
             tmem_ld_x16(tP + lane_off + 16 * (c + 1), pn);
             tmem_ld_x32(tdP + lane_off + 32 * (c + 1), dn);
           }
-          // The dS^T buffer about to be written has been read. Fused dQ: tile g % 2 was last
-          // read by dK and dQ of iteration g-2, which completed before the drain of that dQ
-          // (in iteration g-1, or in the epilogue of the previous unit). Otherwise the
-          // previous dK read dS^T from TMEM.
+          // The dS^T buffer about to be written has been read. Without fused dQ the previous
+          // dK read dS^T from TMEM (dk_done); the fused cases follow below.
           if (!kFusedDq && c == 0) {
             if (!warp_wait(dk_done, (g - 1) & 1, ctl)) {
               tmem_wait_ld();    // the loads of chunk 1 are still in flight
@@ -826,6 +832,16 @@ __global__ void __maxnreg__(168)
           // the last readers of dS tile g % 2 (one phase of ds_done per use of the tile).
           if (kResident && c == 0) {
             if (!warp_wait(ds_done(g & 1), ((g >> 1) & 1) ^ 1, ctl)) {
+              tmem_wait_ld();
+              ok = false;
+              break;
+            }
+          }
+          // Fused dQ: tile g % 3 last staged dQ(g-3); its reduce-add has read it (one phase
+          // of dqs_empty per use of the tile). dK(g-3) and dQ(g-3) were done before that
+          // dQ was drained.
+          if (kFusedDq && !kResident && c == 0) {
+            if (!warp_wait(dqs_empty(g % L::kdSTiles), ((g / L::kdSTiles) & 1) ^ 1, ctl)) {
               tmem_wait_ld();
               ok = false;
               break;
@@ -846,7 +862,8 @@ __global__ void __maxnreg__(168)
           if constexpr (kFusedDq) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<uint4 *>(sdS_ptr + (g & 1) * L::kdSBytes + ds_offset(j, 32 * c + 8 * e)) =
+              *reinterpret_cast<uint4 *>(sdS_ptr + (kResident ? (g & 1) : (g % L::kdSTiles)) * L::kdSBytes +
+                                         ds_offset(j, 32 * c + 8 * e)) =
                   make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
           } else {
             tmem_st_x16(tdS + lane_off + 16 * c, dsk);
