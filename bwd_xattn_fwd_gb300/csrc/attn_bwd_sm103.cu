@@ -246,7 +246,9 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
 // accumulated over the key tiles in a fixed order and written once, in bf16, after the
 // head's last key tile: no fp32 accumulator in global memory, no reduce-adds, no convert
 // pass, and dQ is reproducible. dq: the bf16 output (resident mode only).
-template <int HD, bool kFusedDq, bool kResident = false>
+//
+// kDsTmem (fused dQ, not resident): dK reads dS^T from TMEM (see below).
+template <int HD, bool kFusedDq, bool kResident = false, bool kDsTmem = false>
 __global__ void __maxnreg__(168)
     attn_bwd_main_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                          const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
@@ -257,6 +259,15 @@ __global__ void __maxnreg__(168)
   static_assert(kFusedDq || !kResident, "the resident dQ is a fused-dQ mode");
   using L = BwdLayout<HD, kFusedDq>;
   constexpr int kQS = L::kQStages, kOS = L::kOStages;
+  // kDsTmem (fused dQ, not resident): the dS warps also write dS^T in bf16 over the
+  // first 64 columns of dP^T (which they have read by then), and dK reads its A operand
+  // there instead of from the shared-memory dS tile (32 KB less shared-memory traffic per
+  // iteration; only dQ reads the tile). The next dP^T overwrites those columns, so the
+  // dS side issues it after dK (its MMAs execute in issue order) instead of as soon as
+  // the dS warps have read dP^T: worth it on long units (query groups; measured on gqa
+  // 92.4 -> 89.9 us, long 314 -> 307 us), not on the short units of one query head per
+  // kv head (32 x 1024 x 12 heads: 193.8 -> 196.6 us).
+  static_assert(!kDsTmem || (kFusedDq && !kResident), "dS^T in TMEM is a fused-dQ mode");
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -401,7 +412,8 @@ __global__ void __maxnreg__(168)
   // in its first 64 | dV [256,384) | dK [384,512).
   const uint32_t tS = tmem, tdP = tmem + 128, tP = L::kAlias ? tS : tmem + 256;
   const uint32_t tdV = tmem + (L::kAlias ? 256 : 320), tdK = tmem + 384;
-  const uint32_t tdQ = tmem + 448, tdS = L::kAlias ? tdP : tmem + 448;   // fused dQ: dQ; otherwise dS^T
+  const uint32_t tdQ = tmem + 448;                                       // fused dQ: dQ
+  const uint32_t tdS = (L::kAlias || kDsTmem) ? tdP : tmem + 448;        // dS^T (bf16)
   // One 128-row tile of a [B, S, heads, hd] tensor: one TMA box per 64-column sub-tile.
   auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int head, int row0, int bb) {
 #pragma unroll
@@ -527,8 +539,10 @@ __global__ void __maxnreg__(168)
       set_unit(u);
       // The unit's first score product: K and V have landed, and this side's warps have
       // read the previous score tile (the last one of the previous unit).
+      // kDsTmem, dS side: the previous dP^T columns hold the last dS^T, which this warp's
+      // own dK (issued before) reads first; the dS warps had read that dP^T before ds_full.
       ok = warp_wait(kv_full, units & 1, ctl) && wait_operands(g, sq, so) &&
-           warp_wait(t_free, (g - 1) & 1, ctl);
+           ((kDsTmem && !p_side) || warp_wait(t_free, (g - 1) & 1, ctl));
       // With P^T over S^T, S^T overwrites the previous P^T: the dS warps have read it.
       if (L::kAlias && p_side) ok = ok && warp_wait(p_free, (g - 1) & 1, ctl);
       if (!ok) break;
@@ -550,13 +564,14 @@ __global__ void __maxnreg__(168)
         // side, once the dS warps have read P^T.
         auto issue_next = [&]() -> bool {
           if (!more) return true;
-          if (!wait_operands(g + 1, sq1, so1) || !warp_wait(t_free, ph, ctl)) return false;
+          if (!wait_operands(g + 1, sq1, so1) || (!(kDsTmem && !p_side) && !warp_wait(t_free, ph, ctl)))
+            return false;
           if (L::kAlias && p_side && !warp_wait(p_free, ph, ctl)) return false;
           tc_fence_after();
           issue_t(sq1, so1);
           return true;
         };
-        if (!L::kAlias && !issue_next()) { ok = false; break; }
+        if (!L::kAlias && !(kDsTmem && !p_side) && !issue_next()) { ok = false; break; }
         if (p_side) {
           if (!warp_wait(o_full(so), (g / kOS) & 1, ctl) || !warp_wait(p_full, ph, ctl)) { ok = false; break; }
           tc_fence_after();
@@ -580,12 +595,19 @@ __global__ void __maxnreg__(168)
             const uint32_t dsb = (kResident ? (g & 1) : (g % L::kdSTiles)) * (L::kdSBytes >> 4);  // dS tile
             if (elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < kTileRows / 16; ++kk)                    // dK += dS^T Q
-                mma_ss(tdK, kdS_k + dsb + (kk >> 2) * 1024 + (kk & 3) * 2,
-                       kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kTileRows / 16; ++kk) {                  // dK += dS^T Q
+                if constexpr (kDsTmem)
+                  mma_ts(tdK, tdS + kk * 8, kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc,
+                         (t > 0 || kk > 0) ? 1u : 0u);
+                else
+                  mma_ss(tdK, kdS_k + dsb + (kk >> 2) * 1024 + (kk & 3) * 2,
+                         kQ_mn + sq * kStageDesc + kk * kRowStep, idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+              }
               mma_commit(q_empty(sq));               // dP^T and dK are done with the Q stage
             }
             __syncwarp();
+            // kDsTmem: the next dP^T, over this dS^T, after dK in issue order.
+            if (kDsTmem && !issue_next()) { ok = false; break; }
             if constexpr (kResident) {
               // dQ of query tile (r, m) += dS K_n, in its own TMEM columns; the head's first
               // key tile (n = 0, which every query tile sees) overwrites. The head's first
@@ -865,6 +887,8 @@ __global__ void __maxnreg__(168)
               *reinterpret_cast<uint4 *>(sdS_ptr + (kResident ? (g & 1) : (g % L::kdSTiles)) * L::kdSBytes +
                                          ds_offset(j, 32 * c + 8 * e)) =
                   make_uint4(dsk[4 * e], dsk[4 * e + 1], dsk[4 * e + 2], dsk[4 * e + 3]);
+            // dS^T columns [16c, 16c + 16) lie in dP^T columns already read (chunks <= c/2).
+            if constexpr (kDsTmem) tmem_st_x16(tdS + lane_off + 16 * c, dsk);
           } else {
             tmem_st_x16(tdS + lane_off + 16 * c, dsk);
           }
@@ -876,11 +900,15 @@ __global__ void __maxnreg__(168)
           if (c == 2) {          // P^T(t) and dP^T(t) are all in registers
             tc_fence_before();
             mbar_arrive(p_free);
-            mbar_arrive(dp_free);
+            if constexpr (!kDsTmem) mbar_arrive(dp_free);   // kDsTmem: ds_full covers it
           }
         }
         if (!ok) break;
         if constexpr (kFusedDq) {
+          if constexpr (kDsTmem) {
+            tmem_wait_st();
+            tc_fence_before();
+          }
           fence_proxy_async_smem();
           mbar_arrive(ds_full);
           if (!kResident && t > 0 && !drain_dq(g - 1)) { ok = false; break; }
@@ -967,13 +995,13 @@ __global__ void __maxnreg__(168)
   }
 }
 
-template <int HD, bool kFusedDq, bool kResident = false>
+template <int HD, bool kFusedDq, bool kResident = false, bool kDsTmem = false>
 cudaError_t launch_main_hd(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                            const CUtensorMap &mdo, const CUtensorMap &maux, const CUtensorMap &mdq,
                            __nv_bfloat16 *dk, __nv_bfloat16 *dv, __nv_bfloat16 *dq, int B, int S, int nh,
                            int nkv, float scale, int *status, uint64_t timeout_ns, cudaStream_t stream) {
   using L = BwdLayout<HD, kFusedDq>;
-  auto kernel = attn_bwd_main_kernel<HD, kFusedDq, kResident>;
+  auto kernel = attn_bwd_main_kernel<HD, kFusedDq, kResident, kDsTmem>;
   cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kDynBytes);
   if (err != cudaSuccess) return err;
   // Persistent CTAs: one per SM, or one per unit (resident dQ: per head) when there are
@@ -1039,6 +1067,14 @@ cudaError_t launch_bwd_main_bf16(const CUtensorMap &mq, const CUtensorMap &mk,
   // Without a dQ accumulator map the kernel computes dK and dV only; its mdq parameter
   // is then unused (maux stands in for it).
   const CUtensorMap &md = mdq ? *mdq : maux;
+  if (mdq && nh != nkv) {     // query groups: dK reads dS^T from TMEM
+    if (hd == 64)
+      return launch_main_hd<64, true, false, true>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale,
+                                                   status, timeout_ns, stream);
+    if (hd == 32)
+      return launch_main_hd<32, true, false, true>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale,
+                                                   status, timeout_ns, stream);
+  }
   if (hd == 64)
     return mdq ? launch_main_hd<64, true>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale, status, timeout_ns, stream)
                : launch_main_hd<64, false>(mq, mk, mv, mdo, maux, md, dk, dv, nullptr, B, S, nh, nkv, scale, status, timeout_ns, stream);
