@@ -235,9 +235,11 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
 // overlap the dS arithmetic of iteration t.
 // TMEM columns: S^T [0,128) fp32 | dP^T [128,256) fp32 | P^T bf16 [256,320) |
 //               dV [320,384) | dK [384,448) | dQ fp32 (fused) or dS^T bf16 [448,512)
+//               (kDsTmem: dS^T bf16 over dP^T's first 64 columns)
 // Each region has one producer and its readers release it with an mbarrier before it is
-// rewritten: S^T (s_free), dP^T (dp_free), P^T (p_free by the dS warps, dv_done by the
-// dV product), dQ (dq_empty) or dS^T (dk_done).
+// rewritten: S^T (s_free), dP^T (dp_free; kDsTmem: ds_full and the issue order of dK),
+// P^T (p_free by the dS warps, dv_done by the dV product), dQ (dq_empty) or dS^T
+// (dk_done).
 // mdq (fused dQ only): fp32 map over the dQ accumulator.
 //
 // kResident (with kFusedDq, small problems): a CTA takes every key tile of one (batch, kv
