@@ -61,6 +61,12 @@ EDGE = [
     (2, 200, 6, 3, 32),
     (1, 300, 4, 1, 64),
     (1, 513, 2, 2, 64),
+    # several units per CTA with a ragged last tile: query groups (dK from dS^T in TMEM,
+    # dQ staged in the dS tiles across unit boundaries) and one query head per kv head,
+    # at hd 64 and 32
+    (48, 300, 8, 2, 64),
+    (48, 200, 6, 3, 32),
+    (40, 300, 4, 4, 64),
 ]
 
 
