@@ -136,10 +136,18 @@ __global__ void __maxnreg__(168)
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tdP = tmem + 128, tdS = tmem + 256, tdQ = tmem + 320;
   // One 128-row tile of a [B, S, heads, hd] tensor: one TMA box per 64-column sub-tile.
+  // Debug builds check the tile's coordinates and that it lands inside the tile region.
   auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int head, int row0, int bb) {
+    XATTN_DCHECK(head >= 0 && head < nh && row0 >= 0 && row0 < (S + kTileRows - 1) / kTileRows * kTileRows &&
+                     row0 % kTileRows == 0 && bb >= 0 && bb < B && dst >= smem_u32(smem) &&
+                     dst + L::kTileBytes <= smem_u32(smem + L::kBars),
+                 status);
 #pragma unroll
-    for (int c = 0; c < L::kSubTiles; ++c)
+    for (int c = 0; c < L::kSubTiles; ++c) {
+      XATTN_DCHECK((c * static_cast<int>(L::kAtomBytes / 2)) % 8 == 0 && c * static_cast<int>(L::kAtomBytes / 2) < HD,
+                   status);
       tma_load_4d_elect(dst + c * L::kSubBytes, map, bar, c * static_cast<int>(L::kAtomBytes / 2), head, row0, bb);
+    }
   };
 
   if (warp == 0) {
@@ -151,6 +159,7 @@ __global__ void __maxnreg__(168)
     for (int n = 0, s = 0, use = 0; n < T; ++n) {
       if (!warp_wait(empty(s), (use & 1) ^ 1, ctl)) break;
       mbar_expect_tx_elect(full(s), 2 * L::kTileBytes);
+      XATTN_DCHECK(kvh < nkv && s < kDqStages, status);
       load_tile(sK + s * L::kTileBytes, &mk, full(s), kvh, n * kTileRows, b);
       load_tile(sV + s * L::kTileBytes, &mv, full(s), kvh, n * kTileRows, b);
       issued = n + 1;
@@ -305,6 +314,8 @@ __global__ void __maxnreg__(168)
         tmem_wait_ld();
         reg_fence<16>(v);
         if (ig < S) {
+          XATTN_DCHECK(static_cast<size_t>(row) * HD + g * kHalf + c + 16 <= static_cast<size_t>(B) * S * nh * HD,
+                       status);
           uint4 *dst = reinterpret_cast<uint4 *>(dq + row * HD + g * kHalf + c);
 #pragma unroll
           for (int e = 0; e < 2; ++e)

@@ -417,10 +417,20 @@ __global__ void __maxnreg__(168)
   const uint32_t tdQ = tmem + 448;                                       // fused dQ: dQ
   const uint32_t tdS = (L::kAlias || kDsTmem) ? tdP : tmem + 448;        // dS^T (bf16)
   // One 128-row tile of a [B, S, heads, hd] tensor: one TMA box per 64-column sub-tile.
+  // Debug builds check the tile's coordinates (heads < nh covers both Q/dO and K/V) and
+  // that it lands inside the K / V / Q / dO region of shared memory.
+  const int S_pad = num_m * kTileRows;
+  (void)S_pad;
   auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int head, int row0, int bb) {
+    XATTN_DCHECK(head >= 0 && head < nh && row0 >= 0 && row0 < S_pad && row0 % kTileRows == 0 && bb >= 0 &&
+                     bb < B && dst >= sK && dst + L::kTileBytes <= smem_u32(smem + L::kdO) + kOS * L::kTileBytes,
+                 status);
 #pragma unroll
-    for (int c = 0; c < L::kSubTiles; ++c)
+    for (int c = 0; c < L::kSubTiles; ++c) {
+      XATTN_DCHECK((c * static_cast<int>(L::kAtomBytes / 2)) % 8 == 0 && c * static_cast<int>(L::kAtomBytes / 2) < HD,
+                   status);
       tma_load_4d_elect(dst + c * L::kSubBytes, map, bar, c * static_cast<int>(L::kAtomBytes / 2), head, row0, bb);
+    }
   };
 
   if (warp == 0) {
@@ -437,6 +447,7 @@ __global__ void __maxnreg__(168)
       if (!warp_wait(q_empty(sq), (uq & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(q_full(sq), L::kTileBytes + L::kAuxTileBytes);
       load_tile(sQ + sq * L::kTileBytes, &mq, q_full(sq), h, m * kTileRows, b);
+      XATTN_DCHECK(sq < kQS && m < num_m && h < nh, status);
       tma_load_4d_elect(sAuxB + sq * L::kAuxTileBytes, &maux, q_full(sq), 0, m * kTileRows, h, b);
       issued_q = g + 1;
       if (!warp_wait(o_empty(so), (uo & 1) ^ 1, ctl)) return false;
@@ -458,6 +469,7 @@ __global__ void __maxnreg__(168)
       for (int t = 0; ok && t < pre; ++t) ok = load_ring(t);
       if (!ok || !warp_wait(acc_done, (units - 1) & 1, ctl)) break;
       mbar_expect_tx_elect(kv_full, 2 * L::kTileBytes);
+      XATTN_DCHECK(kvh < nkv && n < num_m, status);
       load_tile(sK, &mk, kv_full, kvh, n * kTileRows, b);
       load_tile(sV, &mv, kv_full, kvh, n * kTileRows, b);
       ++units;
@@ -617,6 +629,7 @@ __global__ void __maxnreg__(168)
               if (n == 0 && t == 0 && !warp_wait(dqt_free, (heads - 1) & 1, ctl)) { ok = false; break; }
               tc_fence_after();
               const uint32_t col = static_cast<uint32_t>(((t / per_head) * num_m + n + t % per_head) * HD);
+              XATTN_DCHECK(col + HD <= 64u, status);     // the resident dQ tiles fit columns [448, 512)
               if (elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kTileRows / 16; ++kk)
@@ -676,6 +689,10 @@ __global__ void __maxnreg__(168)
         if (lane == 0) {
           const int h = kvh * group + t / per_head, m = n + t % per_head;
           const uint32_t src = smem_u32(sdS_ptr + (g % L::kdSTiles) * L::kdSBytes);
+          // fp32 box: the innermost coordinates 0 and HD/2 are 16-byte multiples.
+          XATTN_DCHECK(h < nh && m < num_m && (HD / 2) % 4 == 0 && src >= sdS &&
+                           src + 2 * L::kDqHalfBytes <= sdS + L::kdSTiles * L::kdSBytes,
+                       status);
           tma_reduce_add_4d(&mdq, src, 0, h, m * kTileRows, b);
           tma_reduce_add_4d(&mdq, src + L::kDqHalfBytes, HD / 2, h, m * kTileRows, b);
           bulk_commit_group();
@@ -763,6 +780,7 @@ __global__ void __maxnreg__(168)
       tc_fence_after();
       const int jg = n * kTileRows + j;
       const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
+      XATTN_DCHECK(jg >= S || row_off + HD <= static_cast<size_t>(B) * S * nkv * HD, status);
 #pragma unroll
       for (int c = 0; c < HD; c += 16) {
         uint32_t v[16];
@@ -806,6 +824,7 @@ __global__ void __maxnreg__(168)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint8_t *row = sdS_ptr + (k % L::kdSTiles) * L::kdSBytes + half * L::kDqHalfBytes + j * L::kDqRowBytes;
+        XATTN_DCHECK(half * L::kDqHalfBytes + (j + 1) * L::kDqRowBytes <= L::kdSBytes, status);
 #pragma unroll
         for (int ch = 0; ch < HD / 8; ++ch) {
           const int sw = (HD == 64) ? (ch ^ (j & 7)) : (ch ^ ((j >> 1) & 3));
@@ -884,6 +903,8 @@ __global__ void __maxnreg__(168)
             dsk[2 * q4 + 1] = pack_bf16x2(t2, t3);
           }
           if constexpr (kFusedDq) {
+            XATTN_DCHECK(ds_offset(j, 32 * c + 24) + 16 <= L::kdSBytes && ds_offset(j, 32 * c) + 16 <= L::kdSBytes,
+                         status);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               *reinterpret_cast<uint4 *>(sdS_ptr + (kResident ? (g & 1) : (g % L::kdSTiles)) * L::kdSBytes +
@@ -930,6 +951,7 @@ __global__ void __maxnreg__(168)
       tc_fence_after();
       const int jg = n * kTileRows + j;
       const size_t row_off = (static_cast<size_t>(b) * S + jg) * nkv * HD + static_cast<size_t>(kvh) * HD;
+      XATTN_DCHECK(jg >= S || row_off + HD <= static_cast<size_t>(B) * S * nkv * HD, status);
 #pragma unroll
       for (int c = 0; c < HD; c += 16) {
         uint32_t v[16];
@@ -962,6 +984,9 @@ __global__ void __maxnreg__(168)
               const int i = m * kTileRows + j;
               __nv_bfloat16 *qrow =
                   dq + ((static_cast<size_t>(b) * S + i) * nh + static_cast<size_t>(kvh) * group + r) * HD;
+              XATTN_DCHECK(i >= S || ((static_cast<size_t>(b) * S + i) * nh + static_cast<size_t>(kvh) * group + r + 1) *
+                                             HD <= static_cast<size_t>(B) * S * nh * HD,
+                           status);
 #pragma unroll
               for (int c = 0; c < HD; c += 16) {
                 uint32_t v[16];

@@ -200,10 +200,20 @@ __global__ void __maxnreg__(168)
   auto tO = [&](int x) { return tmem + 256u + (L::kAliasP ? 128u : 64u) * x; };
   auto tP = [&](int x) { return L::kAliasP ? tS(x) : tmem + 384u + 64u * x; };
   // One 128-row tile of a [B, S, heads, hd] tensor: one TMA box per 64-column sub-tile.
+  // Debug builds check the tile's coordinates (heads < nh covers both Q and K/V) and that
+  // it lands inside the tile region of shared memory.
+  const int S_pad = (S + kTileRows - 1) / kTileRows * kTileRows;
+  (void)S_pad;
   auto load_tile = [&](uint32_t dst, const CUtensorMap *map, uint32_t bar, int head, int row0, int bb) {
+    XATTN_DCHECK(head >= 0 && head < nh && row0 >= 0 && row0 < S_pad && row0 % kTileRows == 0 && bb >= 0 &&
+                     bb < B && dst >= smem_u32(smem) && dst + L::kTileBytes <= smem_u32(smem) + L::kBars,
+                 status);
 #pragma unroll
-    for (int c = 0; c < L::kSubTiles; ++c)
+    for (int c = 0; c < L::kSubTiles; ++c) {
+      XATTN_DCHECK((c * static_cast<int>(L::kAtomBytes / 2)) % 8 == 0 && c * static_cast<int>(L::kAtomBytes / 2) < HD,
+                   status);
       tma_load_4d_elect(dst + c * L::kSubBytes, map, bar, c * static_cast<int>(L::kAtomBytes / 2), head, row0, bb);
+    }
   };
 
   if (warp == 0) {
@@ -217,6 +227,7 @@ __global__ void __maxnreg__(168)
       const int s = R % kFwdStages;
       if (!warp_wait(empty(s), ((R / kFwdStages) & 1) ^ 1, ctl)) return false;
       mbar_expect_tx_elect(full(s), 2 * L::kTileBytes);
+      XATTN_DCHECK(kvh < nkv && n <= (S - 1) / kTileRows, status);
       load_tile(sK + s * L::kTileBytes, &mk, full(s), kvh, n * kTileRows, b);
       load_tile(sV + s * L::kTileBytes, &mv, full(s), kvh, n * kTileRows, b);
       issued = ++R;
@@ -491,6 +502,9 @@ __global__ void __maxnreg__(168)
       const int i = mX * kTileRows + row;
       const float inv = 1.f / lrow;
       __nv_bfloat16 *orow = o + (static_cast<size_t>(b) * S + i) * nh * HD + static_cast<size_t>(h) * HD;
+      XATTN_DCHECK(i >= S || (static_cast<size_t>(b) * S + i) * nh * HD + static_cast<size_t>(h + 1) * HD <=
+                                 static_cast<size_t>(B) * S * nh * HD,
+                   status);
 #pragma unroll
       for (int c = 0; c < HD; c += 32) {
         uint32_t ov[32];

@@ -13,6 +13,22 @@ namespace xattn {
 
 // Status values written to the device status word (mirror xattn_status in xattn.h).
 constexpr int kStatusTimeout = 8;
+constexpr int kStatusBounds = 12;
+
+// Debug builds (XATTN_DEBUG): a failed check records kStatusBounds in the status word
+// (the first failure since the last read wins) and the kernel carries on; release builds
+// compile the checks out. Checks only read indices: they never touch the memory checked.
+#ifdef XATTN_DEBUG
+static __device__ __noinline__ void debug_bounds_fail(int *status) { atomicCAS(status, 0, kStatusBounds); }
+#define XATTN_DCHECK(cond, status)                          \
+  do {                                                      \
+    if (!(cond)) ::xattn::debug_bounds_fail(status);        \
+  } while (0)
+#else
+#define XATTN_DCHECK(cond, status) \
+  do {                             \
+  } while (0)
+#endif
 
 // ----------------------------------------------------------------------------------
 // Small helpers

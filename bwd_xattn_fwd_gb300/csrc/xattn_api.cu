@@ -66,6 +66,15 @@ __global__ void wait_selftest_kernel(int *status, unsigned long long limit_ns) {
   (void)mbar_wait(smem_u32(&bar), 0, ctl);
 }
 
+// A bounds check that fails by construction (index n of a range of n elements, never
+// used for an access): in a debug build it records XATTN_ERR_DEVICE_BOUNDS.
+__global__ void bounds_selftest_kernel(int *status, int n) {
+  const int i = n;
+  XATTN_DCHECK(i < n, status);
+  (void)i;
+  (void)status;
+}
+
 xattn_status device_info(DeviceInfo **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return XATTN_ERR_CUDA;
@@ -432,6 +441,8 @@ const char *xattn_status_string(xattn_status s) {
     case XATTN_ERR_WORKSPACE: return "workspace is NULL, not 256-byte aligned, or too small";
     case XATTN_ERR_SCRATCH_LIMIT:
       return "these sizes need more scratch than xattn_bwd_noalloc's fixed array holds";
+    case XATTN_ERR_DEVICE_BOUNDS:
+      return "an on-device bounds check failed (debug build)";
   }
   return "unknown xattn status";
 }
@@ -441,6 +452,21 @@ xattn_status xattn_selftest_wait_timeout(unsigned long long limit_ns, void *stre
   DeviceInfo *dev = nullptr;
   XATTN_TRY(device_info(&dev));
   wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status, limit_ns);
+  return cuda_status(cudaGetLastError());
+}
+
+int xattn_build_flags(void) {
+#ifdef XATTN_DEBUG
+  return XATTN_BUILD_DEVICE_CHECKS;
+#else
+  return 0;
+#endif
+}
+
+xattn_status xattn_selftest_bounds_check(void *stream) {
+  DeviceInfo *dev = nullptr;
+  XATTN_TRY(device_info(&dev));
+  bounds_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(dev->status, 1);
   return cuda_status(cudaGetLastError());
 }
 

@@ -79,8 +79,14 @@ _lib.xattn_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i]
 _lib.xattn_bwd_workspace_bytes.restype = ctypes.c_size_t
 _lib.xattn_bwd_dq_mode.argtypes = [_i, _i, _i, _i, _i]
 _lib.xattn_bwd_dq_mode.restype = ctypes.c_int
+_lib.xattn_build_flags.argtypes = []
+_lib.xattn_build_flags.restype = ctypes.c_int
+_lib.xattn_selftest_bounds_check.argtypes = [_vp]
+_lib.xattn_selftest_bounds_check.restype = ctypes.c_int
 
 BWD_FUSED_DQ, BWD_RESIDENT_DQ, BWD_QUERY_DQ = 0, 1, 2
+BUILD_DEVICE_CHECKS = 1             # xattn_build_flags bit: on-device bounds checks compiled in
+ERR_DEVICE_TIMEOUT, ERR_DEVICE_BOUNDS = 8, 12
 
 
 def lib_path() -> str:
@@ -191,6 +197,17 @@ def xattn_selftest_wait_timeout(limit_ns, stream=None):
     st = fn(int(limit_ns), _stream(stream))
     if st != 0:
         raise XattnError(st, "xattn_selftest_wait_timeout")
+
+
+def xattn_build_flags() -> int:
+    """Bit BUILD_DEVICE_CHECKS is set in a debug build (on-device bounds checks)."""
+    return int(_lib.xattn_build_flags())
+
+
+def xattn_selftest_bounds_check(stream=None):
+    st = _lib.xattn_selftest_bounds_check(_stream(stream))
+    if st != 0:
+        raise XattnError(st, "xattn_selftest_bounds_check")
 
 
 def xattn_status_string(status: int) -> str:

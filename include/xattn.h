@@ -66,7 +66,9 @@ typedef enum {
     XATTN_ERR_BAD_SCALE = 9,          /* scale is not finite (bf16 backward: or
                                          0 < |scale| < 2^-64) */
     XATTN_ERR_WORKSPACE = 10,         /* workspace pointer NULL/misaligned or too small */
-    XATTN_ERR_SCRATCH_LIMIT = 11      /* xattn_bwd_noalloc: sizes need more than its fixed scratch */
+    XATTN_ERR_SCRATCH_LIMIT = 11,     /* xattn_bwd_noalloc: sizes need more than its fixed scratch */
+    XATTN_ERR_DEVICE_BOUNDS = 12      /* debug builds only: an on-device bounds check failed
+                                         (reported later, like a timeout) */
 } xattn_status;
 
 /*
@@ -230,7 +232,8 @@ const char *xattn_status_string(xattn_status status);
 /*
  * Synchronises `stream`, then reads and clears the current device's status word.
  * Returns XATTN_ERR_DEVICE_TIMEOUT if a kernel gave up on a bounded wait since the
- * last check, XATTN_ERR_CUDA if the synchronisation failed, else XATTN_OK.
+ * last check (XATTN_ERR_DEVICE_BOUNDS if, in a debug build, a bounds check failed first),
+ * XATTN_ERR_CUDA if the synchronisation failed, else XATTN_OK.
  */
 xattn_status xattn_check_device_status(void *stream);
 
@@ -245,6 +248,26 @@ xattn_status xattn_check_device_status(void *stream);
  * Asynchronous on `stream`; returns XATTN_OK once launched.
  */
 xattn_status xattn_selftest_wait_timeout(unsigned long long limit_ns, void *stream);
+
+/*
+ * Debug build (the library compiled with XATTN_DEBUG; bwd_xattn_fwd_gb300/build.py
+ * builds it with `--debug` into its own directory). The tensor-core kernels then check,
+ * before each use, the indices they compute -- TMA tile coordinates against the tensor's
+ * extents and the 16-byte rule for the innermost coordinate, shared-memory offsets
+ * against their tile, tensor-memory columns against their region, and global row offsets
+ * of direct stores against the tensor -- and record XATTN_ERR_DEVICE_BOUNDS in the device
+ * status word when one fails (no trap; xattn_check_device_status reports it). It stands in
+ * for a memory checker; release builds compile the checks out.
+ *
+ * xattn_build_flags: bit 0 set in a debug build. No device work.
+ * xattn_selftest_bounds_check: launches one small kernel whose only work is a bounds check
+ * that fails (an index one past the end of a 1-element range, never used for an access),
+ * so a test can see XATTN_ERR_DEVICE_BOUNDS reported in a debug build (and nothing in a
+ * release build). Asynchronous on `stream`; returns XATTN_OK once launched.
+ */
+#define XATTN_BUILD_DEVICE_CHECKS 1
+int xattn_build_flags(void);
+xattn_status xattn_selftest_bounds_check(void *stream);
 
 #ifdef __cplusplus
 }

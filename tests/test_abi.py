@@ -43,12 +43,27 @@ def test_binding_exposes_the_same_names():
 def test_status_strings(lib):
     lib.xattn_status_string.restype = ctypes.c_char_p
     seen = set()
-    for code in range(0, 12):
+    for code in range(0, 13):
         s = lib.xattn_status_string(code).decode()
         assert s and s != "unknown xattn status"
         seen.add(s)
-    assert len(seen) == 12
+    assert len(seen) == 13
     assert lib.xattn_status_string(99).decode() == "unknown xattn status"
+
+
+def test_release_build_has_no_device_checks(lib):
+    """The default build compiles the on-device bounds checks out (bit 0 of the flags);
+    the debug build (build(debug=True)) is a separate library."""
+    lib.xattn_build_flags.restype = ctypes.c_int
+    assert lib.xattn_build_flags() == 0
+
+
+def test_debug_build_compiles_and_reports_its_checks():
+    """The debug build (XATTN_DEBUG) builds without a GPU and says so in its flags."""
+    from bwd_xattn_fwd_gb300 import build
+    dbg = ctypes.CDLL(build.build(debug=True))
+    dbg.xattn_build_flags.restype = ctypes.c_int
+    assert dbg.xattn_build_flags() == 1
 
 
 def _fwd(lib, q=16, k=32, v=48, B=1, S=4, nh=2, nkv=1, hd=64, scale=0.125, o=64, lse=80):
