@@ -17,8 +17,11 @@
 //        S^T  = K_n Q_m^T - LSE/scale   (TMEM, 128 x 128 fp32; the per-query term is one
 //        dP^T = V_n dO_m^T - D          extra tensor-core K step over the auxiliary rows)
 //        P^T  = exp2(S^T scale log2e)               -> bf16 into TMEM
-//        dS^T = P^T dP^T                            -> bf16 into TMEM
-//        dV_n += P^T dO_m ,  dK_n += dS^T Q_m       (A operands from TMEM)
+//        dS^T = P^T dP^T                            -> bf16 into TMEM (for dK) and, with
+//                                                      fused dQ, shared memory (for dQ)
+//        dV_n += P^T dO_m ,  dK_n += dS^T Q_m       (A operands from TMEM; with fused dQ
+//                                                      and one query head per kv head,
+//                                                      dK reads dS^T from shared memory)
 //      The softmax scale of dS is applied once, to dK_n in the epilogue.
 //      Warps: 0 = TMA producer, 1 = TMEM owner + MMA issuer of S^T and dV,
 //      3 = MMA issuer of dP^T and dK, 4-7 = P, 8-11 = dS (one thread per key row).
@@ -228,8 +231,8 @@ __device__ __forceinline__ uint32_t ds_offset(int j, int i) {
 //   warps 4-7  : P^T = exp2(S^T scale log2e), S^T already holding -LSE/scale, one
 //                thread per key row, all 128 query columns (the special-function work)
 //   warps 8-11 : dS^T = P^T (dP^T - D), dP^T already holding -D, one thread per key
-//                row (the FMA work); fused dQ: also the dQ drain (TMEM -> shared-memory
-//                staging, one query row per thread)
+//                row (the FMA work); fused dQ: also the dQ drain (TMEM -> the shared-
+//                memory dS tile the dQ was computed from, one query row per thread)
 // The two compute warpgroups work on consecutive (r, m) iterations at the same time, so
 // each SM sub-partition runs one warp of each and the exponentials of iteration t+1
 // overlap the dS arithmetic of iteration t.
