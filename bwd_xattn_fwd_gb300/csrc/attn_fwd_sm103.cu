@@ -386,11 +386,16 @@ __global__ void __maxnreg__(168)
       const int mX = x == 0 ? mA : mB;
       if (x == 1 && !hasB) continue;
       float mrow = -INFINITY, lrow = 0.f;
-#pragma unroll 1
-      for (int n = 0; n <= mX; ++n, ++gx) {
-        if (!warp_wait(s_full(x), gx & 1, ctl)) { ok = false; break; }
+      // One key step; `masked` selects the diagonal tile's copy, compiled apart from the
+      // loop over the other tiles so that their code carries no mask. On the diagonal
+      // tile the warp's rows are 32 q .. 32 q + 31 (q = quarter): 32-column chunks below q
+      // are wholly visible, chunk q is masked per lane (key column > row), chunks above q
+      // are wholly masked (P = 0 without exponentials); q is warp-uniform, so each chunk
+      // takes one branch-free path.
+      auto step = [&](auto masked, int n) -> bool {
+        constexpr bool kDiag = decltype(masked)::value;
+        if (!warp_wait(s_full(x), gx & 1, ctl)) return false;
         tc_fence_after();
-        const bool diag = (n == mX);
         // The whole row of S_X(n) comes into registers with one TMEM read, and the buffer
         // is released at once: S_X(n+1) is computed while this softmax runs.
         uint32_t r[128];
@@ -404,11 +409,11 @@ __global__ void __maxnreg__(168)
         // (scale >= 0) or their scaled minimum (scale < 0); masked columns do not count.
         constexpr float kFill = kNegScale ? INFINITY : -INFINITY;
         float mx4[4] = {kFill, kFill, kFill, kFill};
-        auto maxpass = [&](auto masked) {
+        auto max_chunk = [&](auto mask_chunk, int c32) {
 #pragma unroll
-          for (int c = 0; c < 128; c += 2) {
+          for (int c = c32; c < c32 + 32; c += 2) {
             float v0 = __uint_as_float(r[c]), v1 = __uint_as_float(r[c + 1]);
-            if (decltype(masked)::value) {
+            if (decltype(mask_chunk)::value) {
               if (c > row) v0 = kFill;
               if (c + 1 > row) v1 = kFill;
             }
@@ -416,8 +421,11 @@ __global__ void __maxnreg__(168)
             a = kNegScale ? fmin3(a, v0, v1) : fmax3(a, v0, v1);
           }
         };
-        if (diag) maxpass(std::true_type{});
-        else maxpass(std::false_type{});
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          if (!kDiag || cc < quarter) max_chunk(std::false_type{}, 32 * cc);
+          else if (cc == quarter) max_chunk(std::true_type{}, 32 * cc);
+        }
         const float mx = (kNegScale ? fmin3(mx4[0], mx4[1], fminf(mx4[2], mx4[3]))
                                     : fmax3(mx4[0], mx4[1], fmaxf(mx4[2], mx4[3]))) * scale_log2;
         // Conditional rescaling: keep the stale max unless some row of the warp grew by
@@ -433,26 +441,25 @@ __global__ void __maxnreg__(168)
         const float neg_m = -m_use;
         // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
         // included), the exponentials, row sums and bf16 P, packed in place into r[0, 64).
-        // One pair in eight of an unmasked tile is exponentiated on the FMA pipe
+        // One pair in eight of a visible chunk is exponentiated on the FMA pipe
         // (exp2_fma2) instead of MUFU, which both tiles' softmax warps share.
-        // The diagonal tile has its own copy of the body, so the common one is branch-free.
         // The first three quarters of P are computed before waiting for the previous PV_X
         // (which still reads P_X), so that product's latency overlaps the exponentials;
         // storing them before the last quarter keeps the register peak at one S row.
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-        auto chunk = [&](auto masked, int c32) {
+        auto exp_chunk = [&](auto mask_chunk, int c32) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c = c32 + 2 * e;
             float x0, x1;
             ffma2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), scale_log2, scale_log2,
                   neg_m, neg_m);
-            if (decltype(masked)::value) {
+            if (decltype(mask_chunk)::value) {
               if (c > row) x0 = -INFINITY;
               if (c + 1 > row) x1 = -INFINITY;
             }
             float p0, p1;
-            if (!decltype(masked)::value && (e & 7) == 7) {
+            if (!decltype(mask_chunk)::value && (e & 7) == 7) {
               exp2_fma2(x0, x1, p0, p1);
             } else {
               p0 = ex2_approx(x0);
@@ -463,20 +470,25 @@ __global__ void __maxnreg__(168)
             r[c32 / 2 + e] = pack_bf16x2(p0, p1);
           }
         };
-        auto body = [&](auto masked) -> bool {
-          chunk(masked, 0);
-          chunk(masked, 32);
-          chunk(masked, 64);
-          if (!warp_wait(o_done(x), (gx - 1) & 1, ctl)) return false;
-          tc_fence_after();
-          tmem_st_x32(tPx, r);
-          tmem_st_x16(tPx + 32, r + 32);
-          chunk(masked, 96);
-          tmem_st_x16(tPx + 48, r + 48);
-          return true;
+        auto chunk = [&](int cc) {
+          if (!kDiag || cc < quarter) {
+            exp_chunk(std::false_type{}, 32 * cc);
+          } else if (cc == quarter) {
+            exp_chunk(std::true_type{}, 32 * cc);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) r[16 * cc + e] = 0u;
+          }
         };
-        const bool okb = diag ? body(std::true_type{}) : body(std::false_type{});
-        if (!okb) { ok = false; break; }
+        chunk(0);
+        chunk(1);
+        chunk(2);
+        if (!warp_wait(o_done(x), (gx - 1) & 1, ctl)) return false;
+        tc_fence_after();
+        tmem_st_x32(tPx, r);
+        tmem_st_x16(tPx + 32, r + 32);
+        chunk(3);
+        tmem_st_x16(tPx + 48, r + 48);
         if (rescale && n > 0) {
 #pragma unroll
           for (int c = 0; c < HD; c += 32) {
@@ -494,6 +506,15 @@ __global__ void __maxnreg__(168)
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(p_full(x));
+        return true;
+      };
+#pragma unroll 1
+      for (int n = 0; n < mX; ++n, ++gx) {
+        if (!step(std::false_type{}, n)) { ok = false; break; }
+      }
+      if (ok) {
+        if (!step(std::true_type{}, mX)) ok = false;
+        ++gx;
       }
       if (!ok) break;
       // Epilogue: O / l in bf16 and the LSE; then O_X is free for the next unit.
