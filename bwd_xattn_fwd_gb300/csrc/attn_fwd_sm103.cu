@@ -441,8 +441,9 @@ __global__ void __maxnreg__(168)
         const float neg_m = -m_use;
         // Exponents, the causal mask on them (-inf -> exact zeros for any scale, 0
         // included), the exponentials, row sums and bf16 P, packed in place into r[0, 64).
-        // One pair in eight of a visible chunk is exponentiated on the FMA pipe
-        // (exp2_fma2) instead of MUFU, which both tiles' softmax warps share.
+        // One pair in eight of the other tiles' chunks is exponentiated on the FMA pipe
+        // (exp2_fma2) instead of MUFU, which both tiles' softmax warps share (the diagonal
+        // copy keeps MUFU: measured slightly faster there).
         // The first three quarters of P are computed before waiting for the previous PV_X
         // (which still reads P_X), so that product's latency overlaps the exponentials;
         // storing them before the last quarter keeps the register peak at one S row.
@@ -459,7 +460,7 @@ __global__ void __maxnreg__(168)
               if (c + 1 > row) x1 = -INFINITY;
             }
             float p0, p1;
-            if (!decltype(mask_chunk)::value && (e & 7) == 7) {
+            if (!kDiag && !decltype(mask_chunk)::value && (e & 7) == 7) {
               exp2_fma2(x0, x1, p0, p1);
             } else {
               p0 = ex2_approx(x0);
