@@ -8,20 +8,30 @@
 // on the device (M2c). Grouped KV heads as in the training path (row T15): query head h
 // reads kv head h / group.
 //
-// GB300 mapping. The work is a matrix-vector product per (sequence, query head): two
-// multiply-adds per cached K or V element and group, so it is bound by HBM reading the
-// cache, not by arithmetic -- it runs on the CUDA cores, with every cached byte read once.
-//   1. decode_partial_kernel: one CTA per (batch, kv head, 256-key chunk), 256 threads.
-//      The chunk's K and V rows are copied once into shared memory (coalesced 16-byte
-//      cp.async pieces, all in flight at once; V lands during the score pass) and serve
-//      all `group` query heads of the kv head: one key per thread for the scores, a
-//      chunk-local softmax (max and sum in fp32, log2 domain), then two head-dim elements
-//      per thread over a contiguous run of keys for the unnormalised partial outputs.
-//      Each chunk writes (max, sum, partial O) per query head to the scratch buffer.
-//      The arithmetic, not HBM, is what the CTAs spend most issue slots on, so both
-//      passes use the packed two-lane fp32 FMA (__ffma2_rn): the scores pair adjacent
-//      head-dim elements, P V pairs adjacent keys (two partial sums per output, added at
-//      the end); each lane is an ordinary fp32 fma.
+// GB300 mapping. Per (sequence, kv head) the work is two thin products against the
+// cache -- S^T = K q^T (keys x the group's query heads) and O^T = V^T P^T -- so it is bound
+// by HBM reading the cache once. Both products run on the tensor cores (tcgen05, fp32
+// accumulators in TMEM), which leaves the CUDA cores only the softmax of a chunk:
+//   1. decode_partial_kernel: one CTA of 4 warps per (batch, kv head, chunk of C keys),
+//      C = 16384 / hd (512, 256, 128 keys at hd = 32, 64, 128), so that a chunk's K and its
+//      V are 32 KB each (three CTAs share an SM).
+//      * Loads: one elected thread issues TMA loads of the chunk's C/128 K tiles and V
+//        tiles (128-key boxes of one kv head, swizzled like the training kernels' tiles;
+//        keys past T read as zeros); the threads write the group's query rows, padded to
+//        16 rows with zeros, as a K-major operand tile.
+//      * Scores: per 128-key tile, S^T = K q^T (M = 128 keys, N = 16, K = hd) into TMEM.
+//      * Softmax: thread i owns key i of every tile (its TMEM lane). The chunk maximum
+//        and sum of each head (fp32, log2 domain) are reduced over the CTA; P^T goes to
+//        shared memory in bf16 as a K-major operand whose row (tile j, head r) holds the
+//        128 keys of tile j; the sum adds the rounded values that P V uses.
+//      * P V: one product per chunk. A = the chunk's V tiles read as one MN-major operand
+//        of M = 128 rows, row (tile j, head-dim element d) (hd = 64: two tiles, each one
+//        64-element swizzle atom; hd = 32: four; hd = 128: one tile of two atoms);
+//        B = P^T with N = (C/128) x G columns (tile j', head r). The blocks j = j' are the
+//        tiles' partial outputs; the others are discarded (the products are tiny next to
+//        the loads).
+//      * Epilogue: thread (tile j, d) reads its block's head columns, the tiles are summed
+//        through shared memory, and the chunk writes (max, sum, partial O) per head.
 //   2. decode_combine_kernel: one warp per (batch, query head) merges the chunks
 //      (rescaling each by 2^(m_c - M)), writes O in bf16 and LSE = (M + log2 L) ln 2.
 #include "sm103_ptx.cuh"
@@ -29,258 +39,308 @@
 
 namespace xattn {
 
+int decode_chunk_keys(int hd) { return 16384 / hd; }
+
 size_t decode_workspace_bytes(int B, int T, int nh, int hd) {
-  const size_t chunks = static_cast<size_t>((T + kDecodeChunk - 1) / kDecodeChunk);
+  const int ck = decode_chunk_keys(hd);
+  const size_t chunks = static_cast<size_t>((T + ck - 1) / ck);
   return static_cast<size_t>(B) * nh * chunks * (static_cast<size_t>(hd) + 2) * sizeof(float);
 }
 
 namespace {
 
-constexpr int kDecodeThreads = kDecodeChunk;   // one key per thread in the score pass
-constexpr int kDecodeWarps = kDecodeThreads / 32;
+constexpr int kDecThreads = 128;   // one thread per key of a 128-key tile (TMEM lane)
 
-// Dynamic shared memory of decode_partial_kernel:
-//   region A: first the chunk's K rows [kChunk][HD + 8] bf16 (padded by 16 bytes so that
-//             one-row-per-thread reads spread over all banks); after the score pass, which
-//             is their last reader, the exponentials p [group][kChunk] and the per
-//             key-subset partial outputs acc [nks][group][HD] (nks = kDecodeThreads / (HD/2))
-//   vs  [kChunk][HD + 8] bf16  the chunk's V rows (K and V are copied with cp.async at the
-//                              start in two groups: the score pass waits for K only)
-//   q   [group][HD] float      the query rows, pre-scaled by scale * log2(e)
-//   red [kDecodeWarps][group]  warp partials of the max / sum
-template <int HD>
-__host__ __device__ constexpr int decode_row_elems() { return HD + 8; }
+// Shared memory and TMEM of one CTA; G = the group padded to 4, 8 or 16 (at least
+// 16 / kSub, so that P V has N a multiple of 16).
+//   [kK, +32 KB)  the chunk's K tiles (tile j at j * kTileBytes; at hd = 128 two 64-column
+//                 sub-tiles each); after the scores, the epilogue's per-tile partials
+//                 [kSub][G][HD] fp32
+//   [kV, +32 KB)  the chunk's V tiles, same layout
+//   [kQP, ...)    the query tile [16 rows x hd] (K-major, the tiles' swizzle), then P^T
+//                 [kNpv rows x 128 keys] bf16 (K-major, 128-byte swizzle, two 64-key columns)
+//   [kRed, ...)   per-warp maxima and sums [2][4 warps][16 heads]
+//   barriers: full_k, full_v, s_done, o_done; TMEM address; abort flag
+// TMEM columns: S^T of tile j at [16 j, 16 j + 16); O^T at [kTmemO, kTmemO + kNpv).
+template <int HD, int G>
+struct DecLayout {
+  static constexpr int kSub = 128 / HD;                       // 128-key tiles per chunk
+  static constexpr int kChunk = 128 * kSub;                   // keys per chunk
+  static constexpr uint32_t kAtomBytes = HD * 2 < 128 ? HD * 2 : 128;   // swizzle-atom row
+  static constexpr int kSubTiles = HD * 2 / static_cast<int>(kAtomBytes);
+  static constexpr uint32_t kSubBytes = kTileRows * kAtomBytes;
+  static constexpr uint32_t kTileBytes = kTileRows * HD * 2;
+  static constexpr uint32_t kKVBytes = kSub * kTileBytes;
+  static constexpr uint32_t kSwizzle = HD == 32 ? kSwizzle64 : kSwizzle128;
+  static constexpr int kNpv = kSub * G;
+  static constexpr uint32_t kPColBytes = kNpv * 128;          // 64 keys of every P^T row
+  static constexpr uint32_t kPBytes = 2 * kPColBytes;
+  static constexpr uint32_t kQColBytes = 16 * kAtomBytes;     // one atom column of the query tile
+  static constexpr uint32_t kQBytes = kSubTiles * kQColBytes;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kKVBytes;
+  static constexpr uint32_t kQP = 2 * kKVBytes;
+  static constexpr uint32_t kRed = kQP + (kPBytes > kQBytes ? kPBytes : kQBytes);
+  static constexpr uint32_t kBars = kRed + 2 * 4 * 16 * 4;
+  static constexpr uint32_t kMisc = kBars + 4 * 8;
+  static constexpr uint32_t kUsed = kMisc + 32;
+  static constexpr uint32_t kDynBytes = kUsed + 1024;        // + alignment of the base to 1 KB
+  static constexpr uint32_t kTmemO = 16 * kSub;
+  static constexpr uint32_t kTmemCols = kTmemO + kNpv <= 32 ? 32 : (kTmemO + kNpv <= 64 ? 64 : 128);
+  static_assert(kNpv % 16 == 0 && kTmemO + kNpv <= 128, "P V: N a multiple of 16, TMEM within 128 columns");
+  static_assert(kSub * G * HD * 4 <= kKVBytes, "the epilogue's partials fit the K region");
+  static_assert(kPColBytes % 1024 == 0 && kSubBytes % 1024 == 0 && kQP % 1024 == 0,
+                "swizzled operands need 1024-byte alignment");
+  static_assert(3 * (kDynBytes + 1024) <= 228 * 1024 || G == 16, "three CTAs per SM");
+};
 
-template <int HD>
-__host__ __device__ constexpr size_t decode_region_a_bytes(int group) {
-  const size_t k_rows = static_cast<size_t>(kDecodeChunk) * decode_row_elems<HD>() * 2;
-  const size_t p_acc = sizeof(float) * static_cast<size_t>(group) * (kDecodeChunk + (kDecodeThreads / (HD / 2)) * HD);
-  return k_rows > p_acc ? k_rows : p_acc;
+// Warp-uniform bounded wait: every lane waits, then all agree.
+__device__ __forceinline__ bool dec_warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
+  const bool ok = mbar_wait(bar, parity, ctl);
+  return __all_sync(0xffffffffu, ok);
 }
 
-template <int HD>
-__host__ __device__ constexpr size_t decode_smem_bytes(int group) {
-  return decode_region_a_bytes<HD>(group) + static_cast<size_t>(kDecodeChunk) * decode_row_elems<HD>() * 2 +
-         sizeof(float) * static_cast<size_t>(group) * (HD + kDecodeWarps);
-}
+template <int HD, int G>
+__global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
+    const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+    const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o, float *__restrict__ ws_ml, int B, int T,
+    int nh, int nkv, float scale_log2, int *status, unsigned long long timeout_ns) {
+  using L = DecLayout<HD, G>;
+  extern __shared__ uint8_t dsm_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0), lane = threadIdx.x & 31;
+  const int t = threadIdx.x;
+  const int group = nh / nkv;
+  const int BK = B * nkv;
+  const int bk = static_cast<int>(blockIdx.x % static_cast<unsigned>(BK));
+  const int chunk = static_cast<int>(blockIdx.x / static_cast<unsigned>(BK));
+  const int chunks = static_cast<int>(gridDim.x / static_cast<unsigned>(BK));
+  const int b = bk / nkv, kvh = bk % nkv;
+  const int key0 = chunk * L::kChunk;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+  const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV), sQP = smem_u32(smem + L::kQP);
+  float *red_max = reinterpret_cast<float *>(smem + L::kRed);   // [4][16]
+  float *red_sum = red_max + 64;                                  // [4][16]
+  const uint32_t bar0 = smem_u32(smem + L::kBars);
+  const uint32_t full_k = bar0, full_v = bar0 + 8, s_done = bar0 + 16, o_done = bar0 + 24;
+  uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + L::kMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
+  const WaitCtl ctl{abort_flag, status, timeout_ns};
 
-// MAXG: a compile-time bound on the group (4, 8 or 16), so the per-head register arrays
-// are no larger than needed.
-template <int HD, int MAXG>
-__global__ void __launch_bounds__(kDecodeThreads) decode_partial_kernel(
-    const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-    const __nv_bfloat16 *__restrict__ v, float *__restrict__ ws_o, float *__restrict__ ws_ml, int T,
-    int nh, int nkv, float scale_log2) {
-  constexpr int kPairs = HD / 2;                       // head-dim pairs
-  constexpr int kSubsets = kDecodeThreads / kPairs;    // key subsets of the PV pass
-  extern __shared__ __align__(16) uint8_t dsm_raw[];
+  if (t == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8u * i, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&mk);
+      tma_prefetch_desc(&mv);
+    }
+    tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   grid_dep_launch();
   grid_dep_wait();
-  const int group = nh / nkv;
-  const int chunk = blockIdx.y, chunks = gridDim.y;
-  const int bk = blockIdx.x, b = bk / nkv, kvh = bk % nkv;
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  constexpr int kRow = decode_row_elems<HD>();          // padded smem row, elements
-  const size_t region_a = decode_region_a_bytes<HD>(group);
-  __nv_bfloat16 *kt = reinterpret_cast<__nv_bfloat16 *>(dsm_raw);                   // [kChunk][kRow]
-  float *ps = reinterpret_cast<float *>(dsm_raw);       // [group][kDecodeChunk], after the scores
-  float *acc = ps + group * kDecodeChunk;               // [kSubsets][group][HD], after the scores
-  __nv_bfloat16 *vs = reinterpret_cast<__nv_bfloat16 *>(dsm_raw + region_a);         // [kChunk][kRow]
-  float *qs = reinterpret_cast<float *>(vs + kDecodeChunk * kRow);                  // [group][HD]
-  float *red = qs + group * HD;                         // [kDecodeWarps][group]
+  const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
 
-  const int j = chunk * kDecodeChunk + t;
-  const bool valid = j < T;
-  const size_t row_stride = static_cast<size_t>(nkv) * HD;           // elements between keys
-  const size_t kv_base = (static_cast<size_t>(b) * T * nkv + kvh) * HD;
-  // The chunk's K rows, then its V rows, stream into shared memory: consecutive threads
-  // copy consecutive 16-byte pieces of a row, so every request is a whole row segment.
-  // Rows past T are not copied and never read. V lands while the scores are computed.
-  const int n_valid = min(kDecodeChunk, T - chunk * kDecodeChunk);
-  constexpr int kPieces = HD / 8;                       // 16-byte pieces per row
-  {
-    const __nv_bfloat16 *kc = k + kv_base + static_cast<size_t>(chunk) * kDecodeChunk * row_stride;
-    const __nv_bfloat16 *vc = v + kv_base + static_cast<size_t>(chunk) * kDecodeChunk * row_stride;
-    for (int e = t; e < n_valid * kPieces; e += kDecodeThreads) {
-      const int row = e / kPieces, pc = e % kPieces;
-      cp_async16(smem_u32(kt + row * kRow + 8 * pc), kc + static_cast<size_t>(row) * row_stride + 8 * pc);
-    }
-    cp_async_commit();
-    for (int e = t; e < n_valid * kPieces; e += kDecodeThreads) {
-      const int row = e / kPieces, pc = e % kPieces;
-      cp_async16(smem_u32(vs + row * kRow + 8 * pc), vc + static_cast<size_t>(row) * row_stride + 8 * pc);
-    }
-    cp_async_commit();
+  // ---- loads: the chunk's K tiles, then its V tiles (one barrier each) ----
+  if (warp == 0) {
+    XATTN_DCHECK(b < B && kvh < nkv && key0 < T, status);
+    mbar_expect_tx_elect(full_k, L::kKVBytes);
+#pragma unroll
+    for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+      for (int c = 0; c < L::kSubTiles; ++c)
+        tma_load_4d_elect(sK + j * L::kTileBytes + c * L::kSubBytes, &mk, full_k, c * 64, kvh,
+                          key0 + j * kTileRows, b);
+    mbar_expect_tx_elect(full_v, L::kKVBytes);
+#pragma unroll
+    for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+      for (int c = 0; c < L::kSubTiles; ++c)
+        tma_load_4d_elect(sV + j * L::kTileBytes + c * L::kSubBytes, &mv, full_v, c * 64, kvh,
+                          key0 + j * kTileRows, b);
   }
-
-  // Query rows of the group's heads (kvh * group + r), scaled into the log2 domain.
-  const __nv_bfloat16 *qg = q + (static_cast<size_t>(b) * nh + static_cast<size_t>(kvh) * group) * HD;
-  for (int e = t; e < group * HD; e += kDecodeThreads) qs[e] = __bfloat162float(qg[e]) * scale_log2;
-  cp_async_wait<1>();                                   // this thread's K pieces have landed
-  __syncthreads();                                      // ... and every thread's
-
-  // ---- scores: thread t takes key j = chunk * kDecodeChunk + t, all heads of the group ----
-  float s[MAXG];
+  // ---- the query tile: rows r < group are query heads kvh * group + r, the rest zero ----
   {
-    float2 s2[MAXG];
+    constexpr int kPieces = HD / 8;                              // 16-byte pieces per row
+    constexpr int kAtomPieces = static_cast<int>(L::kAtomBytes / 16);
+    const __nv_bfloat16 *qg = q + (static_cast<size_t>(b) * nh + static_cast<size_t>(kvh) * group) * HD;
+    for (int e = t; e < 16 * kPieces; e += kDecThreads) {
+      const int n = e / kPieces, pc = e % kPieces;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (n < group) val = *reinterpret_cast<const uint4 *>(qg + n * HD + 8 * pc);
+      const int col = pc / kAtomPieces, ch = pc % kAtomPieces;
+      const int sw = L::kAtomBytes == 128 ? (ch ^ (n & 7)) : (ch ^ ((n >> 1) & 3));
+      *reinterpret_cast<uint4 *>(smem + L::kQP + col * L::kQColBytes + n * L::kAtomBytes + (sw << 4)) = val;
+    }
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+
+  // ---- scores S^T = K q^T, one M = 128, N = 16 product per tile ----
+  bool ok = true, issued_s = false, issued_o = false;
+  if (warp == 0) {
+    ok = dec_warp_wait(full_k, 0, ctl);
+    if (ok) {
+      tc_fence_after();
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16, false, false);
+      const uint64_t dK = smem_desc(sK, 16, 8 * L::kAtomBytes, L::kSwizzle);
+      const uint64_t dQ = smem_desc(sQP, 16, 8 * L::kAtomBytes, L::kSwizzle);
+      if (elect_one()) {
 #pragma unroll
-    for (int r = 0; r < MAXG; ++r) s2[r] = make_float2(0.f, 0.f);
-    if (valid) {
-      const uint4 *krow = reinterpret_cast<const uint4 *>(kt + t * kRow);
+        for (int j = 0; j < L::kSub; ++j)
 #pragma unroll
-      for (int c = 0; c < HD / 8; ++c) {
-        const uint4 kv8 = krow[c];
-        const float2 k01 = make_float2(bf16lo_to_f32(kv8.x), bf16hi_to_f32(kv8.x));
-        const float2 k23 = make_float2(bf16lo_to_f32(kv8.y), bf16hi_to_f32(kv8.y));
-        const float2 k45 = make_float2(bf16lo_to_f32(kv8.z), bf16hi_to_f32(kv8.z));
-        const float2 k67 = make_float2(bf16lo_to_f32(kv8.w), bf16hi_to_f32(kv8.w));
-#pragma unroll
-        for (int r = 0; r < MAXG; ++r) {
-          if (r < group) {
-            const float4 qa = *reinterpret_cast<const float4 *>(qs + r * HD + 8 * c);
-            const float4 qb = *reinterpret_cast<const float4 *>(qs + r * HD + 8 * c + 4);
-            s2[r] = __ffma2_rn(make_float2(qa.x, qa.y), k01, s2[r]);
-            s2[r] = __ffma2_rn(make_float2(qa.z, qa.w), k23, s2[r]);
-            s2[r] = __ffma2_rn(make_float2(qb.x, qb.y), k45, s2[r]);
-            s2[r] = __ffma2_rn(make_float2(qb.z, qb.w), k67, s2[r]);
+          for (int kk = 0; kk < HD / 16; ++kk) {
+            // a K step of 16 elements is +32 bytes within a swizzled row; the fifth step
+            // starts the second 64-column atom (hd = 128)
+            const uint32_t kstep = (kk % 4) * 2;
+            mma_ss(tmem + 16u * j, dK + j * (L::kTileBytes >> 4) + (kk / 4) * (L::kSubBytes >> 4) + kstep,
+                   dQ + (kk / 4) * (L::kQColBytes >> 4) + kstep, idesc_s, kk > 0 ? 1u : 0u);
           }
-        }
+        mma_commit(s_done);
       }
+      __syncwarp();
+      issued_s = true;
     }
-#pragma unroll
-    for (int r = 0; r < MAXG; ++r) s[r] = s2[r].x + s2[r].y;
   }
+  ok = ok && mbar_wait(s_done, 0, ctl);
 
-  // ---- chunk softmax per head: max, exponentials, sum (log2 domain) ----
-  float mx[MAXG] = {};
-#pragma unroll
-  for (int r = 0; r < MAXG; ++r) {
-    if (r < group) {
-      float m = valid ? s[r] : -INFINITY;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      if (lane == 0) red[warp * group + r] = m;
-    }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < MAXG; ++r) {
-    if (r < group) {
-      float m = red[r];
-#pragma unroll
-      for (int w = 1; w < kDecodeWarps; ++w) m = fmaxf(m, red[w * group + r]);
-      mx[r] = m;                                       // finite: the chunk has a valid key
-    }
-  }
-  __syncthreads();                                     // red is reused for the sums
-#pragma unroll
-  for (int r = 0; r < MAXG; ++r) {
-    if (r < group) {
-      const float p = valid ? ex2_approx(s[r] - mx[r]) : 0.f;
-      ps[r * kDecodeChunk + t] = p;
-      float l = p;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-      if (lane == 0) red[warp * group + r] = l;
-    }
-  }
-  __syncthreads();
-
-  // ---- P V: thread (subset ks, pair dp) sums the keys [ks * kPer, (ks + 1) * kPer) of
-  // the chunk for head-dim elements 2 dp and 2 dp + 1; the exponentials of four keys
-  // come in one 16-byte broadcast read ----
-  const int dp = t % kPairs, ks = t / kPairs;
-  float o0[MAXG], o1[MAXG];
-#pragma unroll
-  for (int r = 0; r < MAXG; ++r) o0[r] = o1[r] = 0.f;
-  cp_async_wait<0>();
-  __syncthreads();                                     // every thread's V pieces have landed
-  const uint32_t *vcol = reinterpret_cast<const uint32_t *>(vs) + dp;
-  constexpr int kPer = kDecodeChunk / kSubsets;        // contiguous keys per subset
-  const int k0 = ks * kPer;
-  const int kn = max(0, min(kPer, n_valid - k0));
-  const float *pk = ps + k0;
-  int jj = 0;
+  // ---- chunk softmax: thread t owns key key0 + 128 j + t of tile j ----
+  float x[L::kSub][G];
   {
-    float2 ae[MAXG], ao[MAXG];                         // even / odd head-dim element, key pairs
+    uint32_t sr[16 * L::kSub];
+    if (ok) {
+      tc_fence_after();
+      const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+      if constexpr (L::kSub == 1) {
+        tmem_ld_x16(tl, sr);
+      } else {
 #pragma unroll
-    for (int r = 0; r < MAXG; ++r) ae[r] = ao[r] = make_float2(0.f, 0.f);
-#pragma unroll(MAXG > 8 ? 1 : 2)
-    for (; jj + 4 <= kn; jj += 4) {
-      uint32_t vv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) vv[u] = vcol[(k0 + jj + u) * (kRow / 2)];
-      const float2 e01 = make_float2(bf16lo_to_f32(vv[0]), bf16lo_to_f32(vv[1]));
-      const float2 e23 = make_float2(bf16lo_to_f32(vv[2]), bf16lo_to_f32(vv[3]));
-      const float2 o01 = make_float2(bf16hi_to_f32(vv[0]), bf16hi_to_f32(vv[1]));
-      const float2 o23 = make_float2(bf16hi_to_f32(vv[2]), bf16hi_to_f32(vv[3]));
-#pragma unroll
-      for (int r = 0; r < MAXG; ++r) {
-        if (r < group) {
-          const float4 p4 = *reinterpret_cast<const float4 *>(pk + r * kDecodeChunk + jj);
-          const float2 p01 = make_float2(p4.x, p4.y), p23 = make_float2(p4.z, p4.w);
-          ae[r] = __ffma2_rn(p01, e01, ae[r]);
-          ae[r] = __ffma2_rn(p23, e23, ae[r]);
-          ao[r] = __ffma2_rn(p01, o01, ao[r]);
-          ao[r] = __ffma2_rn(p23, o23, ao[r]);
-        }
+        for (int c = 0; c < 16 * L::kSub; c += 32) tmem_ld_x32(tl + c, sr + c);
       }
+      tmem_wait_ld();
+      reg_fence<16 * L::kSub>(sr);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16 * L::kSub; ++i) sr[i] = 0u;
     }
 #pragma unroll
-    for (int r = 0; r < MAXG; ++r) {
-      o0[r] = ae[r].x + ae[r].y;
-      o1[r] = ao[r].x + ao[r].y;
-    }
+    for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+      for (int r = 0; r < G; ++r) x[j][r] = __uint_as_float(sr[16 * j + r]) * scale_log2;
   }
-  for (; jj < kn; ++jj) {
-    const uint32_t vv = vcol[(k0 + jj) * (kRow / 2)];
-    const float v0 = bf16lo_to_f32(vv), v1 = bf16hi_to_f32(vv);
+  bool valid[L::kSub];
 #pragma unroll
-    for (int r = 0; r < MAXG; ++r) {
-      if (r < group) {
-        const float p = pk[r * kDecodeChunk + jj];
-        o0[r] = fmaf(p, v0, o0[r]);
-        o1[r] = fmaf(p, v1, o1[r]);
-      }
-    }
-  }
+  for (int j = 0; j < L::kSub; ++j) valid[j] = key0 + j * kTileRows + t < T;
 #pragma unroll
-  for (int r = 0; r < MAXG; ++r) {
-    if (r < group) {
-      acc[(ks * group + r) * HD + 2 * dp] = o0[r];
-      acc[(ks * group + r) * HD + 2 * dp + 1] = o1[r];
-    }
+  for (int r = 0; r < G; ++r) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < L::kSub; ++j)
+      if (valid[j]) m = fmaxf(m, x[j][r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) red_max[warp * 16 + r] = m;
   }
   __syncthreads();
-
-  // ---- chunk result: (max, sum, partial O) per head of the group ----
-  const size_t rec = (static_cast<size_t>(bk) * chunks + chunk) * group;   // [B, nkv, chunks, group]
-  for (int e = t; e < group * HD; e += kDecodeThreads) {
-    const int r = e / HD, d = e % HD;
-    float a = 0.f;
-#pragma unroll 4
-    for (int q4 = 0; q4 < kSubsets; ++q4) a += acc[(q4 * group + r) * HD + d];
-    ws_o[(rec + r) * HD + d] = a;
-  }
-  if (t < group) {
+#pragma unroll
+  for (int r = 0; r < G; ++r) {
+    // finite for r < group: every chunk holds at least one key below T
+    const float M = fmaxf(fmaxf(red_max[r], red_max[16 + r]), fmaxf(red_max[32 + r], red_max[48 + r]));
     float l = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) l += red[w * group + t];
-    // mx[] lives in registers (compile-time indexed): pick this thread's head.
-    float m = 0.f;
+    for (int j = 0; j < L::kSub; ++j) {
+      const float p = (valid[j] && r < group) ? ex2_approx(x[j][r] - M) : 0.f;
+      const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+      l += __bfloat162float(pb);
+      // P^T row (j, r), key t: 64-key column t / 64, 16-byte chunk (t % 64) / 8 swizzled
+      const int n = j * G + r;
+      const uint32_t off = L::kQP + (t >> 6) * L::kPColBytes + n * 128 + (((((t & 63) >> 3) ^ (n & 7))) << 4) +
+                           (t & 7) * 2;
+      *reinterpret_cast<__nv_bfloat16 *>(smem + off) = pb;
+    }
 #pragma unroll
-    for (int r = 0; r < MAXG; ++r)
-      if (r == t) m = mx[r];
-    ws_ml[2 * (rec + t)] = m;
-    ws_ml[2 * (rec + t) + 1] = l;
+    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+    if (lane == 0) red_sum[warp * 16 + r] = l;
   }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // ---- P V: O^T (+)= [V tiles as M = 128 rows (j, d)] x [P^T, N = kSub x G] ----
+  if (warp == 0 && ok) {
+    ok = dec_warp_wait(full_v, 0, ctl);
+    if (ok) {
+      tc_fence_after();
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, L::kNpv, true, false);
+      // MN-major A: LBO = distance between 64-element atoms along M (the next tile, or
+      // the second sub-tile at hd = 128), SBO = 8 key rows; a K step is 16 key rows.
+      const uint64_t dV = smem_desc(sV, L::kSubBytes, 8 * L::kAtomBytes, L::kSwizzle);
+      const uint64_t dP = smem_desc(sQP, 16, 1024, kSwizzle128);
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kTileRows / 16; ++kk)
+          mma_ss(tmem + L::kTmemO, dV + kk * ((16 * L::kAtomBytes) >> 4),
+                 dP + (kk / 4) * (L::kPColBytes >> 4) + (kk % 4) * 2, idesc_pv, kk > 0 ? 1u : 0u);
+        mma_commit(o_done);
+      }
+      __syncwarp();
+      issued_o = true;
+    }
+  }
+  ok = ok && mbar_wait(o_done, 0, ctl);
+
+  // ---- epilogue: row m = 32 warp + lane of O^T is (tile j, element d) ----
+  float *acc = reinterpret_cast<float *>(smem + L::kK);   // [kSub][G][HD]; K is no longer read
+  if (ok) {
+    tc_fence_after();
+    const int m = warp * 32 + lane;
+    const int j = m / HD, d = m % HD;
+    uint32_t orow[G < 8 ? 8 : G];
+    const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + L::kTmemO + j * G;
+    if constexpr (G == 16) {
+      tmem_ld_x16(ta, orow);
+    } else {
+      tmem_ld_x8(ta, orow);
+    }
+    tmem_wait_ld();
+    reg_fence<(G < 8 ? 8 : G)>(orow);
+#pragma unroll
+    for (int r = 0; r < G; ++r) acc[(j * G + r) * HD + d] = __uint_as_float(orow[r]);
+  }
+  __syncthreads();
+  const size_t rec = (static_cast<size_t>(bk) * chunks + chunk) * group;   // [B, nkv, chunks, group]
+  if (ok) {
+    for (int e = t; e < group * HD; e += kDecThreads) {
+      const int r = e / HD, d = e % HD;
+      float a = 0.f;
+#pragma unroll
+      for (int j = 0; j < L::kSub; ++j) a += acc[(j * G + r) * HD + d];
+      ws_o[(rec + r) * HD + d] = a;
+    }
+    if (t < group) {
+      const float M = fmaxf(fmaxf(red_max[t], red_max[16 + t]), fmaxf(red_max[32 + t], red_max[48 + t]));
+      const float l = (red_sum[t] + red_sum[16 + t]) + (red_sum[32 + t] + red_sum[48 + t]);
+      ws_ml[2 * (rec + t)] = M;
+      ws_ml[2 * (rec + t) + 1] = l;
+    }
+  }
+
+  // ---- teardown: let copies and products in flight land, then free TMEM ----
+  if (warp == 0) {
+    mbar_drain(full_k, 0, ctl);
+    mbar_drain(full_v, 0, ctl);
+    if (issued_s) mbar_drain(s_done, 0, ctl);
+    if (issued_o) mbar_drain(o_done, 0, ctl);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, L::kTmemCols);
 }
 
 // One warp per (batch, query head): merge the chunks, write O (bf16) and the LSE. The
@@ -332,21 +392,20 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float *__rest
   if (lane == 0) lse[static_cast<size_t>(b) * nh + h] = (M + __log2f(L)) * kLn2;
 }
 
-template <int HD, int MAXG>
-cudaError_t launch_decode_hd(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
+template <int HD, int G>
+cudaError_t launch_decode_hd(const CUtensorMap &mk, const CUtensorMap &mv, const __nv_bfloat16 *q,
                              __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, float scale,
-                             void *workspace, cudaStream_t stream) {
-  const int group = nh / nkv;
-  const int chunks = (T + kDecodeChunk - 1) / kDecodeChunk;
+                             void *workspace, int *status, uint64_t timeout_ns, cudaStream_t stream) {
+  using L = DecLayout<HD, G>;
+  const int chunks = (T + L::kChunk - 1) / L::kChunk;
   float *ws_o = static_cast<float *>(workspace);
   float *ws_ml = ws_o + static_cast<size_t>(B) * nh * chunks * HD;
-  const size_t smem = decode_smem_bytes<HD>(group);
-  cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<HD, MAXG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L::kDynBytes));
   if (err != cudaSuccess) return err;
-  const dim3 grid1(static_cast<unsigned>(B * nkv), static_cast<unsigned>(chunks));
-  err = launch_pdl(decode_partial_kernel<HD, MAXG>, grid1, kDecodeThreads, smem, stream, q, k, v, ws_o, ws_ml, T,
-                   nh, nkv, scale * kLog2e);
+  const unsigned grid1 = static_cast<unsigned>(static_cast<long long>(B) * nkv * chunks);
+  err = launch_pdl(decode_partial_kernel<HD, G>, dim3(grid1), kDecThreads, L::kDynBytes, stream, mk, mv, q, ws_o,
+                   ws_ml, B, T, nh, nkv, scale * kLog2e, status, static_cast<unsigned long long>(timeout_ns));
   if (err != cudaSuccess) return err;
   const unsigned blocks = static_cast<unsigned>((static_cast<long long>(B) * nh * 32 + 127) / 128);
   return launch_pdl(decode_combine_kernel<HD>, blocks, 128, 0, stream, static_cast<const float *>(ws_o),
@@ -355,19 +414,24 @@ cudaError_t launch_decode_hd(const __nv_bfloat16 *q, const __nv_bfloat16 *k, con
 
 }  // namespace
 
-cudaError_t launch_decode_bf16(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
-                               __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, int hd,
-                               float scale, void *workspace, cudaStream_t stream) {
+cudaError_t launch_decode_bf16(const CUtensorMap &mk, const CUtensorMap &mv, const __nv_bfloat16 *q,
+                               __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, int hd, float scale,
+                               void *workspace, int *status, uint64_t timeout_ns, cudaStream_t stream) {
   const int group = nh / nkv;
   if (group > kMaxDecodeGroup) return cudaErrorInvalidValue;
-#define XATTN_DECODE_G(HD)                                                                              \
-  if (group <= 4) return launch_decode_hd<HD, 4>(q, k, v, o, lse, B, T, nh, nkv, scale, workspace, stream); \
-  if (group <= 8) return launch_decode_hd<HD, 8>(q, k, v, o, lse, B, T, nh, nkv, scale, workspace, stream); \
-  return launch_decode_hd<HD, 16>(q, k, v, o, lse, B, T, nh, nkv, scale, workspace, stream)
-  if (hd == 64) { XATTN_DECODE_G(64); }
-  if (hd == 32) { XATTN_DECODE_G(32); }
-  if (hd == 128) { XATTN_DECODE_G(128); }
-#undef XATTN_DECODE_G
+#define XATTN_DECODE(HD, G) \
+  return launch_decode_hd<HD, G>(mk, mv, q, o, lse, B, T, nh, nkv, scale, workspace, status, timeout_ns, stream)
+  if (hd == 32) {
+    if (group <= 4) XATTN_DECODE(32, 4);
+    if (group <= 8) XATTN_DECODE(32, 8);
+    XATTN_DECODE(32, 16);
+  }
+  if (hd == 64) {
+    if (group <= 8) XATTN_DECODE(64, 8);
+    XATTN_DECODE(64, 16);
+  }
+  if (hd == 128) XATTN_DECODE(128, 16);
+#undef XATTN_DECODE
   return cudaErrorInvalidValue;
 }
 

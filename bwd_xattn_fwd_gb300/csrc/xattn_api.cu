@@ -336,20 +336,23 @@ xattn_status xattn_decode(const void *q, const void *k_cache, const void *v_cach
   XATTN_TRY(check_shape(B, T, nh, nkv, hd, scale));
   if (nh / nkv > kMaxDecodeGroup) return XATTN_ERR_GROUP;
   if (hd != 32 && hd != 64 && hd != 128) return XATTN_ERR_UNSUPPORTED_HD;
-  // The chunk count is a grid dimension (at most 65535 256-key chunks).
-  if ((T + kDecodeChunk - 1) / kDecodeChunk > 65535) return XATTN_ERR_BAD_SHAPE;
+  // One CTA per (batch, kv head, chunk): the grid is one-dimensional.
+  const long long chunks = (static_cast<long long>(T) + decode_chunk_keys(hd) - 1) / decode_chunk_keys(hd);
+  if (static_cast<long long>(B) * nkv * chunks > 0x7fffffffLL) return XATTN_ERR_BAD_SHAPE;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
       (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return XATTN_ERR_MISALIGNED;
   DeviceInfo *dev = nullptr;
   XATTN_TRY(bf16_device(&dev));
+  CUtensorMap mk, mv;
+  XATTN_TRY(make_map(&mk, k_cache, B, T, nkv, hd));
+  XATTN_TRY(make_map(&mv, v_cache, B, T, nkv, hd));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   void *ws = nullptr;
   if (cudaMallocAsync(&ws, decode_workspace_bytes(B, T, nh, hd), st) != cudaSuccess) return XATTN_ERR_CUDA;
-  xattn_status r = cuda_status(launch_decode_bf16(
-      static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k_cache),
-      static_cast<const __nv_bfloat16 *>(v_cache), static_cast<__nv_bfloat16 *>(o), lse, B, T, nh, nkv, hd,
-      scale, ws, st));
+  xattn_status r = cuda_status(launch_decode_bf16(mk, mv, static_cast<const __nv_bfloat16 *>(q),
+                                                  static_cast<__nv_bfloat16 *>(o), lse, B, T, nh, nkv, hd, scale, ws,
+                                                  dev->status, wait_limit_ns(), st));
   const cudaError_t fe = cudaFreeAsync(ws, st);
   if (r == XATTN_OK && fe != cudaSuccess) r = XATTN_ERR_CUDA;
   return r;

@@ -97,14 +97,16 @@ cudaError_t launch_bwd_dq_bf16(const CUtensorMap &mq, const CUtensorMap &mk, con
                                int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // Decode (one query per sequence against its T cached keys/values), bf16, hd in
-// {32, 64, 128}, group = nh / nkv <= kMaxDecodeGroup. The workspace holds each 256-key
-// chunk's (max, sum, partial O) per query head: decode_workspace_bytes() bytes.
-constexpr int kDecodeChunk = 256;
+// {32, 64, 128}, group = nh / nkv <= kMaxDecodeGroup. mk, mv: maps over the caches as
+// make_map builds them for [B, T, nkv, hd]. A chunk is decode_chunk_keys(hd) keys (32 KB
+// of K); the workspace holds each chunk's (max, sum, partial O) per query head:
+// decode_workspace_bytes() bytes.
 constexpr int kMaxDecodeGroup = 16;
+int decode_chunk_keys(int hd);
 size_t decode_workspace_bytes(int B, int T, int nh, int hd);
-cudaError_t launch_decode_bf16(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_bfloat16 *v,
-                               __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, int hd,
-                               float scale, void *workspace, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const CUtensorMap &mk, const CUtensorMap &mv, const __nv_bfloat16 *q,
+                               __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, int hd, float scale,
+                               void *workspace, int *status, uint64_t timeout_ns, cudaStream_t stream);
 
 // fp32 CUDA-core path (hd <= 128).
 cudaError_t launch_fwd_f32(const float *q, const float *k, const float *v, float *o, float *lse,

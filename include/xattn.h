@@ -216,13 +216,16 @@ xattn_status xattn_bwd_f32(const float *q, const float *k, const float *v, const
  *   o      [B, nh, hd]      bf16 out;  lse [B, nh] float out (natural log of the sum of
  *                           exp of the scaled scores, as xattn_fwd's lse)
  * Query head h reads kv head h / (nh / nkv). hd in {32, 64, 128}; nh / nkv <= 16
- * (else XATTN_ERR_GROUP); 1 <= T <= 65535 * 256; any finite scale. q, k, v, o 16-byte
+ * (else XATTN_ERR_GROUP); T >= 1 with B * nkv * ceil(T / C) < 2^31, C = 16384 / hd
+ * keys per chunk (else XATTN_ERR_BAD_SHAPE); any finite scale. q, k, v, o 16-byte
  * aligned, lse 4-byte aligned.
- * Arithmetic: fp32 products and softmax statistics on bf16 inputs; o rounded to nearest
- * even. Scratch (B * nh * ceil(T / 256) * (hd + 2) floats: per 256-key chunk the
- * maximum, sum and unnormalised output of each query head) is taken with
- * cudaMallocAsync on `stream` and released with cudaFreeAsync; nothing else is
- * allocated. The result is bit-for-bit reproducible (fixed reduction order).
+ * Arithmetic: tensor-core products on the bf16 inputs with fp32 accumulation (the
+ * scores q . k, and the sum over keys of p v with the probabilities p rounded to bf16,
+ * as in xattn_fwd); softmax statistics in fp32; o rounded to nearest even. Scratch
+ * (B * nh * ceil(T / C) * (hd + 2) floats: per C-key chunk the maximum, sum and
+ * unnormalised output of each query head) is taken with cudaMallocAsync on `stream` and
+ * released with cudaFreeAsync; nothing else is allocated. The result is bit-for-bit
+ * reproducible (fixed reduction order).
  */
 xattn_status xattn_decode(const void *q, const void *k_cache, const void *v_cache, int B, int T,
                           int nh, int nkv, int hd, float scale, void *o, float *lse, void *stream);

@@ -39,8 +39,9 @@ def _check(x, scale, label, sel=slice(None)):
 
 
 SHAPES = [
-    # (B, T, nh, nkv, hd): one key; chunk edges 255/256/257; long caches; groups 1..16;
-    # head dims 32, 64, 128
+    # (B, T, nh, nkv, hd): one key; chunk and tile edges (chunks of 512, 256, 128 keys at
+    # hd 32, 64, 128; last chunks with tiles wholly past T); long caches; groups 1..16
+    # (each padded width of the query tile at each head dim); head dims 32, 64, 128
     (1, 1, 2, 1, 64),
     (3, 255, 8, 2, 64),
     (2, 256, 4, 4, 32),
@@ -49,6 +50,8 @@ SHAPES = [
     (2, 777, 32, 2, 64),
     (4, 2049, 8, 1, 32),
     (1, 5000, 4, 2, 128),
+    (2, 600, 16, 1, 32),
+    (2, 1300, 16, 2, 64),
 ]
 
 
