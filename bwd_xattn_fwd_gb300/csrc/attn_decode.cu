@@ -128,16 +128,29 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
 
+  // Thread 0 starts the chunk's loads first (K tiles, then V tiles, one barrier each);
+  // the TMEM allocation and the query tile follow while they are in flight.
   if (t == 0) {
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8u * i, 1);
     fence_mbar_init();
+    grid_dep_wait();
+    XATTN_DCHECK(b < B && kvh < nkv && key0 < T, status);
+    mbar_expect_tx(full_k, L::kKVBytes);
+#pragma unroll
+    for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+      for (int c = 0; c < L::kSubTiles; ++c)
+        tma_load_4d(sK + j * L::kTileBytes + c * L::kSubBytes, &mk, full_k, c * 64, kvh, key0 + j * kTileRows, b);
+    mbar_expect_tx(full_v, L::kKVBytes);
+#pragma unroll
+    for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+      for (int c = 0; c < L::kSubTiles; ++c)
+        tma_load_4d(sV + j * L::kTileBytes + c * L::kSubBytes, &mv, full_v, c * 64, kvh, key0 + j * kTileRows, b);
   }
   if (warp == 0) {
-    if (lane == 0) {
-      tma_prefetch_desc(&mk);
-      tma_prefetch_desc(&mv);
-    }
+    __syncwarp();
     tmem_alloc(smem_u32(tmem_holder), L::kTmemCols);
     tmem_relinquish();
   }
@@ -148,24 +161,6 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
   grid_dep_wait();
   const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_holder, 0);
 
-  // ---- loads: the chunk's K tiles, then its V tiles (one barrier each) ----
-  if (warp == 0) {
-    XATTN_DCHECK(b < B && kvh < nkv && key0 < T, status);
-    mbar_expect_tx_elect(full_k, L::kKVBytes);
-#pragma unroll
-    for (int j = 0; j < L::kSub; ++j)
-#pragma unroll
-      for (int c = 0; c < L::kSubTiles; ++c)
-        tma_load_4d_elect(sK + j * L::kTileBytes + c * L::kSubBytes, &mk, full_k, c * 64, kvh,
-                          key0 + j * kTileRows, b);
-    mbar_expect_tx_elect(full_v, L::kKVBytes);
-#pragma unroll
-    for (int j = 0; j < L::kSub; ++j)
-#pragma unroll
-      for (int c = 0; c < L::kSubTiles; ++c)
-        tma_load_4d_elect(sV + j * L::kTileBytes + c * L::kSubBytes, &mv, full_v, c * 64, kvh,
-                          key0 + j * kTileRows, b);
-  }
   // ---- the query tile: rows r < group are query heads kvh * group + r, the rest zero ----
   {
     constexpr int kPieces = HD / 8;                              // 16-byte pieces per row
