@@ -100,7 +100,10 @@ __device__ __forceinline__ bool dec_warp_wait(uint32_t bar, uint32_t parity, con
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int HD, int G>
+// GV: heads computed (the group rounded up to 4, 8 or 16; GV <= G). Heads GV..G-1 only pad
+// the operand tiles: their scores are not reduced and their P^T rows are not written (they
+// reach O^T columns that nothing reads).
+template <int HD, int G, int GV>
 __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
     const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o, float *__restrict__ ws_ml, int B, int T,
@@ -207,7 +210,8 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
   ok = ok && mbar_wait(s_done, 0, ctl);
 
   // ---- chunk softmax: thread t owns key key0 + 128 j + t of tile j ----
-  float x[L::kSub][G];
+  static_assert(GV <= G, "computed heads within the padded tile");
+  float x[L::kSub][GV];
   {
     uint32_t sr[16 * L::kSub];
     if (ok) {
@@ -228,13 +232,13 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
 #pragma unroll
     for (int j = 0; j < L::kSub; ++j)
 #pragma unroll
-      for (int r = 0; r < G; ++r) x[j][r] = __uint_as_float(sr[16 * j + r]) * scale_log2;
+      for (int r = 0; r < GV; ++r) x[j][r] = __uint_as_float(sr[16 * j + r]) * scale_log2;
   }
   bool valid[L::kSub];
 #pragma unroll
   for (int j = 0; j < L::kSub; ++j) valid[j] = key0 + j * kTileRows + t < T;
 #pragma unroll
-  for (int r = 0; r < G; ++r) {
+  for (int r = 0; r < GV; ++r) {
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < L::kSub; ++j)
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
   }
   __syncthreads();
 #pragma unroll
-  for (int r = 0; r < G; ++r) {
+  for (int r = 0; r < GV; ++r) {
     // finite for r < group: every chunk holds at least one key below T
     const float M = fmaxf(fmaxf(red_max[r], red_max[16 + r]), fmaxf(red_max[32 + r], red_max[48 + r]));
     float l = 0.f;
@@ -296,17 +300,17 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
     tc_fence_after();
     const int m = warp * 32 + lane;
     const int j = m / HD, d = m % HD;
-    uint32_t orow[G < 8 ? 8 : G];
+    uint32_t orow[GV < 8 ? 8 : GV];
     const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + L::kTmemO + j * G;
-    if constexpr (G == 16) {
+    if constexpr (GV == 16) {
       tmem_ld_x16(ta, orow);
     } else {
       tmem_ld_x8(ta, orow);
     }
     tmem_wait_ld();
-    reg_fence<(G < 8 ? 8 : G)>(orow);
+    reg_fence<(GV < 8 ? 8 : GV)>(orow);
 #pragma unroll
-    for (int r = 0; r < G; ++r) acc[(j * G + r) * HD + d] = __uint_as_float(orow[r]);
+    for (int r = 0; r < GV; ++r) acc[(j * G + r) * HD + d] = __uint_as_float(orow[r]);
   }
   __syncthreads();
   const size_t rec = (static_cast<size_t>(bk) * chunks + chunk) * group;   // [B, nkv, chunks, group]
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(128) decode_combine_kernel(const float *__rest
   if (lane == 0) lse[static_cast<size_t>(b) * nh + h] = (M + __log2f(L)) * kLn2;
 }
 
-template <int HD, int G>
+template <int HD, int G, int GV>
 cudaError_t launch_decode_hd(const CUtensorMap &mk, const CUtensorMap &mv, const __nv_bfloat16 *q,
                              __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, float scale,
                              void *workspace, int *status, uint64_t timeout_ns, cudaStream_t stream) {
@@ -395,11 +399,11 @@ cudaError_t launch_decode_hd(const CUtensorMap &mk, const CUtensorMap &mv, const
   const int chunks = (T + L::kChunk - 1) / L::kChunk;
   float *ws_o = static_cast<float *>(workspace);
   float *ws_ml = ws_o + static_cast<size_t>(B) * nh * chunks * HD;
-  cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<HD, G, GV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(L::kDynBytes));
   if (err != cudaSuccess) return err;
   const unsigned grid1 = static_cast<unsigned>(static_cast<long long>(B) * nkv * chunks);
-  err = launch_pdl(decode_partial_kernel<HD, G>, dim3(grid1), kDecThreads, L::kDynBytes, stream, mk, mv, q, ws_o,
+  err = launch_pdl(decode_partial_kernel<HD, G, GV>, dim3(grid1), kDecThreads, L::kDynBytes, stream, mk, mv, q, ws_o,
                    ws_ml, B, T, nh, nkv, scale * kLog2e, status, static_cast<unsigned long long>(timeout_ns));
   if (err != cudaSuccess) return err;
   const unsigned blocks = static_cast<unsigned>((static_cast<long long>(B) * nh * 32 + 127) / 128);
@@ -414,18 +418,25 @@ cudaError_t launch_decode_bf16(const CUtensorMap &mk, const CUtensorMap &mv, con
                                void *workspace, int *status, uint64_t timeout_ns, cudaStream_t stream) {
   const int group = nh / nkv;
   if (group > kMaxDecodeGroup) return cudaErrorInvalidValue;
-#define XATTN_DECODE(HD, G) \
-  return launch_decode_hd<HD, G>(mk, mv, q, o, lse, B, T, nh, nkv, scale, workspace, status, timeout_ns, stream)
+  // G: the padded width of the query and P^T tiles (at least 16 / (128 / hd) so that P V
+  // has N a multiple of 16); GV: the heads computed.
+#define XATTN_DECODE(HD, G, GV) \
+  return launch_decode_hd<HD, G, GV>(mk, mv, q, o, lse, B, T, nh, nkv, scale, workspace, status, timeout_ns, stream)
   if (hd == 32) {
-    if (group <= 4) XATTN_DECODE(32, 4);
-    if (group <= 8) XATTN_DECODE(32, 8);
-    XATTN_DECODE(32, 16);
+    if (group <= 4) XATTN_DECODE(32, 4, 4);
+    if (group <= 8) XATTN_DECODE(32, 8, 8);
+    XATTN_DECODE(32, 16, 16);
   }
   if (hd == 64) {
-    if (group <= 8) XATTN_DECODE(64, 8);
-    XATTN_DECODE(64, 16);
+    if (group <= 4) XATTN_DECODE(64, 8, 4);
+    if (group <= 8) XATTN_DECODE(64, 8, 8);
+    XATTN_DECODE(64, 16, 16);
   }
-  if (hd == 128) XATTN_DECODE(128, 16);
+  if (hd == 128) {
+    if (group <= 4) XATTN_DECODE(128, 16, 4);
+    if (group <= 8) XATTN_DECODE(128, 16, 8);
+    XATTN_DECODE(128, 16, 16);
+  }
 #undef XATTN_DECODE
   return cudaErrorInvalidValue;
 }
