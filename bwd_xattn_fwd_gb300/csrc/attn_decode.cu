@@ -175,7 +175,9 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
       if (n < group) val = *reinterpret_cast<const uint4 *>(qg + n * HD + 8 * pc);
       const int col = pc / kAtomPieces, ch = pc % kAtomPieces;
       const int sw = L::kAtomBytes == 128 ? (ch ^ (n & 7)) : (ch ^ ((n >> 1) & 3));
-      *reinterpret_cast<uint4 *>(smem + L::kQP + col * L::kQColBytes + n * L::kAtomBytes + (sw << 4)) = val;
+      const uint32_t qoff = col * L::kQColBytes + n * L::kAtomBytes + (sw << 4);
+      XATTN_DCHECK(qoff + 16 <= L::kQBytes, status);
+      *reinterpret_cast<uint4 *>(smem + L::kQP + qoff) = val;
     }
     fence_proxy_async_smem();
   }
@@ -262,6 +264,7 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
       const int n = j * G + r;
       const uint32_t off = L::kQP + (t >> 6) * L::kPColBytes + n * 128 + (((((t & 63) >> 3) ^ (n & 7))) << 4) +
                            (t & 7) * 2;
+      XATTN_DCHECK(off + 2 <= L::kQP + L::kPBytes, status);
       *reinterpret_cast<__nv_bfloat16 *>(smem + off) = pb;
     }
 #pragma unroll
@@ -309,6 +312,7 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
     }
     tmem_wait_ld();
     reg_fence<(GV < 8 ? 8 : GV)>(orow);
+    XATTN_DCHECK(((j + 1) * G) * HD <= L::kSub * G * HD && d < HD, status);
 #pragma unroll
     for (int r = 0; r < GV; ++r) acc[(j * G + r) * HD + d] = __uint_as_float(orow[r]);
   }
@@ -320,6 +324,7 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
       float a = 0.f;
 #pragma unroll
       for (int j = 0; j < L::kSub; ++j) a += acc[(j * G + r) * HD + d];
+      XATTN_DCHECK((rec + r + 1) * HD <= static_cast<size_t>(B) * nh * chunks * HD, status);
       ws_o[(rec + r) * HD + d] = a;
     }
     if (t < group) {

@@ -5,8 +5,9 @@ the GPU, in a child process that loads it in place of the release library:
   * its self-test's failing check is reported, once, and cleared by the read;
   * the attention path on edge shapes -- the fused-dQ backward with query groups and with
     one head per kv head, the deterministic backward (query-stationary and resident dQ),
-    hd 32, 64 and 128, ragged last tiles, several units per CTA -- passes every check
-    (the status word stays clear) and matches the oracle."""
+    hd 32, 64 and 128, ragged last tiles, several units per CTA -- and the decode kernels
+    (ragged last chunks, padded groups, hd 32, 64 and 128) pass every check (the status
+    word stays clear) and match the oracle."""
 import os
 import subprocess
 import sys
@@ -44,6 +45,19 @@ for shape, det in CASES:
     x = W.make_inputs(w, seed=5)
     out = run_gpu(w, x, deterministic=det)   # asserts that the status word is clear
     compare(out, oracle_full(w, x), "bf16", str(shape))
+# decode: ragged last chunks with tiles wholly past T, padded groups, hd 32 / 64 / 128
+import numpy as np
+import oracle
+import torch
+from gpu_path import TOL_BF16, TOL_LSE, rel_err
+for B, T, nh, nkv, hd in [(3, 777, 8, 2, 64), (2, 2049, 8, 1, 32), (2, 300, 16, 4, 128)]:
+    w = W.DecodeWorkload("debug", B=B, T=T, nh=nh, nkv=nkv, hd=hd)
+    x = W.make_decode_inputs(w, seed=7)
+    o, lse = xattn.attention_decode(*(x[n].cuda() for n in ("q", "k", "v")), w.scale)
+    torch.cuda.synchronize()
+    assert xattn.xattn_check_device_status() == 0, (B, T, nh, nkv, hd)
+    ro, rl = oracle.default().decode(*(W.as_f64(x[n]) for n in ("q", "k", "v")), w.scale)
+    assert rel_err(W.as_f64(o), ro) <= TOL_BF16 and float(np.abs(W.as_f64(lse) - rl).max()) <= TOL_LSE
 print("debug build ok")
 """
 
