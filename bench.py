@@ -706,6 +706,9 @@ def run_decode(args, w):
     total_ms = max_over_ranks(pg, e0.elapsed_time(e1), dev)
     ms = total_ms / args.steps
     value = w.io_bytes * world * args.steps / (total_ms * 1e-3) / 1e9
+    # one kernel when each (sequence, kv head) is one run, else the partial kernel and the combine
+    runs = xattn.xattn_decode_runs(B, T, nh, nkv, hd, torch.cuda.get_device_properties(dev).multi_processor_count)
+    launches_per_step = 1 if runs == 1 else 2
     pk = peaks()
     roofline = {"kernel": "decode_partial_kernel + decode_combine_kernel", "bound": "hbm",
                 "achieved": value / world, "peak": pk["gbs"], "unit": "GB/s",
@@ -760,7 +763,7 @@ def run_decode(args, w):
                            "l2": "no flush: each step reads caches of %.0f MB (> L2), alternating "
                                  "between two copies" % (w.cache_bytes / 1e6)},
                 "tok_per_s": B * world / (ms * 1e-3), "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 2 * args.steps, "clocks": clk.summary()}
+                "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary()}
         print(json.dumps(line), flush=True)
     if pg is not None:
         pg.destroy_process_group()

@@ -11,14 +11,17 @@
 // GB300 mapping. Per (sequence, kv head) the work is two thin products against the
 // cache -- S^T = K q^T (keys x the group's query heads) and O^T = V^T P^T -- so it is bound
 // by HBM reading the cache once. Both products run on the tensor cores (tcgen05, fp32
-// accumulators in TMEM), which leaves the CUDA cores only the softmax of a chunk:
-//   1. decode_partial_kernel: one CTA of 4 warps per (batch, kv head, chunk of C keys),
-//      C = 16384 / hd (512, 256, 128 keys at hd = 32, 64, 128), so that a chunk's K and its
-//      V are 32 KB each (three CTAs share an SM).
-//      * Loads: one elected thread issues TMA loads of the chunk's C/128 K tiles and V
-//        tiles (128-key boxes of one kv head, swizzled like the training kernels' tiles;
-//        keys past T read as zeros); the threads write the group's query rows, padded to
-//        16 rows with zeros, as a K-major operand tile.
+// accumulators in TMEM), which leaves the CUDA cores only the softmax of a chunk.
+//   1. decode_partial_kernel: one CTA of 4 warps per (sequence, kv head, run of chunks),
+//      a chunk being C = 16384 / hd keys (512, 256, 128 at hd = 32, 64, 128), so its K and
+//      its V are 32 KB each (three CTAs share an SM). A (sequence, kv head) is one run
+//      when the B x nkv pairs fill the SMs in one wave of resident CTAs; shorter batches
+//      split it into more runs (decode_nsplit).
+//      * Loads: one K and one V buffer. Thread 0 issues the run's first TMA loads before
+//        anything else (128-key boxes of one kv head, swizzled like the training
+//        kernels' tiles; keys past T read as zeros); the next chunk's K loads as soon as
+//        this chunk's scores are done, its V as soon as this chunk's P V is done. The
+//        threads write the group's query rows, padded to 16 rows, as a K-major tile.
 //      * Scores: per 128-key tile, S^T = K q^T (M = 128 keys, N = 16, K = hd) into TMEM.
 //      * Softmax: thread i owns key i of every tile (its TMEM lane). The chunk maximum
 //        and sum of each head (fp32, log2 domain) are reduced over the CTA; P^T goes to
@@ -30,10 +33,13 @@
 //        B = P^T with N = (C/128) x G columns (tile j', head r). The blocks j = j' are the
 //        tiles' partial outputs; the others are discarded (the products are tiny next to
 //        the loads).
-//      * Epilogue: thread (tile j, d) reads its block's head columns, the tiles are summed
-//        through shared memory, and the chunk writes (max, sum, partial O) per head.
-//   2. decode_combine_kernel: one warp per (batch, query head) merges the chunks
-//      (rescaling each by 2^(m_c - M)), writes O in bf16 and LSE = (M + log2 L) ln 2.
+//      * Merge: thread (tile j, d) reads its block's head columns and folds the chunk into
+//        its running output, rescaled by 2^(M_old - M_new) as the run's maximum grows.
+//      * End of the run: the tiles' partials are summed through shared memory; a whole
+//        sequence writes O (bf16) and LSE = (M + log2 L) ln 2, a part of one writes
+//        (M, L, partial O) per head to the scratch.
+//   2. decode_combine_kernel (runs > 1 only): one warp per (sequence, query head) merges
+//      the runs (rescaling each by 2^(m_r - M)), writes O in bf16 and the LSE.
 #include "sm103_ptx.cuh"
 #include "xattn_internal.h"
 
@@ -50,6 +56,34 @@ size_t decode_workspace_bytes(int B, int T, int nh, int hd) {
 namespace {
 
 constexpr int kDecThreads = 128;   // one thread per key of a 128-key tile (TMEM lane)
+
+// Key runs per (batch, kv head) for bk pairs of `chunks` chunks and `slots` resident CTAs
+// on `sms` SMs:
+//  * bk >= sms and bk <= slots: one run each (every CTA resident at once, streaming its
+//    whole cache; no combine);
+//  * bk < sms: as many runs as fill one wave of CTAs (the parallelism a short batch lacks);
+//  * bk > slots: the count that minimises (waves of CTAs) x (chunks per CTA, the length of
+//    a CTA's chain), a split costing about one chunk more for its combine.
+// Every run is non-empty.
+int decode_nsplit(int bk, int chunks, int slots, int sms) {
+  auto fit = [chunks](int s) {   // largest count <= s whose runs are all non-empty
+    s = s < 1 ? 1 : (s > chunks ? chunks : s);
+    while (s > 1 && (s - 1) * ((chunks + s - 1) / s) >= chunks) --s;
+    return s;
+  };
+  if (bk <= slots) return bk >= sms ? 1 : fit(slots / bk);
+  int best = 1;
+  long long best_cost = -1;
+  const int top = chunks < 4096 ? chunks : 4096;
+  for (int s = 1; s <= top; ++s) {
+    if (fit(s) != s) continue;
+    const int per = (chunks + s - 1) / s;
+    const long long waves = (static_cast<long long>(bk) * s + slots - 1) / slots;
+    const long long cost = waves * per + (s > 1 ? 1 : 0);
+    if (best_cost < 0 || cost < best_cost) best = s, best_cost = cost;
+  }
+  return best;
+}
 
 // Shared memory and TMEM of one CTA; G = the group padded to 4, 8 or 16 (at least
 // 16 / kSub, so that P V has N a multiple of 16).
@@ -80,7 +114,7 @@ struct DecLayout {
   static constexpr uint32_t kK = 0;
   static constexpr uint32_t kV = kKVBytes;
   static constexpr uint32_t kQP = 2 * kKVBytes;
-  static constexpr uint32_t kRed = kQP + (kPBytes > kQBytes ? kPBytes : kQBytes);
+  static constexpr uint32_t kRed = kQP + (kQBytes + 1023) / 1024 * 1024 + kPBytes;
   static constexpr uint32_t kBars = kRed + 2 * 4 * 16 * 4;
   static constexpr uint32_t kMisc = kBars + 4 * 8;
   static constexpr uint32_t kUsed = kMisc + 32;
@@ -94,21 +128,38 @@ struct DecLayout {
   static_assert(3 * (kDynBytes + 1024) <= 228 * 1024 || G == 16, "three CTAs per SM");
 };
 
+// Resident CTAs per SM: shared memory (228 KB, 1 KB reserved per CTA), at most three
+// (the launch bounds' register budget).
+template <int HD, int G>
+constexpr int decode_ctas_per_sm() {
+  constexpr int n = static_cast<int>((228u * 1024u) / (DecLayout<HD, G>::kDynBytes + 1024u));
+  return n < 3 ? n : 3;
+}
+
 // Warp-uniform bounded wait: every lane waits, then all agree.
 __device__ __forceinline__ bool dec_warp_wait(uint32_t bar, uint32_t parity, const WaitCtl &ctl) {
   const bool ok = mbar_wait(bar, parity, ctl);
   return __all_sync(0xffffffffu, ok);
 }
 
+// A CTA takes one (batch, kv head) and a contiguous run of its chunks [c0, c1): the run's
+// chunks stream through one K and one V buffer (the next chunk's K loads as soon as this
+// chunk's scores are done, its V as soon as this chunk's P V is done), and the chunks are
+// merged online: per head a running maximum M and sum L, and per thread (tile j, element
+// d) the partial outputs of its O^T row, rescaled by 2^(M_old - M_new) as M grows.
+// Whole sequences in one run (nsplit == 1) end with O (bf16) and the LSE; otherwise each
+// run writes a record (M, L, partial O) per head, merged by decode_combine_kernel.
 // GV: heads computed (the group rounded up to 4, 8 or 16; GV <= G). Heads GV..G-1 only pad
 // the operand tiles: their scores are not reduced and their P^T rows are not written (they
 // reach O^T columns that nothing reads).
 template <int HD, int G, int GV>
 __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
     const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-    const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o, float *__restrict__ ws_ml, int B, int T,
-    int nh, int nkv, float scale_log2, int *status, unsigned long long timeout_ns) {
+    const __nv_bfloat16 *__restrict__ q, float *__restrict__ ws_o, float *__restrict__ ws_ml,
+    __nv_bfloat16 *__restrict__ o, float *__restrict__ lse, int B, int T, int nh, int nkv, int nsplit,
+    float scale_log2, int *status, unsigned long long timeout_ns) {
   using L = DecLayout<HD, G>;
+  static_assert(GV <= G, "computed heads within the padded tile");
   extern __shared__ uint8_t dsm_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(dsm_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -117,10 +168,11 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
   const int group = nh / nkv;
   const int BK = B * nkv;
   const int bk = static_cast<int>(blockIdx.x % static_cast<unsigned>(BK));
-  const int chunk = static_cast<int>(blockIdx.x / static_cast<unsigned>(BK));
-  const int chunks = static_cast<int>(gridDim.x / static_cast<unsigned>(BK));
+  const int split = static_cast<int>(blockIdx.x / static_cast<unsigned>(BK));
   const int b = bk / nkv, kvh = bk % nkv;
-  const int key0 = chunk * L::kChunk;
+  const int chunks = (T + L::kChunk - 1) / L::kChunk;
+  const int per = (chunks + nsplit - 1) / nsplit;
+  const int c0 = split * per, c1 = min(chunks, c0 + per);    // c0 < c1 (the host picks nsplit)
 
   const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV), sQP = smem_u32(smem + L::kQP);
   float *red_max = reinterpret_cast<float *>(smem + L::kRed);   // [4][16]
@@ -131,26 +183,26 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kMisc + 16);
   const WaitCtl ctl{abort_flag, status, timeout_ns};
 
-  // Thread 0 starts the chunk's loads first (K tiles, then V tiles, one barrier each);
-  // the TMEM allocation and the query tile follow while they are in flight.
+  // Loads of chunk c's K tiles (or V tiles) into the K (V) buffer, by thread 0.
+  auto load_kv = [&](const CUtensorMap *map, uint32_t dst, uint32_t bar, int c) {
+    XATTN_DCHECK(b < B && kvh < nkv && c < chunks, status);
+    mbar_expect_tx(bar, L::kKVBytes);
+#pragma unroll
+    for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+      for (int sub = 0; sub < L::kSubTiles; ++sub)
+        tma_load_4d(dst + j * L::kTileBytes + sub * L::kSubBytes, map, bar, sub * 64, kvh,
+                    c * L::kChunk + j * kTileRows, b);
+  };
+  // Thread 0 starts the first chunk's loads first; the TMEM allocation and the query tile
+  // follow while they are in flight.
   if (t == 0) {
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) mbar_init(bar0 + 8u * i, 1);
     fence_mbar_init();
     grid_dep_wait();
-    XATTN_DCHECK(b < B && kvh < nkv && key0 < T, status);
-    mbar_expect_tx(full_k, L::kKVBytes);
-#pragma unroll
-    for (int j = 0; j < L::kSub; ++j)
-#pragma unroll
-      for (int c = 0; c < L::kSubTiles; ++c)
-        tma_load_4d(sK + j * L::kTileBytes + c * L::kSubBytes, &mk, full_k, c * 64, kvh, key0 + j * kTileRows, b);
-    mbar_expect_tx(full_v, L::kKVBytes);
-#pragma unroll
-    for (int j = 0; j < L::kSub; ++j)
-#pragma unroll
-      for (int c = 0; c < L::kSubTiles; ++c)
-        tma_load_4d(sV + j * L::kTileBytes + c * L::kSubBytes, &mv, full_v, c * 64, kvh, key0 + j * kTileRows, b);
+    load_kv(&mk, sK, full_k, c0);
+    load_kv(&mv, sV, full_v, c0);
   }
   if (warp == 0) {
     __syncwarp();
@@ -183,164 +235,217 @@ __global__ void __launch_bounds__(kDecThreads, 3) decode_partial_kernel(
   }
   __syncthreads();
 
-  // ---- scores S^T = K q^T, one M = 128, N = 16 product per tile ----
-  bool ok = true, issued_s = false, issued_o = false;
-  if (warp == 0) {
-    ok = dec_warp_wait(full_k, 0, ctl);
-    if (ok) {
-      tc_fence_after();
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16, false, false);
-      const uint64_t dK = smem_desc(sK, 16, 8 * L::kAtomBytes, L::kSwizzle);
-      const uint64_t dQ = smem_desc(sQP, 16, 8 * L::kAtomBytes, L::kSwizzle);
-      if (elect_one()) {
+  // The query tile stays in [kQP, kQP + kQBytes); P^T goes after it.
+  constexpr uint32_t kPOff = (L::kQBytes + 1023) / 1024 * 1024;
+  static_assert(L::kQP + kPOff + L::kPBytes <= L::kRed, "query tile and P^T both fit");
+  const uint32_t sP = sQP + kPOff;
+  constexpr uint32_t idesc_s = idesc_bf16_f32(128, 16, false, false);
+  constexpr uint32_t idesc_pv = idesc_bf16_f32(128, L::kNpv, true, false);
+  // thread t's O^T row: (tile j, element d)
+  const int m = warp * 32 + lane, jrow = m / HD, drow = m % HD;
+  float Mh[GV], Lh[GV], acc[GV];   // running max / sum per head (every thread), partial outputs
 #pragma unroll
-        for (int j = 0; j < L::kSub; ++j)
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk) {
-            // a K step of 16 elements is +32 bytes within a swizzled row; the fifth step
-            // starts the second 64-column atom (hd = 128)
-            const uint32_t kstep = (kk % 4) * 2;
-            mma_ss(tmem + 16u * j, dK + j * (L::kTileBytes >> 4) + (kk / 4) * (L::kSubBytes >> 4) + kstep,
-                   dQ + (kk / 4) * (L::kQColBytes >> 4) + kstep, idesc_s, kk > 0 ? 1u : 0u);
-          }
-        mma_commit(s_done);
-      }
-      __syncwarp();
-      issued_s = true;
-    }
-  }
-  ok = ok && mbar_wait(s_done, 0, ctl);
+  for (int r = 0; r < GV; ++r) Mh[r] = -INFINITY, Lh[r] = 0.f, acc[r] = 0.f;
 
-  // ---- chunk softmax: thread t owns key key0 + 128 j + t of tile j ----
-  static_assert(GV <= G, "computed heads within the padded tile");
-  float x[L::kSub][GV];
-  {
-    uint32_t sr[16 * L::kSub];
-    if (ok) {
+  bool ok = true;
+  int last_s = -1, last_o = -1, k_loaded = c0 + 1, v_loaded = c0 + 1;   // chunks whose loads were issued
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    const uint32_t par = static_cast<uint32_t>((c - c0) & 1);
+    const int key0 = c * L::kChunk;
+    // ---- scores S^T = K q^T, one M = 128, N = 16 product per tile ----
+    if (warp == 0) {
+      ok = ok && dec_warp_wait(full_k, par, ctl);
+      if (ok) {
+        tc_fence_after();
+        const uint64_t dK = smem_desc(sK, 16, 8 * L::kAtomBytes, L::kSwizzle);
+        const uint64_t dQ = smem_desc(sQP, 16, 8 * L::kAtomBytes, L::kSwizzle);
+        if (elect_one()) {
+#pragma unroll
+          for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+            for (int kk = 0; kk < HD / 16; ++kk) {
+              // a K step of 16 elements is +32 bytes within a swizzled row; the fifth step
+              // starts the second 64-column atom (hd = 128)
+              const uint32_t kstep = (kk % 4) * 2;
+              mma_ss(tmem + 16u * j, dK + j * (L::kTileBytes >> 4) + (kk / 4) * (L::kSubBytes >> 4) + kstep,
+                     dQ + (kk / 4) * (L::kQColBytes >> 4) + kstep, idesc_s, kk > 0 ? 1u : 0u);
+            }
+          mma_commit(s_done);
+        }
+        __syncwarp();
+        last_s = c - c0;
+      }
+    }
+    ok = ok && mbar_wait(s_done, par, ctl);
+    // The scores are done with the K buffer: the next chunk's K tiles load meanwhile.
+    if (t == 0 && ok && c + 1 < c1) {
+      load_kv(&mk, sK, full_k, c + 1);
+      k_loaded = c + 2;
+    }
+
+    // ---- chunk softmax: thread t owns key key0 + 128 j + t of tile j ----
+    float x[L::kSub][GV];
+    {
+      uint32_t sr[16 * L::kSub];
       tc_fence_after();
       const uint32_t tl = tmem + (static_cast<uint32_t>(warp * 32) << 16);
       if constexpr (L::kSub == 1) {
         tmem_ld_x16(tl, sr);
       } else {
 #pragma unroll
-        for (int c = 0; c < 16 * L::kSub; c += 32) tmem_ld_x32(tl + c, sr + c);
+        for (int i = 0; i < 16 * L::kSub; i += 32) tmem_ld_x32(tl + i, sr + i);
       }
       tmem_wait_ld();
       reg_fence<16 * L::kSub>(sr);
-    } else {
 #pragma unroll
-      for (int i = 0; i < 16 * L::kSub; ++i) sr[i] = 0u;
+      for (int j = 0; j < L::kSub; ++j)
+#pragma unroll
+        for (int r = 0; r < GV; ++r) x[j][r] = __uint_as_float(sr[16 * j + r]) * scale_log2;
     }
+    bool valid[L::kSub];
 #pragma unroll
-    for (int j = 0; j < L::kSub; ++j)
+    for (int j = 0; j < L::kSub; ++j) valid[j] = key0 + j * kTileRows + t < T;
 #pragma unroll
-      for (int r = 0; r < GV; ++r) x[j][r] = __uint_as_float(sr[16 * j + r]) * scale_log2;
-  }
-  bool valid[L::kSub];
+    for (int r = 0; r < GV; ++r) {
+      float mx = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < L::kSub; ++j) valid[j] = key0 + j * kTileRows + t < T;
+      for (int j = 0; j < L::kSub; ++j)
+        if (valid[j]) mx = fmaxf(mx, x[j][r]);
 #pragma unroll
-  for (int r = 0; r < GV; ++r) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < L::kSub; ++j)
-      if (valid[j]) m = fmaxf(m, x[j][r]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    if (lane == 0) red_max[warp * 16 + r] = m;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int r = 0; r < GV; ++r) {
-    // finite for r < group: every chunk holds at least one key below T
-    const float M = fmaxf(fmaxf(red_max[r], red_max[16 + r]), fmaxf(red_max[32 + r], red_max[48 + r]));
-    float l = 0.f;
-#pragma unroll
-    for (int j = 0; j < L::kSub; ++j) {
-      const float p = (valid[j] && r < group) ? ex2_approx(x[j][r] - M) : 0.f;
-      const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-      l += __bfloat162float(pb);
-      // P^T row (j, r), key t: 64-key column t / 64, 16-byte chunk (t % 64) / 8 swizzled
-      const int n = j * G + r;
-      const uint32_t off = L::kQP + (t >> 6) * L::kPColBytes + n * 128 + (((((t & 63) >> 3) ^ (n & 7))) << 4) +
-                           (t & 7) * 2;
-      XATTN_DCHECK(off + 2 <= L::kQP + L::kPBytes, status);
-      *reinterpret_cast<__nv_bfloat16 *>(smem + off) = pb;
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane == 0) red_max[warp * 16 + r] = mx;
     }
+    __syncthreads();
+    float mc[GV];   // the chunk's maximum per head
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-    if (lane == 0) red_sum[warp * 16 + r] = l;
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-
-  // ---- P V: O^T (+)= [V tiles as M = 128 rows (j, d)] x [P^T, N = kSub x G] ----
-  if (warp == 0 && ok) {
-    ok = dec_warp_wait(full_v, 0, ctl);
-    if (ok) {
-      tc_fence_after();
-      constexpr uint32_t idesc_pv = idesc_bf16_f32(128, L::kNpv, true, false);
-      // MN-major A: LBO = distance between 64-element atoms along M (the next tile, or
-      // the second sub-tile at hd = 128), SBO = 8 key rows; a K step is 16 key rows.
-      const uint64_t dV = smem_desc(sV, L::kSubBytes, 8 * L::kAtomBytes, L::kSwizzle);
-      const uint64_t dP = smem_desc(sQP, 16, 1024, kSwizzle128);
-      if (elect_one()) {
+    for (int r = 0; r < GV; ++r) {
+      // finite for r < group: every chunk holds at least one key below T
+      mc[r] = fmaxf(fmaxf(red_max[r], red_max[16 + r]), fmaxf(red_max[32 + r], red_max[48 + r]));
+      float l = 0.f;
 #pragma unroll
-        for (int kk = 0; kk < kTileRows / 16; ++kk)
-          mma_ss(tmem + L::kTmemO, dV + kk * ((16 * L::kAtomBytes) >> 4),
-                 dP + (kk / 4) * (L::kPColBytes >> 4) + (kk % 4) * 2, idesc_pv, kk > 0 ? 1u : 0u);
-        mma_commit(o_done);
+      for (int j = 0; j < L::kSub; ++j) {
+        const float p = (valid[j] && r < group) ? ex2_approx(x[j][r] - mc[r]) : 0.f;
+        const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+        l += __bfloat162float(pb);
+        // P^T row (j, r), key t: 64-key column t / 64, 16-byte chunk (t % 64) / 8 swizzled
+        const int n = j * G + r;
+        const uint32_t off = kPOff + (t >> 6) * L::kPColBytes + n * 128 + ((((t & 63) >> 3) ^ (n & 7)) << 4) +
+                             (t & 7) * 2;
+        XATTN_DCHECK(off + 2 <= kPOff + L::kPBytes, status);
+        *reinterpret_cast<__nv_bfloat16 *>(smem + L::kQP + off) = pb;
       }
-      __syncwarp();
-      issued_o = true;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+      if (lane == 0) red_sum[warp * 16 + r] = l;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- P V: O^T = [V tiles as M = 128 rows (j, d)] x [P^T, N = kSub x G] ----
+    if (warp == 0 && ok) {
+      ok = dec_warp_wait(full_v, par, ctl);
+      if (ok) {
+        tc_fence_after();
+        // MN-major A: LBO = distance between 64-element atoms along M (the next tile, or
+        // the second sub-tile at hd = 128), SBO = 8 key rows; a K step is 16 key rows.
+        const uint64_t dV = smem_desc(sV, L::kSubBytes, 8 * L::kAtomBytes, L::kSwizzle);
+        const uint64_t dP = smem_desc(sP, 16, 1024, kSwizzle128);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kTileRows / 16; ++kk)
+            mma_ss(tmem + L::kTmemO, dV + kk * ((16 * L::kAtomBytes) >> 4),
+                   dP + (kk / 4) * (L::kPColBytes >> 4) + (kk % 4) * 2, idesc_pv, kk > 0 ? 1u : 0u);
+          mma_commit(o_done);
+        }
+        __syncwarp();
+        last_o = c - c0;
+      }
+    }
+    ok = ok && mbar_wait(o_done, par, ctl);
+    // P V is done with the V buffer: the next chunk's V tiles load meanwhile.
+    if (t == 0 && ok && c + 1 < c1) {
+      load_kv(&mv, sV, full_v, c + 1);
+      v_loaded = c + 2;
+    }
+
+    // ---- merge the chunk: rescale to the new running maximum and add ----
+    {
+      tc_fence_after();
+      uint32_t orow[GV < 8 ? 8 : GV];
+      const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + L::kTmemO + jrow * G;
+      if constexpr (GV == 16) {
+        tmem_ld_x16(ta, orow);
+      } else {
+        tmem_ld_x8(ta, orow);
+      }
+      tmem_wait_ld();
+      reg_fence<(GV < 8 ? 8 : GV)>(orow);
+#pragma unroll
+      for (int r = 0; r < GV; ++r) {
+        const float lc = (red_sum[r] + red_sum[16 + r]) + (red_sum[32 + r] + red_sum[48 + r]);
+        const float mn = fmaxf(Mh[r], mc[r]);
+        const float a_old = ex2_approx(Mh[r] - mn), a_new = ex2_approx(mc[r] - mn);   // 2^-inf = 0
+        acc[r] = acc[r] * a_old + __uint_as_float(orow[r]) * a_new;
+        Lh[r] = Lh[r] * a_old + lc * a_new;
+        Mh[r] = mn;
+      }
+    }
+    // Every thread has read red_max / red_sum and the O^T rows before the next chunk
+    // overwrites them; on a failed wait anywhere all threads leave the loop together.
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) {
+      ok = false;
+      break;
     }
   }
-  ok = ok && mbar_wait(o_done, 0, ctl);
 
-  // ---- epilogue: row m = 32 warp + lane of O^T is (tile j, element d) ----
-  float *acc = reinterpret_cast<float *>(smem + L::kK);   // [kSub][G][HD]; K is no longer read
+  // ---- the run's result: the tiles' partials summed through shared memory ----
+  float *part = reinterpret_cast<float *>(smem + L::kK);   // [kSub][G][HD]; K is no longer read
+  float *stat = red_max;                                   // [0, 16): M, [16, 32): L per head
   if (ok) {
-    tc_fence_after();
-    const int m = warp * 32 + lane;
-    const int j = m / HD, d = m % HD;
-    uint32_t orow[GV < 8 ? 8 : GV];
-    const uint32_t ta = tmem + (static_cast<uint32_t>(warp * 32) << 16) + L::kTmemO + j * G;
-    if constexpr (GV == 16) {
-      tmem_ld_x16(ta, orow);
-    } else {
-      tmem_ld_x8(ta, orow);
-    }
-    tmem_wait_ld();
-    reg_fence<(GV < 8 ? 8 : GV)>(orow);
-    XATTN_DCHECK(((j + 1) * G) * HD <= L::kSub * G * HD && d < HD, status);
+    XATTN_DCHECK(((jrow + 1) * G) * HD <= L::kSub * G * HD && drow < HD, status);
 #pragma unroll
-    for (int r = 0; r < GV; ++r) acc[(j * G + r) * HD + d] = __uint_as_float(orow[r]);
+    for (int r = 0; r < GV; ++r) part[(jrow * G + r) * HD + drow] = acc[r];
+    if (t == 0) {
+#pragma unroll
+      for (int r = 0; r < GV; ++r) stat[r] = Mh[r], stat[16 + r] = Lh[r];
+    }
   }
   __syncthreads();
-  const size_t rec = (static_cast<size_t>(bk) * chunks + chunk) * group;   // [B, nkv, chunks, group]
   if (ok) {
+    const size_t h0 = static_cast<size_t>(b) * nh + static_cast<size_t>(kvh) * group;
+    const size_t rec0 = (static_cast<size_t>(bk) * nsplit + split) * group;   // records [B, nkv, nsplit, group]
     for (int e = t; e < group * HD; e += kDecThreads) {
       const int r = e / HD, d = e % HD;
       float a = 0.f;
 #pragma unroll
-      for (int j = 0; j < L::kSub; ++j) a += acc[(j * G + r) * HD + d];
-      XATTN_DCHECK((rec + r + 1) * HD <= static_cast<size_t>(B) * nh * chunks * HD, status);
-      ws_o[(rec + r) * HD + d] = a;
+      for (int j = 0; j < L::kSub; ++j) a += part[(j * G + r) * HD + d];
+      if (nsplit == 1) {
+        o[(h0 + r) * HD + d] = __float2bfloat16_rn(a / stat[16 + r]);
+      } else {
+        XATTN_DCHECK((rec0 + r + 1) * HD <= static_cast<size_t>(B) * nh * nsplit * HD, status);
+        ws_o[(rec0 + r) * HD + d] = a;
+      }
     }
     if (t < group) {
-      const float M = fmaxf(fmaxf(red_max[t], red_max[16 + t]), fmaxf(red_max[32 + t], red_max[48 + t]));
-      const float l = (red_sum[t] + red_sum[16 + t]) + (red_sum[32 + t] + red_sum[48 + t]);
-      ws_ml[2 * (rec + t)] = M;
-      ws_ml[2 * (rec + t) + 1] = l;
+      if (nsplit == 1) {
+        lse[h0 + t] = (stat[t] + __log2f(stat[16 + t])) * kLn2;
+      } else {
+        ws_ml[2 * (rec0 + t)] = stat[t];
+        ws_ml[2 * (rec0 + t) + 1] = stat[16 + t];
+      }
     }
   }
 
   // ---- teardown: let copies and products in flight land, then free TMEM ----
-  if (warp == 0) {
-    mbar_drain(full_k, 0, ctl);
-    mbar_drain(full_v, 0, ctl);
-    if (issued_s) mbar_drain(s_done, 0, ctl);
-    if (issued_o) mbar_drain(o_done, 0, ctl);
+  if (t == 0) {
+    mbar_drain(full_k, static_cast<uint32_t>((k_loaded - 1 - c0) & 1), ctl);
+    mbar_drain(full_v, static_cast<uint32_t>((v_loaded - 1 - c0) & 1), ctl);
+    if (last_s >= 0) mbar_drain(s_done, static_cast<uint32_t>(last_s & 1), ctl);
+    if (last_o >= 0) mbar_drain(o_done, static_cast<uint32_t>(last_o & 1), ctl);
   }
   tc_fence_before();
   __syncthreads();
@@ -402,21 +507,42 @@ cudaError_t launch_decode_hd(const CUtensorMap &mk, const CUtensorMap &mv, const
                              void *workspace, int *status, uint64_t timeout_ns, cudaStream_t stream) {
   using L = DecLayout<HD, G>;
   const int chunks = (T + L::kChunk - 1) / L::kChunk;
+  int dev = 0, sms = 0;
+  cudaError_t err;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+  const int nsplit = decode_nsplit(B * nkv, chunks, decode_ctas_per_sm<HD, G>() * sms, sms);
   float *ws_o = static_cast<float *>(workspace);
-  float *ws_ml = ws_o + static_cast<size_t>(B) * nh * chunks * HD;
-  cudaError_t err = cudaFuncSetAttribute(decode_partial_kernel<HD, G, GV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(L::kDynBytes));
-  if (err != cudaSuccess) return err;
-  const unsigned grid1 = static_cast<unsigned>(static_cast<long long>(B) * nkv * chunks);
-  err = launch_pdl(decode_partial_kernel<HD, G, GV>, dim3(grid1), kDecThreads, L::kDynBytes, stream, mk, mv, q, ws_o,
-                   ws_ml, B, T, nh, nkv, scale * kLog2e, status, static_cast<unsigned long long>(timeout_ns));
-  if (err != cudaSuccess) return err;
+  float *ws_ml = ws_o + static_cast<size_t>(B) * nh * nsplit * HD;
+  if ((err = cudaFuncSetAttribute(decode_partial_kernel<HD, G, GV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(L::kDynBytes))) != cudaSuccess)
+    return err;
+  const unsigned grid1 = static_cast<unsigned>(static_cast<long long>(B) * nkv * nsplit);
+  err = launch_pdl(decode_partial_kernel<HD, G, GV>, dim3(grid1), kDecThreads, L::kDynBytes, stream, mk, mv, q,
+                   ws_o, ws_ml, o, lse, B, T, nh, nkv, nsplit, scale * kLog2e, status,
+                   static_cast<unsigned long long>(timeout_ns));
+  if (err != cudaSuccess || nsplit == 1) return err;
   const unsigned blocks = static_cast<unsigned>((static_cast<long long>(B) * nh * 32 + 127) / 128);
   return launch_pdl(decode_combine_kernel<HD>, blocks, 128, 0, stream, static_cast<const float *>(ws_o),
-                    static_cast<const float *>(ws_ml), o, lse, B, nh, nkv, chunks);
+                    static_cast<const float *>(ws_ml), o, lse, B, nh, nkv, nsplit);
+}
+
+template <int HD, int G>
+int decode_runs_hd(int B, int T, int nkv, int sms) {
+  using L = DecLayout<HD, G>;
+  const int chunks = (T + L::kChunk - 1) / L::kChunk;
+  return decode_nsplit(B * nkv, chunks, decode_ctas_per_sm<HD, G>() * sms, sms);
 }
 
 }  // namespace
+
+int decode_runs(int B, int T, int nh, int nkv, int hd, int sms) {
+  const int group = nh / nkv;
+  if (hd == 32) return group <= 4 ? decode_runs_hd<32, 4>(B, T, nkv, sms)
+                                  : (group <= 8 ? decode_runs_hd<32, 8>(B, T, nkv, sms) : decode_runs_hd<32, 16>(B, T, nkv, sms));
+  if (hd == 64) return group <= 8 ? decode_runs_hd<64, 8>(B, T, nkv, sms) : decode_runs_hd<64, 16>(B, T, nkv, sms);
+  return decode_runs_hd<128, 16>(B, T, nkv, sms);
+}
 
 cudaError_t launch_decode_bf16(const CUtensorMap &mk, const CUtensorMap &mv, const __nv_bfloat16 *q,
                                __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, int hd, float scale,

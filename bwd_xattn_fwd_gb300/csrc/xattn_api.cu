@@ -238,6 +238,14 @@ int xattn_bwd_dq_mode(int S, int nh, int nkv, int hd, int deterministic) {
   return bwd_resident_dq_ok(S, nh, nkv, hd) ? XATTN_BWD_RESIDENT_DQ : XATTN_BWD_QUERY_DQ;
 }
 
+int xattn_decode_runs(int B, int T, int nh, int nkv, int hd, int num_sms) {
+  if (B <= 0 || T <= 0 || nh <= 0 || nkv <= 0 || nh % nkv != 0 || num_sms <= 0) return -1;
+  if (nh / nkv > kMaxDecodeGroup || (hd != 32 && hd != 64 && hd != 128)) return -1;
+  const long long chunks = (static_cast<long long>(T) + decode_chunk_keys(hd) - 1) / decode_chunk_keys(hd);
+  if (static_cast<long long>(B) * nkv * chunks > 0x7fffffffLL) return -1;
+  return decode_runs(B, T, nh, nkv, hd, num_sms);
+}
+
 size_t xattn_bwd_workspace_bytes(int B, int S, int nh, int hd) {
   if (B <= 0 || S <= 0 || nh <= 0 || hd <= 0) return 0;
   return bwd_workspace_bytes(B, S, nh, hd, true);

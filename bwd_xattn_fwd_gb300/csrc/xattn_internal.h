@@ -104,6 +104,9 @@ cudaError_t launch_bwd_dq_bf16(const CUtensorMap &mq, const CUtensorMap &mk, con
 constexpr int kMaxDecodeGroup = 16;
 int decode_chunk_keys(int hd);
 size_t decode_workspace_bytes(int B, int T, int nh, int hd);
+// Key runs per (batch, kv head) that launch_decode_bf16 uses on a GPU with `sms` SMs
+// (1: one CTA streams a whole cache and writes O; more: per-run records and a combine).
+int decode_runs(int B, int T, int nh, int nkv, int hd, int sms);
 cudaError_t launch_decode_bf16(const CUtensorMap &mk, const CUtensorMap &mv, const __nv_bfloat16 *q,
                                __nv_bfloat16 *o, float *lse, int B, int T, int nh, int nkv, int hd, float scale,
                                void *workspace, int *status, uint64_t timeout_ns, cudaStream_t stream);

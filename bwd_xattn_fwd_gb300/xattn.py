@@ -79,6 +79,8 @@ _lib.xattn_bwd_workspace_bytes.argtypes = [_i, _i, _i, _i]
 _lib.xattn_bwd_workspace_bytes.restype = ctypes.c_size_t
 _lib.xattn_bwd_dq_mode.argtypes = [_i, _i, _i, _i, _i]
 _lib.xattn_bwd_dq_mode.restype = ctypes.c_int
+_lib.xattn_decode_runs.argtypes = [_i, _i, _i, _i, _i, _i]
+_lib.xattn_decode_runs.restype = ctypes.c_int
 _lib.xattn_build_flags.argtypes = []
 _lib.xattn_build_flags.restype = ctypes.c_int
 _lib.xattn_selftest_bounds_check.argtypes = [_vp]
@@ -151,6 +153,11 @@ NOALLOC_SCRATCH_BYTES = 64 * 1024 * 1024   # XATTN_NOALLOC_SCRATCH_BYTES in xatt
 
 def xattn_bwd_workspace_bytes(B, S, nh, hd) -> int:
     return int(_lib.xattn_bwd_workspace_bytes(B, S, nh, hd))
+
+
+def xattn_decode_runs(B, T, nh, nkv, hd, num_sms) -> int:
+    """Key runs per (sequence, kv head) that xattn_decode uses on num_sms SMs (-1: rejected)."""
+    return int(_lib.xattn_decode_runs(B, T, nh, nkv, hd, num_sms))
 
 
 def xattn_bwd_dq_mode(S, nh, nkv, hd, deterministic=False) -> int:

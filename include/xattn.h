@@ -221,14 +221,27 @@ xattn_status xattn_bwd_f32(const float *q, const float *k, const float *v, const
  * aligned, lse 4-byte aligned.
  * Arithmetic: tensor-core products on the bf16 inputs with fp32 accumulation (the
  * scores q . k, and the sum over keys of p v with the probabilities p rounded to bf16,
- * as in xattn_fwd); softmax statistics in fp32; o rounded to nearest even. Scratch
- * (B * nh * ceil(T / C) * (hd + 2) floats: per C-key chunk the maximum, sum and
- * unnormalised output of each query head) is taken with cudaMallocAsync on `stream` and
- * released with cudaFreeAsync; nothing else is allocated. The result is bit-for-bit
- * reproducible (fixed reduction order).
+ * as in xattn_fwd); softmax statistics in fp32, merged across chunks online; o rounded
+ * to nearest even. Scratch (B * nh * ceil(T / C) * (hd + 2) floats, an upper bound on the
+ * per-run records that xattn_decode_runs describes) is taken with cudaMallocAsync on
+ * `stream` and released with cudaFreeAsync; nothing else is allocated. The result is
+ * bit-for-bit reproducible (fixed reduction order for given sizes and SM count).
  */
 xattn_status xattn_decode(const void *q, const void *k_cache, const void *v_cache, int B, int T,
                           int nh, int nkv, int hd, float scale, void *o, float *lse, void *stream);
+
+/*
+ * How xattn_decode splits the caches on a GPU with num_sms SMs; no device work, -1 for
+ * sizes xattn_decode rejects (or num_sms <= 0). The result R is the number of key runs per
+ * (sequence, kv head): each run is one CTA that streams its C-key chunks through shared
+ * memory and merges them online.
+ *   R == 1  one kernel: a CTA per (sequence, kv head) writes o and lse itself; chosen when
+ *           the B * nkv pairs fill the SMs in one wave of resident CTAs;
+ *   R > 1   each run writes (maximum, sum, unnormalised output) per query head to the
+ *           scratch and a second kernel merges the runs; chosen for short batches, to
+ *           give the GPU enough CTAs, and for batches beyond one wave.
+ */
+int xattn_decode_runs(int B, int T, int nh, int nkv, int hd, int num_sms);
 
 const char *xattn_status_string(xattn_status status);
 

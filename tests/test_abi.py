@@ -197,6 +197,24 @@ def test_selftest_limit_checks(lib):
     assert f(20 * 10**9, None) == 2
 
 
+def test_decode_runs(lib):
+    """How the decode splits the caches (a pure function of the sizes and the SM count)."""
+    f = lib.xattn_decode_runs
+    f.restype = ctypes.c_int
+    # 64 sequences x 4 kv heads fill 152 SMs in one wave: one CTA per (sequence, kv head)
+    assert f(64, 4096, 16, 4, 64, 152) == 1
+    assert f(40, 1000, 16, 4, 128, 152) == 1
+    # 32 pairs: as many runs as fill one wave, each run non-empty (12 chunks of 256 keys)
+    assert f(8, 3000, 16, 4, 64, 152) == 12
+    assert f(1, 1, 2, 1, 64, 152) == 1
+    # more pairs than resident CTAs: a count between 1 and the chunk count
+    r = f(128, 700, 32, 8, 64, 152)
+    assert 1 <= r <= 3
+    for bad in [(0, 10, 4, 2, 64, 152), (1, 10, 6, 4, 64, 152), (1, 10, 4, 2, 48, 152), (1, 10, 34, 2, 64, 152),
+                (1, 10, 4, 2, 64, 0)]:
+        assert f(*bad) == -1, bad
+
+
 def test_bwd_dq_mode(lib):
     """The backward that xattn_bwd / xattn_bwd_deterministic pick, by sizes: xattn_bwd runs
     the fused-dQ backward at hd 32 and 64 and the query-stationary one at hd 128; the

@@ -52,6 +52,12 @@ SHAPES = [
     (1, 5000, 4, 2, 128),
     (2, 600, 16, 1, 32),
     (2, 1300, 16, 2, 64),
+    # one CTA per (sequence, kv head) streaming a ragged cache (no combine), at each head
+    # dim; and more (sequence, kv head) pairs than resident CTAs (several waves of runs)
+    (40, 1000, 16, 4, 64),
+    (40, 1000, 16, 4, 128),
+    (40, 1500, 8, 4, 32),
+    (128, 700, 32, 8, 64),
 ]
 
 
@@ -69,8 +75,13 @@ def test_decode_scales(scale):
 
 
 def test_decode_workload():
-    """The full decode workload (64 sequences x 4096 cached positions), every sequence."""
+    """The full decode workload (64 sequences x 4096 cached positions), every sequence; on
+    a GB300 (152 SMs) it runs as one CTA per (sequence, kv head)."""
+    from bwd_xattn_fwd_gb300 import xattn
     w = W.DECODE_WORKLOADS["decode"]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms >= 128:
+        assert xattn.xattn_decode_runs(w.B, w.T, w.nh, w.nkv, w.hd, sms) == 1
     eo, el = _check(W.make_decode_inputs(w), w.scale, "decode workload")
     print("decode workload: o", eo, "lse", el)
 
