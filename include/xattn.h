@@ -238,8 +238,11 @@ xattn_status xattn_decode(const void *q, const void *k_cache, const void *v_cach
  *   R == 1  one kernel: a CTA per (sequence, kv head) writes o and lse itself; chosen when
  *           the B * nkv pairs fill the SMs in one wave of resident CTAs;
  *   R > 1   each run writes (maximum, sum, unnormalised output) per query head to the
- *           scratch and a second kernel merges the runs; chosen for short batches, to
- *           give the GPU enough CTAs, and for batches beyond one wave.
+ *           scratch and a second kernel merges the runs; chosen when B * nkv is below the
+ *           SM count (more CTAs for the GPU), and for batches beyond one wave where a split
+ *           shortens the waves of CTAs.
+ * The split depends only on these sizes and num_sms, so results are reproducible on one
+ * GPU model.
  */
 int xattn_decode_runs(int B, int T, int nh, int nkv, int hd, int num_sms);
 
